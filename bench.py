@@ -1,0 +1,396 @@
+"""Benchmark: exact attention forward on the GPT-2-medium-shaped prefill, plus split-KV decode.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = the whole forward path over one batch: fa_fwd non-causal and fa_fwd causal on
+B=64, H=16, N=Nk=1024, d=dv=64 (bf16 inputs iid N(0,1), seed 0; bf16 O and fp32 LSE).
+FLOPs follow the pages' count, 4*N*Nk*d per head (2*N*Nk*d for Q K^T plus 2*N*Nk*dv for
+P V), halved for causal.  Inputs (403 MB) are larger than the 129 MB L2, so no flush is
+needed between iterations.  The split-KV decode (B=16, H=32, d=128, lengths uniform in
+[1024, 32768], 4.4 GB of K/V read per call) is timed in the same run and reported under
+"decode" in GB/s of algorithmic K/V bytes.
+
+Timing: CUDA events recorded on the launching stream around every kernel launch, W
+untimed warm-up steps, a barrier and a device synchronisation on both sides of exactly K
+timed steps, max over ranks.  SM clocks and throttle reasons are sampled with nvidia-smi
+during the timed region.  Under torchrun every rank runs the same per-GPU work on its own
+GPU (replicas: the path has no data exchange), so scaling is weak.
+
+--impl reference times the CPU FP64 oracle on the host cores instead (each step a bounded
+sample of two (b, h) slices in each causal mode of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fa_inputs import attention_inputs, decode_inputs, sample_slices  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s (% of BF16 peak); decode KV GB/s (% of HBM peak)"
+UNIT = "TFLOP/s"
+FWD = dict(B=64, H=16, N=1024, Nk=1024, d=64)
+DEC = dict(B=16, H=32, Nk_max=32768, d=128, lo=1024, hi=32768)
+WORKLOAD = "GPT-2-medium-shaped prefill B=64 H=16 N=Nk=1024 d=dv=64, fa_fwd non-causal + causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture, keyed by
+# the SHA-256 of the kernel source it was taken on; reported only while the source is unchanged.
+KERNEL_TRAFFIC = {}
+
+
+def fwd_flops(B, H, N, Nk, d, causal):
+    f = 4.0 * N * Nk * d * B * H
+    return f / 2 if causal else f
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("fa_fwd_kernel.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "exact_tiled_attention_fa_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ----------------------------------------------------------------------------------------------
+def oracle_sample(slices_per_mode, seed=0):
+    """Time the FP64 oracle on (b, h) slices of the forward workload, both causal modes.
+
+    Returns (seconds, flops, threads, description)."""
+    import oracle
+    oracle.build()
+    B, H, N, Nk, d = FWD["B"], FWD["H"], FWD["N"], FWD["Nk"], FWD["d"]
+    g = torch.Generator().manual_seed(seed)
+    picks = sample_slices(B * H, slices_per_mode, seed=1)
+    # only the picked heads are generated (same per-head distribution as the full batch)
+    q = torch.randn((len(picks), N, d), generator=g).to(torch.bfloat16)
+    k = torch.randn((len(picks), Nk, d), generator=g).to(torch.bfloat16)
+    v = torch.randn((len(picks), Nk, d), generator=g).to(torch.bfloat16)
+    threads = oracle.cores()
+    t0 = time.perf_counter()
+    for causal in (False, True):
+        oracle.attention(q, k, v, causal=causal, scale=1 / math.sqrt(d), threads=threads)
+    dt = time.perf_counter() - t0
+    flops = len(picks) * (fwd_flops(1, 1, N, Nk, d, False) + fwd_flops(1, 1, N, Nk, d, True))
+    desc = (f"{len(picks)} (b,h) slices of N=Nk=1024 d=64, non-causal + causal each, "
+            f"FP64 C oracle on {threads} threads")
+    return dt, flops, threads, desc
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    per_step = 2
+    for _ in range(args.warmup):
+        oracle_sample(per_step)
+    total_t, total_f, threads, desc = 0.0, 0.0, 1, ""
+    for _ in range(args.steps):
+        dt, fl, threads, desc = oracle_sample(per_step)
+        total_t += dt
+        total_f += fl
+    value = total_f / total_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD + " (bounded sample per step)", "sample_per_step": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import exact_tiled_attention_fa_gb300 as fa
+    fa.library()  # fails loudly if the CUDA library is not built
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    if args.decode_only:
+        decode = run_decode(fa, dev, stream, args, world)
+        if rank == 0:
+            print(json.dumps({"decode": decode}), flush=True)
+        return 0
+    B, H, N, Nk, d = FWD["B"], FWD["H"], FWD["N"], FWD["Nk"], FWD["d"]
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=rank, device=dev)
+    o_nc = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    o_c = torch.empty_like(o_nc)
+    l_nc = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    l_c = torch.empty_like(l_nc)
+    scale = 1.0 / math.sqrt(d)
+    f_nc, f_c = fwd_flops(B, H, N, Nk, d, False), fwd_flops(B, H, N, Nk, d, True)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fa.fwd(q, k, v, causal=False, scale=scale, out=o_nc, lse=l_nc)
+        if ev is not None:
+            ev[1].record(stream)
+            ev[2].record(stream)
+        fa.fwd(q, k, v, causal=True, scale=scale, out=o_c, lse=l_c)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    assert fa.get_device_error(dev) == fa.FA_OK
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(dev.index if dev.index is not None else 0)
+    sampler.start()
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    nc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    c_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    assert fa.get_device_error(dev) == fa.FA_OK
+    value = world * args.steps * (f_nc + f_c) / (total_ms / 1e3) / 1e12
+
+    # ---- end to end through the public API: pinned host inputs in, O and LSE back to the host
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(fa, dev, stream, args, world, (q, k, v), (o_nc, o_c, l_nc, l_c), scale, f_nc + f_c)
+
+    # ---- split-KV decode in the same run
+    decode = None
+    if not args.no_decode:
+        decode = run_decode(fa, dev, stream, args, world)
+
+    pk, pk_src = peaks()
+    peak = float(pk["bf16_tflops"])
+    achieved = f_nc / (nc_ms / 1e3) / 1e12
+    src_hash = kernel_source_hash()
+    traffic = KERNEL_TRAFFIC.get(src_hash)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "Nk": Nk, "d": d, "dv": d, "o_dtype": "bf16",
+                   "flops_per_step": f_nc + f_c, "l2": "inputs 403 MB > 129 MB L2 (no flush needed)",
+                   "parallelism": f"replicas x{world}"},
+        "kernels": {
+            "fa_fwd non-causal": {"ms": nc_ms, "tflops": achieved, "frac_of_peak": achieved / peak},
+            "fa_fwd causal": {"ms": c_ms, "tflops": f_c / (c_ms / 1e3) / 1e12,
+                              "frac_of_peak": f_c / (c_ms / 1e3) / 1e12 / peak},
+        },
+        "roofline": {"kernel": "fa_fwd_kernel<64, non-causal, bf16>", "bound": "tensor", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"{pk_src} bf16_tflops (burst; kernel timed in short launches)",
+                     "algorithmic_flops_per_launch": f_nc},
+        "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+    }
+    if decode is not None:
+        line["decode"] = decode
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl, threads, desc = oracle_sample(args.cpu_slices)
+        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(fa, dev, stream, args, world, inputs, outputs, scale, flops_per_step):
+    q, k, v = inputs
+    o_nc, o_c, l_nc, l_c = outputs
+    hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
+    ho_nc, ho_c = (torch.empty(o_nc.shape, dtype=o_nc.dtype).pin_memory() for _ in range(2))
+    hl_nc, hl_c = (torch.empty(l_nc.shape, dtype=l_nc.dtype).pin_memory() for _ in range(2))
+    dq, dk, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def e2e_step():
+        dq.copy_(hq, non_blocking=True)
+        dk.copy_(hk, non_blocking=True)
+        dv_.copy_(hv, non_blocking=True)
+        fa.fwd(dq, dk, dv_, causal=False, scale=scale, out=o_nc, lse=l_nc)
+        fa.fwd(dq, dk, dv_, causal=True, scale=scale, out=o_c, lse=l_c)
+        ho_nc.copy_(o_nc, non_blocking=True)
+        hl_nc.copy_(l_nc, non_blocking=True)
+        ho_c.copy_(o_c, non_blocking=True)
+        hl_c.copy_(l_c, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    n_e2e = args.steps
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+    d2h = sum(t.numel() * t.element_size() for t in (ho_nc, ho_c, hl_nc, hl_c))
+    e2e_value = world * n_e2e * flops_per_step / (e2e_ms / 1e3) / 1e12
+
+    return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def run_decode(fa, dev, stream, args, world):
+    B, H, Nk_max, d = DEC["B"], DEC["H"], DEC["Nk_max"], DEC["d"]
+    q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=0, lo=DEC["lo"], hi=DEC["hi"], device=dev)
+    lens_d = lens.to(dev)
+    n = fa.decode_default_splits(B, H, Nk_max, fa.num_sms(dev))
+    ws = torch.empty(fa.decode_workspace_size(B, H, d, n), dtype=torch.uint8, device=dev)
+    o = torch.empty((B, H, 1, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        fa.decode_splitkv(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
+    torch.cuda.synchronize(dev)
+    steps = max(args.steps // 4, 5)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(steps):
+        fa.decode_splitkv(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+    assert fa.get_device_error(dev) == fa.FA_OK
+    kv_bytes = sum(2 * H * int(n_b) * d * 2 for n_b in lens.tolist())
+    other = B * H * (d * 2 + d * 2 + 4)
+    pk, src = peaks()
+    gbs = world * (kv_bytes + other) / (ms / 1e3) / 1e9
+    return {"workload": "split-KV decode B=16 H=32 d=128, lengths U[1024,32768] (seed 0), bf16 O",
+            "n_splits": n, "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
+            "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode measurement")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-only", action="store_true", help="only the split-KV decode (profiling)")
+    ap.add_argument("--decode-batch", type=int, default=DEC["B"], help="decode batch (smaller cache for profiling)")
+    ap.add_argument("--cpu-slices", type=int, default=64)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    world, rank, local = dist_setup()
+    DEC["B"] = args.decode_batch
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,284 @@
+// fa_api.cu -- the C ABI (include/fa.h): argument checks, TMA tensor maps,
+// workspace layout and kernel dispatch.  Host code only.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa_internal.h"
+
+namespace fa {
+cudaError_t launch_fwd_32(const FwdParams& p, bool causal, fa_dtype o_dtype, cudaStream_t st);
+cudaError_t launch_fwd_64(const FwdParams& p, bool causal, fa_dtype o_dtype, cudaStream_t st);
+cudaError_t launch_fwd_128(const FwdParams& p, bool causal, fa_dtype o_dtype, cudaStream_t st);
+
+cudaError_t launch_fwd(const FwdParams& p, int d, bool causal, fa_dtype o_dtype, cudaStream_t st)
+{
+    switch (d) {
+    case 32: return launch_fwd_32(p, causal, o_dtype, st);
+    case 64: return launch_fwd_64(p, causal, o_dtype, st);
+    case 128: return launch_fwd_128(p, causal, o_dtype, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+}  // namespace fa
+
+namespace {
+
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+
+// Device status word: kernels record the first failure they detect here.
+__device__ int g_device_status;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_status_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+cudaError_t current_device(int* dev)
+{
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    if (*dev < 0 || *dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    return cudaSuccess;
+}
+
+// Device address of the status word on the current device (looked up once per device).
+cudaError_t status_word(int** out)
+{
+    int dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_status_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_device_status);
+        if (e != cudaSuccess) return e;
+        g_status_ptr[dev] = static_cast<int*>(p);
+    }
+    *out = g_status_ptr[dev];
+    return cudaSuccess;
+}
+
+cudaError_t sm_count(int* out)
+{
+    int dev;
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_num_sms[dev] == 0) {
+        e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    *out = g_num_sms[dev];
+    return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 tensor [BH][rows][d] as a 3-D tiled map with a {min(d,64), 128, 1} box,
+// swizzled so that each box row is one swizzle span (64 or 128 bytes).
+bool make_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d)
+{
+    auto enc = encode_fn();
+    if (enc == nullptr) return false;
+    const int cb = d < 64 ? d : 64;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(cb), static_cast<cuuint32_t>(fa::kBlockM), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     cb == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+bool head_ok(int d) { return d == 32 || d == 64 || d == 128; }
+bool dtype_ok(fa_dtype t) { return t == FA_BF16 || t == FA_F32; }
+bool scale_ok(float s) { return std::isfinite(s) && s > 0.f; }
+
+constexpr size_t kAlign = 256;
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fa_status_string(fa_status s)
+{
+    switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FA_ERR_CUDA: return "CUDA error";
+    case FA_ERR_WORKSPACE: return "workspace too small";
+    case FA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+    }
+}
+
+void fa_set_wait_timeout_ns(unsigned long long ns) { g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns); }
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int Nk,
+                 int d, int dv, int causal, float scale, fa_dtype o_dtype, void* stream)
+{
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || N <= 0 || Nk <= 0 || d <= 0 || dv <= 0) return FA_ERR_INVALID_ARG;
+    if ((causal != 0 && causal != 1) || !dtype_ok(o_dtype) || !scale_ok(scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+        return FA_ERR_INVALID_ARG;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long n_qtiles = (static_cast<long long>(N) + fa::kBlockM - 1) / fa::kBlockM;
+    if (BH * n_qtiles > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    if (!head_ok(d) || dv != d) return FA_ERR_UNSUPPORTED;
+
+    fa::FwdParams p;
+    if (!make_map(&p.tm_q, q, static_cast<int>(BH), N, d) || !make_map(&p.tm_k, k, static_cast<int>(BH), Nk, d) ||
+        !make_map(&p.tm_v, v, static_cast<int>(BH), Nk, dv))
+        return FA_ERR_CUDA;
+    int* status = nullptr;
+    if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
+    p.o = o;
+    p.lse = lse;
+    p.status = status;
+    p.BH = static_cast<int>(BH);
+    p.N = N;
+    p.Nk = Nk;
+    p.n_qtiles = static_cast<int>(n_qtiles);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit_ns = g_wait_ns.load();
+    cudaError_t e = fa::launch_fwd(p, d, causal != 0, o_dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+int fa_decode_default_splits(int B, int H, int Nk_max, int num_sms)
+{
+    if (B <= 0 || H <= 0 || Nk_max <= 0 || num_sms <= 0) return 0;
+    // Enough (b, h, split) items for several full waves of 4-warp CTAs, but no
+    // split shorter than a few key blocks.
+    const long long heads = static_cast<long long>(B) * H;
+    const long long target = 64LL * num_sms;
+    long long n = (target + heads - 1) / heads;
+    const long long max_n = (static_cast<long long>(Nk_max) + 4 * fa::kDecodeKeyBlock - 1) / (4 * fa::kDecodeKeyBlock);
+    if (n > max_n) n = max_n;
+    if (n < 1) n = 1;
+    return static_cast<int>(n);
+}
+
+size_t fa_decode_workspace_size(int B, int H, int dv, int n_splits)
+{
+    if (B <= 0 || H <= 0 || dv <= 0 || n_splits <= 0) return 0;
+    const size_t slots = static_cast<size_t>(B) * H * n_splits;
+    return round_up(slots * dv * sizeof(float), kAlign) + round_up(slots * sizeof(float), kAlign);
+}
+
+fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,
+                            float* lse, void* workspace, size_t ws_bytes, int B, int H, int Nk_max, int d, int dv,
+                            float scale, int n_splits, fa_dtype o_dtype, void* stream)
+{
+    if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seqlens_k == nullptr || o == nullptr ||
+        workspace == nullptr)
+        return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || Nk_max <= 0 || d <= 0 || dv <= 0 || n_splits < 0) return FA_ERR_INVALID_ARG;
+    if (!dtype_ok(o_dtype) || !scale_ok(scale)) return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
+        !aligned(lse, 4) || !aligned(seqlens_k, 4) || !aligned(workspace, kAlign))
+        return FA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * H > 0x7fffffffLL || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
+    if (!head_ok(d) || dv != d) return FA_ERR_UNSUPPORTED;
+
+    int n = n_splits;
+    if (n == 0) {
+        int sms = 0;
+        if (sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
+        n = fa_decode_default_splits(B, H, Nk_max, sms);
+    }
+    if (n > Nk_max) n = Nk_max;
+    if (ws_bytes < fa_decode_workspace_size(B, H, dv, n)) return FA_ERR_WORKSPACE;
+    // Fixed chunk per split, a whole number of key blocks; trailing splits may be empty.
+    long long chunk = (static_cast<long long>(Nk_max) + n - 1) / n;
+    chunk = (chunk + fa::kDecodeKeyBlock - 1) / fa::kDecodeKeyBlock * fa::kDecodeKeyBlock;
+    const int n_eff = static_cast<int>((Nk_max + chunk - 1) / chunk);
+
+    int* status = nullptr;
+    if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
+    fa::DecodeParams p;
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.seqlens = seqlens_k;
+    const size_t slots = static_cast<size_t>(B) * H * n_eff;
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(slots * dv * sizeof(float), kAlign));
+    p.o = o;
+    p.lse = lse;
+    p.status = status;
+    p.B = B;
+    p.H = H;
+    p.Nk_max = Nk_max;
+    p.n_splits = n_eff;
+    p.chunk = static_cast<int>(chunk);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    cudaError_t e = fa::launch_decode(p, d, o_dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int n_parts, int rows, int dv, void* o,
+                          float* lse, fa_dtype o_dtype, void* stream)
+{
+    if (o_parts == nullptr || lse_parts == nullptr || o == nullptr) return FA_ERR_INVALID_ARG;
+    if (n_parts <= 0 || rows <= 0 || dv <= 0 || dv > 512 || !dtype_ok(o_dtype)) return FA_ERR_INVALID_ARG;
+    if (!aligned(o_parts, 4) || !aligned(lse_parts, 4) || !aligned(o, 4) || !aligned(lse, 4))
+        return FA_ERR_INVALID_ARG;
+    int* status = nullptr;
+    if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
+    fa::MergeParams m{};
+    m.o_parts = o_parts;
+    m.lse_parts = lse_parts;
+    m.o_part_stride = static_cast<long long>(rows) * dv;
+    m.o_row_stride = dv;
+    m.lse_part_stride = rows;
+    m.lse_row_stride = 1;
+    m.n_parts = n_parts;
+    m.rows = rows;
+    m.dv = dv;
+    m.seqlens = nullptr;
+    m.o = o;
+    m.lse = lse;
+    m.status = status;
+    cudaError_t e = fa::launch_merge(m, o_dtype, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+fa_status fa_get_device_error(void* stream)
+{
+    int* status = nullptr;
+    if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int h = 0;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemcpyAsync(&h, status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return FA_ERR_CUDA;
+    return static_cast<fa_status>(h);
+}
+
+}  // extern "C"

@@ -1,0 +1,298 @@
+// fa_decode.cu -- split-KV single-query decode and the log-sum-exp combine.
+//
+// Algorithm: "flash_lab.py -- FlashAttention, flash-decoding and megakernel in
+// numpy", section 4 `split_kv_decode`.  With one query per (b, h) a query-tiled
+// forward would leave most of the GPU idle, so the keys are cut into splits;
+// each split computes its own normalised output o_s and log-sum-exp lse_s, and
+// a second kernel merges them (lse = log sum_s exp(lse_s),
+// o = sum_s exp(lse_s - lse) o_s -- the lse form of section 1 `merge_states`).
+//
+// The split kernel is bound by HBM bandwidth (one FMA per key element), so it
+// uses no tensor core: every lane streams 16-byte slices of key rows with
+// read-only, L1-bypassing loads, D/8 lanes cooperate on one key, eight loads of
+// K and eight of V are in flight per lane before any arithmetic, and the
+// softmax is online per warp in the base-2 domain.  Partial states go to
+// per-split slots (no atomics), so the result is deterministic.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "ptx.cuh"
+
+namespace fa {
+
+namespace {
+
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kDecWarps = 4;
+constexpr int kDecSteps = 8;  // 16-byte loads of K (and of V) in flight per lane
+
+__device__ __forceinline__ int clamp_len(int n, int hi, int* status)
+{
+    if (n < 0 || n > hi) {
+        atomicCAS(status, 0, FA_ERR_INVALID_ARG);
+        n = n < 0 ? 0 : hi;
+    }
+    return n;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+template <int D>
+struct DecCfg {
+    static constexpr int kLanesPerKey = D / 8;                    // 8 bf16 (16 B) per lane
+    static constexpr int kKeysPerStep = 32 / kLanesPerKey;        // keys one warp-wide load covers
+    static constexpr int kKeysPerIter = kDecSteps * kKeysPerStep; // keys per warp per iteration
+};
+
+// One CTA per (split, h, b).  Writes o_part / lse_part of a non-empty split.
+template <int D>
+__global__ void __launch_bounds__(kDecWarps * 32) fa_decode_split_kernel(const DecodeParams p)
+{
+    using C = DecCfg<D>;
+    const int s = blockIdx.x;
+    const int h = blockIdx.y;
+    const int b = blockIdx.z;
+    const int n = clamp_len(p.seqlens[b], p.Nk_max, p.status);
+    const int k0 = s * p.chunk;
+    if (k0 >= n) return;  // empty split: nothing to write, the combine skips it
+    const int k1 = min(n, k0 + p.chunk);
+    const size_t bh = static_cast<size_t>(b) * p.H + h;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int grp = lane / C::kLanesPerKey;  // which key of a step this lane serves
+    const int sub = lane % C::kLanesPerKey;  // which 8-element slice of the row
+
+    float q[8];
+    unpack8(*reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + bh * D + sub * 8), q);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] *= p.scale_log2;  // scores come out in the base-2 domain
+
+    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(p.k) + bh * p.Nk_max * D + sub * 8;
+    const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(p.v) + bh * p.Nk_max * D + sub * 8;
+
+    float m = -INFINITY;  // running max (warp-uniform)
+    float l = 0.f;        // this lane group's share of the running sum
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+
+    for (int base = k0 + warp * C::kKeysPerIter; base < k1; base += kDecWarps * C::kKeysPerIter) {
+        uint4 kr[kDecSteps], vr[kDecSteps];
+#pragma unroll
+        for (int t = 0; t < kDecSteps; ++t) {
+            const int key = base + t * C::kKeysPerStep + grp;
+            if (key < k1) {
+                kr[t] = ld_stream_v4(kb + static_cast<size_t>(key) * D);
+                vr[t] = ld_stream_v4(vb + static_cast<size_t>(key) * D);
+            } else {
+                kr[t] = make_uint4(0, 0, 0, 0);
+                vr[t] = make_uint4(0, 0, 0, 0);
+            }
+        }
+        float sc[kDecSteps];
+#pragma unroll
+        for (int t = 0; t < kDecSteps; ++t) {
+            float kf[8];
+            unpack8(kr[t], kf);
+            float x = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x = fmaf(q[i], kf[i], x);
+#pragma unroll
+            for (int o = C::kLanesPerKey / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            const int key = base + t * C::kKeysPerStep + grp;
+            sc[t] = key < k1 ? x : -INFINITY;
+        }
+        float bm = sc[0];
+#pragma unroll
+        for (int t = 1; t < kDecSteps; ++t) bm = fmaxf(bm, sc[t]);
+#pragma unroll
+        for (int o = C::kLanesPerKey; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+        // key `base` (group 0, step 0) is always visible, so bm is finite
+        const float m_new = fmaxf(m, bm);
+        const float alpha = ex2(m - m_new);  // 0 on the first block (m = -inf)
+        float ps = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] *= alpha;
+#pragma unroll
+        for (int t = 0; t < kDecSteps; ++t) {
+            const float pt = ex2(sc[t] - m_new);  // 0 for keys past the split
+            ps += pt;
+            float vf[8];
+            unpack8(vr[t], vf);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(pt, vf[i], acc[i]);
+        }
+        l = l * alpha + ps;
+        m = m_new;
+    }
+    // Sum the lane groups of the warp (they share m).
+#pragma unroll
+    for (int o = C::kLanesPerKey; o < 32; o <<= 1) {
+        l += __shfl_xor_sync(0xffffffffu, l, o);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+    }
+    // Merge the warps (each with its own max) through shared memory.
+    __shared__ float sm_m[kDecWarps], sm_l[kDecWarps];
+    __shared__ float sm_acc[kDecWarps][D];
+    if (lane == 0) {
+        sm_m[warp] = m;
+        sm_l[warp] = l;
+    }
+    if (grp == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sm_acc[warp][sub * 8 + i] = acc[i];
+    }
+    __syncthreads();
+    float M = sm_m[0];
+#pragma unroll
+    for (int w = 1; w < kDecWarps; ++w) M = fmaxf(M, sm_m[w]);
+    float f[kDecWarps];
+    float L = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+        f[w] = sm_m[w] == -INFINITY ? 0.f : ex2(sm_m[w] - M);
+        L += sm_l[w] * f[w];
+    }
+    const size_t slot = bh * p.n_splits + s;
+    for (int c = threadIdx.x; c < D; c += kDecWarps * 32) {
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) o = fmaf(sm_acc[w][c], f[w], o);
+        p.o_part[slot * D + c] = o / L;
+    }
+    if (threadIdx.x == 0) p.lse_part[slot] = (M + log2f(L)) * kLn2;
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_out(OutT* o, size_t i, float v);
+template <>
+__device__ __forceinline__ void store_out<float>(float* o, size_t i, float v)
+{
+    o[i] = v;
+}
+template <>
+__device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* o, size_t i, float v)
+{
+    o[i] = __float2bfloat16_rn(v);
+}
+
+constexpr int kMergeMaxPerLane = 16;  // dv <= 512
+
+// One warp per row: combine the row's valid parts.
+template <typename OutT>
+__global__ void __launch_bounds__(128) fa_merge_kernel(const MergeParams p)
+{
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * 4 + warp;
+    if (row >= p.rows) return;
+    int n_valid = p.n_parts;
+    if (p.seqlens != nullptr) {
+        const int n = clamp_len(p.seqlens[row / p.H], p.Nk_max, p.status);
+        n_valid = min(p.n_parts, (n + p.chunk - 1) / p.chunk);
+    }
+    const float* lse_row = p.lse_parts + static_cast<size_t>(row) * p.lse_row_stride;
+    const float* o_row = p.o_parts + static_cast<size_t>(row) * p.o_row_stride;
+
+    float M = -INFINITY;
+    for (int s = lane; s < n_valid; s += 32) M = fmaxf(M, lse_row[s * p.lse_part_stride]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    OutT* out = reinterpret_cast<OutT*>(p.o) + static_cast<size_t>(row) * p.dv;
+    if (M == -INFINITY) {  // every part empty: O = 0, LSE = -inf
+        for (int c = lane; c < p.dv; c += 32) store_out<OutT>(out, c, 0.f);
+        if (p.lse != nullptr && lane == 0) p.lse[row] = -INFINITY;
+        return;
+    }
+    float sum = 0.f;
+    for (int s = lane; s < n_valid; s += 32) {
+        const float x = lse_row[s * p.lse_part_stride];
+        if (x != -INFINITY) sum += ex2((x - M) * kLog2e);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float L = M + log2f(sum) * kLn2;
+
+    float acc[kMergeMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMergeMaxPerLane; ++i) acc[i] = 0.f;
+    for (int s = 0; s < n_valid; ++s) {
+        const float x = lse_row[s * p.lse_part_stride];
+        if (x == -INFINITY) continue;
+        const float w = ex2((x - L) * kLog2e);
+        const float* op = o_row + static_cast<size_t>(s) * p.o_part_stride;
+#pragma unroll
+        for (int i = 0; i < kMergeMaxPerLane; ++i) {
+            const int c = lane + 32 * i;
+            if (c < p.dv) acc[i] = fmaf(w, op[c], acc[i]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kMergeMaxPerLane; ++i) {
+        const int c = lane + 32 * i;
+        if (c < p.dv) store_out<OutT>(out, c, acc[i]);
+    }
+    if (p.lse != nullptr && lane == 0) p.lse[row] = L;
+}
+
+template <int D>
+cudaError_t launch_decode_d(const DecodeParams& p, fa_dtype o_dtype, cudaStream_t st)
+{
+    dim3 grid(p.n_splits, p.H, p.B);
+    fa_decode_split_kernel<D><<<grid, kDecWarps * 32, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    MergeParams m{};
+    m.o_parts = p.o_part;
+    m.lse_parts = p.lse_part;
+    m.o_part_stride = D;
+    m.o_row_stride = static_cast<long long>(p.n_splits) * D;
+    m.lse_part_stride = 1;
+    m.lse_row_stride = p.n_splits;
+    m.n_parts = p.n_splits;
+    m.rows = p.B * p.H;
+    m.dv = D;
+    m.seqlens = p.seqlens;
+    m.H = p.H;
+    m.chunk = p.chunk;
+    m.Nk_max = p.Nk_max;
+    m.o = p.o;
+    m.lse = p.lse;
+    m.status = p.status;
+    return launch_merge(m, o_dtype, st);
+}
+
+}  // namespace
+
+cudaError_t launch_merge(const MergeParams& p, fa_dtype o_dtype, cudaStream_t st)
+{
+    const unsigned grid = static_cast<unsigned>((p.rows + 3) / 4);
+    if (o_dtype == FA_F32)
+        fa_merge_kernel<float><<<grid, 128, 0, st>>>(p);
+    else
+        fa_merge_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeParams& p, int d, fa_dtype o_dtype, cudaStream_t st)
+{
+    switch (d) {
+    case 32: return launch_decode_d<32>(p, o_dtype, st);
+    case 64: return launch_decode_d<64>(p, o_dtype, st);
+    case 128: return launch_decode_d<128>(p, o_dtype, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace fa

@@ -1,0 +1,73 @@
+// fa_internal.h -- parameter blocks and launchers shared by the C-ABI layer and
+// the kernel translation units.  Not part of the public interface.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Forward kernel tile: 128 query rows (the tcgen05 M) x 128 keys.
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 128;
+
+struct FwdParams {
+    CUtensorMap tm_q;  // bf16 [B*H][N][d], box {min(d,64), 128, 1}
+    CUtensorMap tm_k;  // bf16 [B*H][Nk][d]
+    CUtensorMap tm_v;  // bf16 [B*H][Nk][dv]
+    void* o;           // [B*H][N][dv], bf16 or fp32
+    float* lse;        // [B*H][N] or nullptr
+    int* status;       // device status word
+    int BH, N, Nk;
+    int n_qtiles;       // ceil(N / 128)
+    float scale_log2;   // scale * log2(e)
+    unsigned long long wait_limit_ns;
+};
+
+// Launch the forward kernel for head size d (= dv), causal flag and output type.
+cudaError_t launch_fwd(const FwdParams& p, int d, bool causal, fa_dtype o_dtype, cudaStream_t st);
+
+// Decode: keys per block of the split kernel's inner loop; a split is a whole
+// number of such blocks.
+constexpr int kDecodeKeyBlock = 64;
+
+struct DecodeParams {
+    const void* q;        // bf16 [B*H][d]
+    const void* k;        // bf16 [B*H][Nk_max][d]
+    const void* v;        // bf16 [B*H][Nk_max][dv]
+    const int* seqlens;   // int32 [B]
+    float* o_part;        // fp32 [B*H][n_splits][dv]
+    float* lse_part;      // fp32 [B*H][n_splits]
+    void* o;              // [B*H][dv]
+    float* lse;           // [B*H] or nullptr
+    int* status;
+    int B, H, Nk_max, n_splits, chunk;
+    float scale_log2;
+};
+
+cudaError_t launch_decode(const DecodeParams& p, int d, fa_dtype o_dtype, cudaStream_t st);
+
+struct MergeParams {
+    const float* o_parts;   // partial outputs
+    const float* lse_parts; // partial log-sum-exps
+    long long o_part_stride, o_row_stride;     // elements between parts / rows of o_parts
+    long long lse_part_stride, lse_row_stride; // elements between parts / rows of lse_parts
+    int n_parts, rows, dv;
+    // optional per-row count of valid parts: ceil(clamp(seqlens[row / H]) / chunk)
+    const int* seqlens;
+    int H, chunk, Nk_max;
+    void* o;     // [rows][dv]
+    float* lse;  // [rows] or nullptr
+    int* status;
+};
+
+cudaError_t launch_merge(const MergeParams& p, fa_dtype o_dtype, cudaStream_t st);
+
+// Status word helpers (device side records the first failure only).
+enum : int { kStatusOk = 0 };
+
+}  // namespace fa

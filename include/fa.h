@@ -1,0 +1,163 @@
+/*
+ * fa.h -- C ABI of libfa: exact tiled attention on GB300 (sm_103a).
+ *
+ * Operations (page titles and sections they follow):
+ *   fa_fwd              exact attention forward, tiled with an online softmax
+ *                       ("flash_lab.py -- FlashAttention, flash-decoding and
+ *                       megakernel in numpy", section 3 `flash_fwd`, FlashAttention-2
+ *                       loop order; the value it reaches is section 2
+ *                       `standard_attention`).
+ *   fa_decode_splitkv   single-query decode split over the key/value length, each
+ *                       split's normalised output and log-sum-exp merged afterwards
+ *                       ("flash_lab.py", section 4 `split_kv_decode`).
+ *   fa_merge_states     the log-sum-exp combine of partial states on its own
+ *                       ("flash_lab.py", section 4 `split_kv_decode` combine, the
+ *                       lse form of section 1 `merge_states`).
+ *
+ * Conventions shared by every entry point:
+ *   - All tensors are dense, row-major, last dimension contiguous, in the layouts
+ *     stated per argument ([B,H,rows,cols]).  Device pointers must be 16-byte aligned.
+ *   - q, k, v and the caches are bf16.  Arithmetic is fp32 (tensor-core accumulation in
+ *     fp32; softmax statistics in fp32).  O is written as bf16 (FA_BF16) or fp32 (FA_F32);
+ *     LSE is always fp32, natural log, scale included:
+ *       LSE[i] = log sum_{visible j} exp(scale * q_i . k_j).
+ *   - Causal masking places query i at position Nk - N + i and key j at position j
+ *     ("02_flash_forward.py -- FlashAttention forward", demo 1; "flash_lab.py"
+ *     `_causal_mask`).  A query row with no visible key (only when causal and N > Nk)
+ *     gets O = 0 and LSE = -inf.
+ *   - Ownership: the caller allocates and owns every buffer; the library allocates
+ *     nothing.  Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and never synchronise, except
+ *     fa_get_device_error.
+ *   - Errors: every argument is checked on the host before any launch; a bad argument
+ *     returns a status and launches nothing.  A launch failure returns FA_ERR_CUDA.
+ *     Failures the device detects (a bounded wait that ran out, a sequence length out
+ *     of range) are recorded in a device status word read by fa_get_device_error.
+ *   - Supported head sizes: d = dv, d in {32, 64, 128}.  Other sizes return
+ *     FA_ERR_UNSUPPORTED.  Heads are independent: the number of key/value heads equals
+ *     the number of query heads.
+ */
+#ifndef FA_H
+#define FA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, misaligned pointer, bad enum */
+    FA_ERR_UNSUPPORTED = 2, /* valid arguments this build has no kernel for (head size) */
+    FA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    FA_ERR_WORKSPACE = 4,   /* caller-provided workspace smaller than required */
+    FA_ERR_TIMEOUT = 5      /* a device-side bounded wait ran out (kernel returned early) */
+} fa_status;
+
+typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
+
+/*
+ * Exact attention forward ("flash_lab.py" section 3, FlashAttention-2 order): for each
+ * (b, h) and query row i,
+ *   O[b,h,i,:] = sum_j softmax_j(scale * Q[b,h,i,:] . K[b,h,j,:]) V[b,h,j,:]
+ * over the visible keys j (all Nk keys, or j <= Nk - N + i when causal), and
+ *   lse[b,h,i] = log sum_j exp(scale * Q[b,h,i,:] . K[b,h,j,:]).
+ * The N x Nk score matrix never reaches memory.
+ *
+ *   q    bf16 [B, H, N,  d]        (device)
+ *   k    bf16 [B, H, Nk, d]        (device)
+ *   v    bf16 [B, H, Nk, dv]       (device)
+ *   o    o_dtype [B, H, N, dv]     (device, written)
+ *   lse  fp32 [B, H, N]            (device, written; may be NULL to skip it)
+ *   B, H, N, Nk >= 1; d = dv in {32, 64, 128}; causal 0 or 1; scale > 0 and finite
+ *   (1/sqrt(d) is the usual value).
+ * Returns FA_OK after enqueueing the kernel on `stream`.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int Nk, int d, int dv, int causal, float scale, fa_dtype o_dtype,
+                 void* stream);
+
+/*
+ * Split count fa_decode_splitkv uses when asked for n_splits = 0, for a device with
+ * `num_sms` streaming multiprocessors: enough splits of the longest sequence that the
+ * non-empty (b, h, split) work items fill the device several times over, each split at
+ * least one key block long.  Pure host function.  Returns 0 on invalid arguments.
+ */
+int fa_decode_default_splits(int B, int H, int Nk_max, int num_sms);
+
+/*
+ * Bytes of workspace fa_decode_splitkv needs for `n_splits` splits (n_splits >= 1):
+ * fp32 partial outputs [B, H, n_splits, dv] followed by fp32 partial log-sum-exps
+ * [B, H, n_splits], each region 256-byte aligned.  Returns 0 on invalid arguments.
+ */
+size_t fa_decode_workspace_size(int B, int H, int dv, int n_splits);
+
+/*
+ * Split-KV single-query decode ("flash_lab.py" section 4 `split_kv_decode`).  For each
+ * (b, h), the first seqlens_k[b] cached keys are cut into n_splits consecutive chunks of
+ * c = ceil(Nk_max / n_splits) keys (rounded up to the kernel's key block); split s covers
+ * keys [s*c, min((s+1)*c, seqlens_k[b])) and is empty when that range is.  Each non-empty
+ * split writes its normalised output o_s and lse_s to the workspace; a second kernel merges
+ *   lse = log sum_s exp(lse_s),  o = sum_s exp(lse_s - lse) o_s.
+ * The single query sits at position seqlens_k[b] - 1 and sees every cached key.
+ *
+ *   q          bf16 [B, H, 1, d]          (device)
+ *   k_cache    bf16 [B, H, Nk_max, d]     (device; rows past seqlens_k[b] are never read)
+ *   v_cache    bf16 [B, H, Nk_max, dv]    (device; idem)
+ *   seqlens_k  int32 [B]                  (device; 0 <= seqlens_k[b] <= Nk_max.  Values
+ *              outside that range are clamped into it and recorded as FA_ERR_INVALID_ARG in
+ *              the device status word.  A length of 0 gives O = 0, LSE = -inf.)
+ *   o          o_dtype [B, H, 1, dv]      (device, written)
+ *   lse        fp32 [B, H, 1]             (device, written; may be NULL)
+ *   workspace  device scratch of ws_bytes >= fa_decode_workspace_size(B, H, dv, n) bytes,
+ *              256-byte aligned, where n is n_splits or, for n_splits = 0, the automatic
+ *              count fa_decode_default_splits(B, H, Nk_max, <SMs of the current device>).
+ *   n_splits   >= 0; 0 picks the automatic count.  Values above Nk_max are reduced to it.
+ * Returns FA_ERR_WORKSPACE if ws_bytes is too small (nothing launched).
+ */
+fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache,
+                            const int* seqlens_k, void* o, float* lse, void* workspace,
+                            size_t ws_bytes, int B, int H, int Nk_max, int d, int dv, float scale,
+                            int n_splits, fa_dtype o_dtype, void* stream);
+
+/*
+ * Log-sum-exp combine of n_parts partial attention states per row ("flash_lab.py"
+ * section 4 combine; section 1 `merge_states`, where a state with lse = -inf is empty and
+ * gets weight 0):
+ *   lse[r] = log sum_p exp(lse_parts[p, r]),  o[r, :] = sum_p exp(lse_parts[p, r] - lse[r]) o_parts[p, r, :]
+ * A row whose every part is empty gets o = 0, lse = -inf.
+ *
+ *   o_parts    fp32 [n_parts, rows, dv]   (device)
+ *   lse_parts  fp32 [n_parts, rows]       (device)
+ *   o          o_dtype [rows, dv]         (device, written)
+ *   lse        fp32 [rows]                (device, written; may be NULL)
+ *   n_parts >= 1, rows >= 1, 1 <= dv <= 512.
+ */
+fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int n_parts, int rows,
+                          int dv, void* o, float* lse, fa_dtype o_dtype, void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the device status word of the current
+ * device: FA_OK if no kernel recorded a failure since the last call, else the first
+ * recorded status (FA_ERR_TIMEOUT, FA_ERR_INVALID_ARG).  FA_ERR_CUDA if the synchronisation
+ * itself failed.
+ */
+fa_status fa_get_device_error(void* stream);
+
+/*
+ * Upper bound, in nanoseconds of the GPU global timer, on every wait for a barrier inside
+ * the forward kernel (default 2e9).  When a wait runs out the kernel records FA_ERR_TIMEOUT,
+ * drains its own copies in flight, frees its tensor memory and returns.  0 restores the
+ * default.  Applies to launches made after the call.
+ */
+void fa_set_wait_timeout_ns(unsigned long long ns);
+
+/* Static description of a status code. */
+const char* fa_status_string(fa_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H */

@@ -1,0 +1,105 @@
+"""The C-ABI library builds, loads without a GPU, exports every declared symbol,
+and rejects bad arguments on the host before launching anything."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_tiled_attention_fa_gb300 as fa
+from exact_tiled_attention_fa_gb300 import build as fa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa.h")
+
+# A fake but 256-byte-aligned device address: argument checks reject the call before it is used.
+P = ctypes.c_void_p(0x10000000)
+NULL = ctypes.c_void_p(0)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    fa_build.build()
+    return fa.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"fa_fwd", "fa_decode_splitkv", "fa_merge_states", "fa_get_device_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _fwd(lib, q=P, k=P, v=P, o=P, lse=P, B=1, H=1, N=8, Nk=8, d=64, dv=64, causal=0, scale=0.125, odt=0):
+    return lib.fa_fwd(q, k, v, o, lse, B, H, N, Nk, d, dv, causal, scale, odt, NULL)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert _fwd(lib, q=NULL) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, o=NULL) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, B=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, N=-1) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, Nk=0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, causal=2) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, odt=7) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, q=ctypes.c_void_p(0x10000008)) == fa.FA_ERR_INVALID_ARG  # not 16-byte aligned
+    assert _fwd(lib, lse=ctypes.c_void_p(0x10000002)) == fa.FA_ERR_INVALID_ARG
+    assert _fwd(lib, d=48, dv=48) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=64, dv=128) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, d=256, dv=256) == fa.FA_ERR_UNSUPPORTED
+
+
+def _dec(lib, ws_bytes=1 << 20, n_splits=4, q=P, ws=P, B=2, H=2, Nk=1000, d=128, dv=128, scale=0.1, odt=0):
+    return lib.fa_decode_splitkv(q, P, P, P, P, P, ws, ws_bytes, B, H, Nk, d, dv, scale, n_splits, odt, NULL)
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert _dec(lib, q=NULL) == fa.FA_ERR_INVALID_ARG
+    assert _dec(lib, ws=NULL) == fa.FA_ERR_INVALID_ARG
+    assert _dec(lib, ws=ctypes.c_void_p(0x10000010)) == fa.FA_ERR_INVALID_ARG  # workspace not 256-aligned
+    assert _dec(lib, n_splits=-1) == fa.FA_ERR_INVALID_ARG
+    assert _dec(lib, Nk=0) == fa.FA_ERR_INVALID_ARG
+    assert _dec(lib, scale=-1.0) == fa.FA_ERR_INVALID_ARG
+    assert _dec(lib, d=96, dv=96) == fa.FA_ERR_UNSUPPORTED
+    need = lib.fa_decode_workspace_size(2, 2, 128, 4)
+    assert _dec(lib, ws_bytes=need - 1) == fa.FA_ERR_WORKSPACE
+    assert _dec(lib, ws_bytes=0) == fa.FA_ERR_WORKSPACE
+
+
+def test_merge_rejects_bad_arguments(lib):
+    m = lib.fa_merge_states
+    assert m(NULL, P, 2, 3, 4, P, P, 0, NULL) == fa.FA_ERR_INVALID_ARG
+    assert m(P, P, 0, 3, 4, P, P, 0, NULL) == fa.FA_ERR_INVALID_ARG
+    assert m(P, P, 2, 0, 4, P, P, 0, NULL) == fa.FA_ERR_INVALID_ARG
+    assert m(P, P, 2, 3, 513, P, P, 0, NULL) == fa.FA_ERR_INVALID_ARG
+    assert m(P, P, 2, 3, 4, P, P, 5, NULL) == fa.FA_ERR_INVALID_ARG
+
+
+def test_workspace_and_split_heuristic(lib):
+    ws = lib.fa_decode_workspace_size
+    assert ws(0, 1, 1, 1) == 0 and ws(1, 1, 1, 0) == 0
+    # fp32 partial outputs then fp32 partial lse, each rounded up to 256 bytes
+    assert ws(16, 32, 128, 10) == (16 * 32 * 10 * 128 * 4 + 255) // 256 * 256 + (16 * 32 * 10 * 4 + 255) // 256 * 256
+    ds = lib.fa_decode_default_splits
+    assert ds(0, 1, 1, 1) == 0
+    for (B, H, Nk, sms) in ((16, 32, 32768, 148), (1, 1, 100000, 152), (64, 64, 256, 152), (1, 1, 1, 152)):
+        n = ds(B, H, Nk, sms)
+        assert 1 <= n <= max(1, -(-Nk // 256))
+    # more SMs never means fewer splits
+    assert ds(4, 8, 32768, 152) >= ds(4, 8, 32768, 76)
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert isinstance(fa.status_string(s), str) and fa.status_string(s)
+    assert "timed out" in fa.status_string(fa.FA_ERR_TIMEOUT)

@@ -1,0 +1,108 @@
+"""fa_decode_splitkv and fa_merge_states (CUDA, through the C ABI) against the CPU FP64 oracle."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fa_inputs import decode_inputs, merge_inputs
+from tests.parity import assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def fa():
+    import exact_tiled_attention_fa_gb300 as m
+    return m
+
+
+def oracle_decode_compact(q, k, v, lens, scale):
+    """Oracle on each sequence's own prefix (never copies the padding to the host)."""
+    B, H = q.shape[0], q.shape[1]
+    dv = v.shape[-1]
+    O = np.zeros((B, H, 1, dv))
+    L = np.zeros((B, H, 1))
+    for b in range(B):
+        n = int(lens[b])
+        if n == 0:
+            L[b] = -np.inf
+            continue
+        o_b, l_b = oracle.attention(q[b].cpu(), k[b, :, :n].cpu(), v[b, :, :n].cpu(), causal=False, scale=scale)
+        O[b], L[b] = o_b, l_b
+    return O, L
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("n_splits", [1, 3, 16, 0, 999])
+def test_small_decode(d, n_splits):
+    B, H, Nk_max = 4, 3, 1000
+    lens = torch.tensor([1, 64, 65, 1000], dtype=torch.int32)
+    q, k, v, _ = decode_inputs(B, H, Nk_max, d, d, seed=d, device=DEV, seqlens=lens)
+    scale = 1.0 / math.sqrt(d)
+    o_ref, lse_ref = oracle_decode_compact(q, k, v, lens, scale)
+    for dt in (torch.float32, torch.bfloat16):
+        o, lse = fa().decode_splitkv(q, k, v, lens.to(DEV), scale=scale, n_splits=n_splits, out_dtype=dt)
+        torch.cuda.synchronize()
+        assert fa().get_device_error() == 0
+        assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16), what=f"d={d} n={n_splits} {dt}")
+
+
+def test_zero_length_and_clamped_lengths():
+    B, H, Nk_max, d = 3, 2, 300, 64
+    lens_in = torch.tensor([0, -5, 310], dtype=torch.int32)  # -5 and 310 are out of range
+    q, k, v, _ = decode_inputs(B, H, Nk_max, d, d, seed=1, device=DEV, seqlens=torch.tensor([0, 0, 300]))
+    o, lse = fa().decode_splitkv(q, k, v, lens_in.to(DEV), n_splits=4, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == fa().FA_ERR_INVALID_ARG  # recorded, lengths clamped to [0, 300]
+    assert fa().get_device_error() == 0  # reading cleared it
+    assert torch.all(o[:2] == 0) and torch.all(torch.isneginf(lse[:2]))
+    o_ref, lse_ref = oracle_decode_compact(q[2:], k[2:], v[2:], [300], 1 / 8)
+    assert_close(o[2:], lse[2:], o_ref, lse_ref, what="clamped length")
+
+
+def test_split_invariance_and_determinism():
+    B, H, Nk_max, d = 2, 4, 4096, 128
+    q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=3, lo=1, hi=Nk_max, device=DEV)
+    outs = []
+    for n in (1, 2, 7, 32, 64):
+        o, lse = fa().decode_splitkv(q, k, v, lens.to(DEV), n_splits=n, out_dtype=torch.float32)
+        o2, lse2 = fa().decode_splitkv(q, k, v, lens.to(DEV), n_splits=n, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o2) and torch.equal(lse, lse2)
+        outs.append((o, lse))
+    for o, lse in outs[1:]:
+        assert float((o - outs[0][0]).abs().max()) <= 2e-3
+        assert float((lse - outs[0][1]).abs().max()) <= 2e-4
+
+
+def test_full_decode_config():
+    """B=16, H=32, d=128, lengths ~ U{1024..32768} (seed 0), caches padded to 32768 with NaN:
+    every one of the 512 heads against the oracle."""
+    B, H, Nk_max, d = 16, 32, 32768, 128
+    q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=0, lo=1024, hi=32768, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa().decode_splitkv(q, k, v, lens.to(DEV), scale=scale, n_splits=0, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == 0
+    o_ref, lse_ref = oracle_decode_compact(q, k, v, lens, scale)
+    assert_close(o, lse, o_ref, lse_ref, what="decode B16 H32 Nk<=32768")
+
+
+@pytest.mark.parametrize("n_parts,rows,dv,empty", [(1, 5, 128, 0.0), (16, 333, 128, 0.3), (999, 7, 64, 0.5),
+                                                   (3, 64, 512, 0.0), (4, 10, 33, 1.0)])
+def test_merge_states_against_oracle(n_parts, rows, dv, empty):
+    o_parts, lse_parts = merge_inputs(n_parts, rows, dv, seed=n_parts, empty_frac=empty, device=DEV)
+    o_ref, lse_ref = oracle.merge_lse(o_parts.cpu(), lse_parts.cpu())
+    o, lse = fa().merge_states(o_parts, lse_parts, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    a, b = to_np(lse), lse_ref
+    assert np.array_equal(np.isneginf(a), np.isneginf(b))
+    fin = ~np.isneginf(b)
+    if fin.any():
+        assert np.abs(a[fin] - b[fin]).max() <= 1e-5 * max(1.0, np.abs(b[fin]).max())
+    assert np.abs(to_np(o) - o_ref).max() <= 1e-5

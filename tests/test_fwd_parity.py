@@ -1,0 +1,148 @@
+"""fa_fwd (CUDA, through the C ABI) against the CPU FP64 oracle on the same bf16 inputs."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fa_inputs import attention_inputs, sample_slices
+from tests.parity import assert_close, to_np
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def fa():
+    import exact_tiled_attention_fa_gb300 as m
+    return m
+
+
+def run(q, k, v, causal, scale=None, out_dtype=torch.float32):
+    o, lse = fa().fwd(q, k, v, causal=causal, scale=scale, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == 0
+    return o, lse
+
+
+# (B, H, N, Nk, d, mult): the single-head 256 x 256 case, the pages' demo shapes (77 x 513 with
+# causal offset 436, 300 x 300, a single query over 1000 keys), several tiles with ragged tails,
+# and N > Nk (causal rows with no visible key).
+SMALL = [
+    (1, 1, 256, 256, 64, 1.0),
+    (8, 8, 77, 513, 32, 2.0),
+    (2, 3, 300, 300, 64, 1.0),
+    (1, 2, 1, 1000, 64, 1.0),
+    (2, 2, 333, 700, 128, 1.0),
+    (1, 2, 700, 333, 128, 1.0),
+    (1, 1, 200, 100, 64, 1.0),
+    (3, 1, 129, 129, 32, 2.0),
+    (1, 1, 1, 1, 128, 1.0),
+]
+
+
+@pytest.mark.parametrize("B,H,N,Nk,d,mult", SMALL)
+@pytest.mark.parametrize("causal", [False, True])
+def test_small_shapes_full_oracle(B, H, N, Nk, d, mult, causal):
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=0, mult=mult, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=causal, scale=scale)
+    o, lse = run(q, k, v, causal, scale, torch.float32)
+    assert_close(o, lse, o_ref, lse_ref, what=f"fp32 {B,H,N,Nk,d} causal={causal}")
+    ob, lseb = run(q, k, v, causal, scale, torch.bfloat16)
+    assert_close(ob, lseb, o_ref, lse_ref, bf16_out=True, what=f"bf16 {B,H,N,Nk,d} causal={causal}")
+
+
+def test_causal_first_row_is_v0_exactly():
+    q, k, v = attention_inputs(2, 3, 256, 256, 64, 64, seed=4, device=DEV)
+    o, lse = run(q, k, v, True, 0.125, torch.float32)
+    assert torch.equal(o[:, :, 0, :], v[:, :, 0, :].float())
+    ref = (q[:, :, 0, :].double() * k[:, :, 0, :].double()).sum(-1) * 0.125
+    assert float((lse[:, :, 0].double() - ref).abs().max()) <= 1e-5
+
+
+def test_rows_without_visible_keys():
+    q, k, v = attention_inputs(1, 2, 300, 100, 64, 64, seed=5, device=DEV)
+    o, lse = run(q, k, v, True, 0.125, torch.float32)
+    assert torch.all(o[:, :, :200] == 0) and torch.all(torch.isneginf(lse[:, :, :200]))
+
+
+def test_deterministic_and_no_writes_past_output():
+    B, H, N, Nk, d = 2, 2, 333, 257, 128
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=6, device=DEV)
+    guard = 4096
+    for causal in (False, True):
+        for dt in (torch.float32, torch.bfloat16):
+            buf = torch.full((B * H * N * d + guard,), float("nan"), dtype=dt, device=DEV)
+            lbuf = torch.full((B * H * N + guard,), float("nan"), dtype=torch.float32, device=DEV)
+            o = buf[: B * H * N * d].view(B, H, N, d)
+            lse = lbuf[: B * H * N].view(B, H, N)
+            fa().fwd(q, k, v, causal=causal, out=o, lse=lse)
+            torch.cuda.synchronize()
+            assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+            assert torch.isnan(buf[B * H * N * d:]).all() and torch.isnan(lbuf[B * H * N:]).all()
+            o2, lse2 = fa().fwd(q, k, v, causal=causal, out_dtype=dt)
+            torch.cuda.synchronize()
+            assert torch.equal(o, o2) and torch.equal(lse, lse2)
+
+
+def test_q_zero_averages_visible_values():
+    B, H, N, Nk, d = 1, 2, 130, 390, 64
+    _, k, v = attention_inputs(B, H, N, Nk, d, d, seed=7, device=DEV)
+    q = torch.zeros((B, H, N, d), dtype=torch.bfloat16, device=DEV)
+    for causal in (False, True):
+        o, lse = run(q, k, v, causal, 0.125, torch.float32)
+        vv = to_np(v)
+        for i in (0, 1, 77, 129):
+            n = Nk - N + i + 1 if causal else Nk
+            assert np.abs(to_np(o)[:, :, i] - vv[:, :, :n].mean(axis=2)).max() <= 1e-4
+            assert np.abs(to_np(lse)[:, :, i] - math.log(n)).max() <= 1e-5
+
+
+def _sampled_check(B, H, N, Nk, d, mult, causal, n_slices, rows=None, seed=0, out_dtype=torch.float32):
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=seed, mult=mult, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = run(q, k, v, causal, scale, out_dtype)
+    for idx in sample_slices(B * H, n_slices, seed=1):
+        b, h = divmod(idx, H)
+        for (r0, r1) in rows or [(0, N)]:
+            o_ref, lse_ref = oracle.attention(q[b, h].cpu(), k[b, h].cpu(), v[b, h].cpu(), causal=causal,
+                                              scale=scale, rows=(r0, r1))
+            assert_close(o[b, h, r0:r1], lse[b, h, r0:r1], o_ref, lse_ref,
+                         bf16_out=(out_dtype == torch.bfloat16), what=f"(b,h)=({b},{h}) rows {r0}:{r1}")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gpt2_medium_shape_sampled(causal):
+    """B=64, H=16, N=Nk=1024, d=64: 32 seeded (b, h) slices against the oracle."""
+    _sampled_check(64, 16, 1024, 1024, 64, 1.0, causal, 32)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gpt2_medium_shape_bf16_out_sampled(causal):
+    _sampled_check(64, 16, 1024, 1024, 64, 1.0, causal, 4, out_dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_ragged_4097_sampled(causal):
+    """B=4, H=16, N=Nk=4097, d=128, inputs x2: 3 heads, first and last 384 rows (the ragged tail tile)."""
+    _sampled_check(4, 16, 4097, 4097, 128, 2.0, causal, 3, rows=[(0, 384), (3713, 4097)])
+
+
+def test_ragged_77_513_full():
+    """B=8, H=8, N=77, Nk=513, d=32, inputs x2, causal offset 436 (every head)."""
+    q, k, v = attention_inputs(8, 8, 77, 513, 32, 32, seed=0, mult=2.0, device=DEV)
+    scale = 1.0 / math.sqrt(32)
+    for causal in (False, True):
+        o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=causal, scale=scale)
+        o, lse = run(q, k, v, causal, scale)
+        assert_close(o, lse, o_ref, lse_ref, what=f"77x513 causal={causal}")
+
+
+def test_long_causal_sampled():
+    """B=2, H=32, N=Nk=16384, d=128, causal: 4 heads x first 2048 rows, and the last 128 rows of one head."""
+    _sampled_check(2, 32, 16384, 16384, 128, 1.0, True, 4, rows=[(0, 2048)])
+    _sampled_check(2, 32, 16384, 16384, 128, 1.0, True, 1, rows=[(16256, 16384)])
