@@ -381,7 +381,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--decode-only", action="store_true", help="only the split-KV decode (profiling)")
     ap.add_argument("--decode-batch", type=int, default=DEC["B"], help="decode batch (smaller cache for profiling)")
-    ap.add_argument("--cpu-slices", type=int, default=64)
+    ap.add_argument("--cpu-slices", type=int, default=1024)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
