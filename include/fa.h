@@ -122,6 +122,39 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
                             int n_splits, fa_dtype o_dtype, void* stream);
 
 /*
+ * Bytes of device scratch that fa_decode_splitkv_noalloc owns (8 MiB): room for the split
+ * partials of B*H*n_splits*(dv+1) fp32 values, e.g. B=16, H=32, dv=128 with up to 30 splits.
+ */
+#define FA_DECODE_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/*
+ * fa_decode_splitkv without a workspace argument: the same computation, arguments, checks and
+ * result, but the split partials go to a fixed scratch array of FA_DECODE_NOALLOC_SCRATCH_BYTES
+ * that the library keeps in device memory (every GPU that loads the library holds it until the
+ * process exits).  The pages have no counterpart; it exists for callers that cannot allocate
+ * device memory: code whose memory belongs to another allocator (a framework's caching allocator,
+ * a serving engine's fixed pool) and may not call cudaMalloc behind its back, code under a hard
+ * per-process memory budget, and code that must not risk the device-wide synchronisation that
+ * cudaMalloc and cudaFree can cause.  It allocates nothing and calls no allocating routine.
+ *
+ *   - Size limit: returns FA_ERR_WORKSPACE, launching nothing, when
+ *     fa_decode_workspace_size(B, H, dv, n) exceeds FA_DECODE_NOALLOC_SCRATCH_BYTES, where n is
+ *     n_splits or, for n_splits = 0, the automatic count.  Use fewer splits, or
+ *     fa_decode_splitkv with a workspace of your own, for larger problems.
+ *   - Set-up: the first call on each device looks up the scratch array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make that first call
+ *     before any stream capture.  A failed look-up returns FA_ERR_CUDA.
+ *   - Sharing: every call on a device uses the same array, which keeps the last call's contents.
+ *     Nothing in it needs to start at zero (each non-empty split writes its slot before the
+ *     combine reads it, and empty splits are never read).  Calls whose kernels overlap on the GPU
+ *     (concurrent streams, or several host threads) race on the array: order them on one stream.
+ */
+fa_status fa_decode_splitkv_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                    const int* seqlens_k, void* o, float* lse, int B, int H,
+                                    int Nk_max, int d, int dv, float scale, int n_splits,
+                                    fa_dtype o_dtype, void* stream);
+
+/*
  * Log-sum-exp combine of n_parts partial attention states per row ("flash_lab.py"
  * section 4 combine; section 1 `merge_states`, where a state with lse = -inf is empty and
  * gets weight 0):
