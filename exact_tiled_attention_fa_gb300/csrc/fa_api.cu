@@ -146,8 +146,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
         return FA_ERR_INVALID_ARG;
     const long long BH = static_cast<long long>(B) * H;
-    const long long n_qtiles = (static_cast<long long>(N) + fa::kBlockM - 1) / fa::kBlockM;
-    if (BH * n_qtiles > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    const long long n_qp = (static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+    if (BH * n_qp > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     if (!head_ok(d) || dv != d) return FA_ERR_UNSUPPORTED;
 
     fa::FwdParams p;
@@ -156,13 +156,17 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
         return FA_ERR_CUDA;
     int* status = nullptr;
     if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
     p.o = o;
     p.lse = lse;
     p.status = status;
     p.BH = static_cast<int>(BH);
     p.N = N;
     p.Nk = Nk;
-    p.n_qtiles = static_cast<int>(n_qtiles);
+    p.n_qp = static_cast<int>(n_qp);
+    p.n_items = static_cast<int>(BH * n_qp);
+    p.num_ctas = sms;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.wait_limit_ns = g_wait_ns.load();
     cudaError_t e = fa::launch_fwd(p, d, causal != 0, o_dtype, static_cast<cudaStream_t>(stream));

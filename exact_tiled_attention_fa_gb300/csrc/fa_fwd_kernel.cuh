@@ -1,36 +1,47 @@
 // fa_fwd_kernel.cuh -- exact attention forward for sm_103a.
 //
 // Algorithm: "flash_lab.py -- FlashAttention, flash-decoding and megakernel in
-// numpy", section 3 `flash_fwd`, FlashAttention-2 loop order: each CTA owns one
-// tile of 128 query rows and walks the key/value tiles of its head, keeping the
-// running row max m and row sum l (section 1, `softmax_online`: the old sum is
-// rescaled by exp(m_old - m_new)) and an unnormalised O accumulator on chip.
-// O is divided by l once at the end and LSE = m + log l.  With a causal mask
-// the walk stops at the first tile lying wholly after the tile's last query
-// position (query i sits at position Nk - N + i; "02_flash_forward.py", demo 1).
+// numpy", section 3 `flash_fwd`, FlashAttention-2 loop order: a query tile walks
+// the key/value tiles of its head keeping the running row max m and row sum l
+// (section 1, `softmax_online`: the old sum is rescaled by exp(m_old - m_new)) and
+// an unnormalised O accumulator on chip; O is divided by l once at the end and
+// LSE = m + log l.  With a causal mask the walk stops at the first tile lying
+// wholly after the tile's last query position (query i sits at position
+// Nk - N + i; "02_flash_forward.py", demo 1).
 //
-// GB300 mapping (one CTA of 6 warps per 128-row query tile):
-//   warp 4      TMA producer: Q once, then K_j / V_j into a 2-stage ring.
-//   warp 5      tcgen05 issuer: S_j = Q K_j^T into one of two TMEM score buffers,
-//               and O += P_j V_j into a TMEM accumulator; commits signal barriers.
-//               S_{j+1} is issued before P_j is ready, so the tensor core
-//               computes the next scores while the softmax of this tile runs.
-//   warps 0..3  softmax: thread t owns query row t (= TMEM lane t); reads its
-//               score row from TMEM, masks, updates m and l in the base-2 domain
-//               with a log2(e)-prescaled scale, writes P (bf16) to shared memory
-//               in the 128-byte-swizzled K-major layout the MMA reads, and
-//               rescales its O row in TMEM when its max grew.  Then the
-//               epilogue: O / l and LSE to global memory.
-// The running max moves whenever a tile raises it, so the largest P of the
-// row is exactly 1 in bf16.  (Keeping a stale max to skip rescales, with P up
-// to 2^k, would leave that dominant weight rounded: with values of magnitude
-// ~8 the O error then reaches 2e-2, above the 1e-2 the results must meet.)
-// A warp rescales its O rows in TMEM only when the max of one of its rows grew.
+// GB300 mapping.  A persistent grid (one CTA per SM) walks work items; an item is
+// one head and a pair of 128-row query tiles Q0, Q1 that share every K/V tile.
+// Items are ordered head-major (the query pairs of one head run on neighbouring
+// CTAs, so that head's K and V are read from HBM once and then hit in L2), with
+// the heaviest pair of a head first.  Ten warps per CTA:
+//   warps 0-3 / 4-7  softmax warpgroups for Q0 / Q1: thread t owns query row t
+//                    (= TMEM lane t): it reads its score row from TMEM, masks,
+//                    updates m and l in base 2 with a log2(e)-prescaled scale,
+//                    writes P (bf16) back to TMEM, rescales its O row when the max
+//                    grew, and at the end of the item writes O / l and LSE.
+//   warp 8           TMA producer: Q0, Q1 per item, K_j / V_j into a ring of stages.
+//   warp 9           tcgen05 issuer: S_i = Q_i K_j^T (both operands in shared memory)
+//                    and O_i += P_i V_j (P from tensor memory, V from shared memory),
+//                    in the order PV0(j), S0(j+1), PV1(j), S1(j+1): while one
+//                    warpgroup exponentiates, the tensor core runs the other's MMAs.
+// Tensor memory (512 columns): S0, S1 (128 fp32 columns each), O0, O1 (d each) and
+// P0, P1 (64 columns of packed bf16 each).  For d = 128 there is no room left, so
+// P_i overwrites the first half of S_i (already read into registers); S_i(j+1) is
+// then issued only after P_i(j) V_j has completed.
+// Because every commit tracks all earlier MMAs of the issuing thread, the arrival of
+// S_i(j) also means P_i(j-1) V_{j-1} has completed: the softmax can then overwrite
+// P_i and rescale O_i without a separate wait.
 //
-// Every barrier wait is bounded (FwdParams::wait_limit_ns).  A role whose wait
-// runs out records FA_ERR_TIMEOUT, raises the CTA's abort flag so the other
-// roles stop too, and every role then drains what it has in flight (TMA copies,
-// tensor-core operations) before the CTA frees its tensor memory and exits.
+// Precision: the running max moves whenever a tile raises it, so the largest P of a
+// row is exactly 1 in bf16.  (Keeping a stale max to skip rescales, with P up to
+// 2^k, leaves that dominant weight rounded: with values of magnitude ~8 the O error
+// then reaches 2e-2, above the 1e-2 the results must meet.)  A warp rescales its O
+// rows only when the max of one of its rows grew.
+//
+// Every barrier wait is bounded (FwdParams::wait_limit_ns).  A role whose wait runs
+// out records FA_ERR_TIMEOUT and raises the CTA's abort flag so the other roles stop
+// too; each role then drains what it has in flight (TMA copies, tensor-core
+// operations) before the CTA frees its tensor memory and exits.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -42,46 +53,54 @@
 namespace fa {
 
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;  // 1 s for draining after a failure
+constexpr int kFwdThreads = 320;                             // 10 warps
+constexpr int kWarpProducer = 8;
+constexpr int kWarpMma = 9;
 
 template <int D>
 struct FwdCfg {
     static_assert(D == 32 || D == 64 || D == 128, "head size");
-    static constexpr int kCB = D < 64 ? D : 64;        // elements per column block (swizzle span)
-    static constexpr int kNumCB = D / kCB;             // column blocks per row
-    static constexpr int kRowBytes = kCB * 2;          // 64 or 128 bytes
+    static constexpr int kCB = D < 64 ? D : 64;            // elements per column block (swizzle span)
+    static constexpr int kNumCB = D / kCB;                 // column blocks per row
+    static constexpr int kRowBytes = kCB * 2;              // 64 or 128 bytes
     static constexpr uint32_t kLayout = kRowBytes == 128 ? kSwizzle128B : kSwizzle64B;
-    static constexpr int kAtomBytes = 8 * kRowBytes;   // 8-row swizzle atom
+    static constexpr int kAtomBytes = 8 * kRowBytes;       // 8-row swizzle atom
     static constexpr int kBlkBytes = kBlockM * kRowBytes;  // one 128-row column block
     static constexpr int kTileBytes = kNumCB * kBlkBytes;  // 128 x D bf16
-    static constexpr int kPBlkBytes = kBlockM * 128;       // 128 rows x 64 keys bf16
-    static constexpr int kPBytes = 2 * kPBlkBytes;         // P tile: two 64-key column blocks
-    static constexpr int kStages = 2;
-    static constexpr int kOffQ = 0;
-    static constexpr int kOffK = kOffQ + kTileBytes;
+    static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);  // K/V ring depth
+    static constexpr int kOffQ = 0;                                    // Q0, Q1
+    static constexpr int kOffK = 2 * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kOffP = kOffV + kStages * kTileBytes;
-    static constexpr int kOffBar = kOffP + kPBytes;
-    static constexpr int kNumBars = 12;
-    static constexpr int kUsedBytes = kOffBar + kNumBars * 8 + 16;
-    // At least 120 KB so that only one CTA (holding all 512 TMEM columns) fits per SM.
-    static constexpr int kSmemBytes = (kUsedBytes + 1024 > 120 * 1024 ? kUsedBytes + 1024 : 120 * 1024);
+    static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+    static constexpr int kNumBars = 32;
+    static constexpr int kUsedBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
+    // At least 120 KB so that a second CTA (which would wait for the 512 TMEM columns
+    // this persistent CTA holds) never shares the SM.
+    static constexpr int kSmemBytes = kUsedBytes > 120 * 1024 ? kUsedBytes : 120 * 1024;
     static constexpr int kTmemCols = 512;
-    static constexpr int kColS0 = 0;
-    static constexpr int kColO = 256;
+    static constexpr bool kAliasP = (D == 128);
+    __host__ __device__ static constexpr uint32_t col_s(int i) { return 128u * i; }
+    __host__ __device__ static constexpr uint32_t col_o(int i) { return 256u + static_cast<uint32_t>(D) * i; }
+    __host__ __device__ static constexpr uint32_t col_p(int i)
+    {
+        return kAliasP ? col_s(i) : 256u + 2u * D + 64u * i;
+    }
     static constexpr uint32_t kIdescS = idesc_bf16(kBlockM, kBlockN, false);
     static constexpr uint32_t kIdescO = idesc_bf16(kBlockM, D, true);
 };
 
 // barrier slots
 enum : int {
-    kBarQFull = 0,
-    kBarKFull = 1,   // +stage
-    kBarVFull = 3,   // +stage
-    kBarKVEmpty = 5, // +stage
-    kBarSFull = 7,   // +score buffer
-    kBarPFull = 9,
-    kBarPVDone = 10,
-    kBarDrain = 11
+    kBarQFull = 0,    // +tile (2)
+    kBarQEmpty = 2,   // +tile (2)
+    kBarSFull = 4,    // +tile (2)
+    kBarPFull = 6,    // +tile (2)
+    kBarPVDone = 8,   // +tile (2)
+    kBarOReady = 10,  // +tile (2)
+    kBarDrain = 12,
+    kBarKFull = 13,   // +stage (<= 4)
+    kBarVFull = 17,   // +stage
+    kBarKVEmpty = 21  // +stage
 };
 
 __device__ __forceinline__ void record_failure(int* status, volatile int* abort_flag, int code)
@@ -115,10 +134,49 @@ __device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, c
     }
 }
 
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Shape of one work item (head bh, query rows [i0, i0 + 256)).
+struct Item {
+    int bh, i0;
+    int rows[2];  // valid query rows of Q0 / Q1 (0 when the tile lies past N)
+    int n[2];     // key/value tiles each query tile visits
+    int n_kv;     // max(n[0], n[1])
+};
+
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int item, bool causal)
+{
+    Item it;
+    it.bh = item / p.n_qp;
+    const int qp = p.n_qp - 1 - (item - it.bh * p.n_qp);  // heaviest pair of the head first
+    it.i0 = qp * 2 * kBlockM;
+    const int n_all = (p.Nk + kBlockN - 1) / kBlockN;
+    const int off = p.Nk - p.N;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int r0 = it.i0 + i * kBlockM;
+        it.rows[i] = r0 < p.N ? min(kBlockM, p.N - r0) : 0;
+        int n = it.rows[i] > 0 ? n_all : 0;
+        if (causal && n > 0) {
+            const int last_pos = off + r0 + it.rows[i] - 1;  // position of the tile's last query row
+            n = last_pos < 0 ? 0 : min(n_all, last_pos / kBlockN + 1);
+        }
+        it.n[i] = n;
+    }
+    it.n_kv = max(it.n[0], it.n[1]);
+    return it;
+}
+
 template <int D, bool CAUSAL, typename OutT>
-__global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p)
+__global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p)
 {
     using C = FwdCfg<D>;
+    constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -130,38 +188,27 @@ __global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // Work item: heaviest query tiles first (under a causal mask the last tile
-    // of every head has the most visible keys).
-    const int tile_rev = blockIdx.x / p.BH;
-    const int bh = blockIdx.x - tile_rev * p.BH;
-    const int qt = p.n_qtiles - 1 - tile_rev;
-    const int i0 = qt * kBlockM;
-    const int br = min(kBlockM, p.N - i0);
-    const int off = p.Nk - p.N;  // query i sits at key position off + i
-    const int n_kv_all = (p.Nk + kBlockN - 1) / kBlockN;
-    int n_kv = n_kv_all;
-    if (CAUSAL) {
-        const int last_pos = off + i0 + br - 1;  // position of the tile's last query row
-        n_kv = last_pos < 0 ? 0 : min(n_kv_all, last_pos / kBlockN + 1);
-    }
     const unsigned long long limit = p.wait_limit_ns;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(kBarQFull), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kBarQFull + i), 1);
+            mbar_init(bar(kBarQEmpty + i), 1);
+            mbar_init(bar(kBarSFull + i), 1);
+            mbar_init(bar(kBarPFull + i), kBlockM);
+            mbar_init(bar(kBarPVDone + i), 1);
+            mbar_init(bar(kBarOReady + i), 1);
+        }
+        mbar_init(bar(kBarDrain), 1);
+        for (int s = 0; s < S; ++s) {
             mbar_init(bar(kBarKFull + s), 1);
             mbar_init(bar(kBarVFull + s), 1);
             mbar_init(bar(kBarKVEmpty + s), 1);
-            mbar_init(bar(kBarSFull + s), 1);
         }
-        mbar_init(bar(kBarPFull), kBlockM);
-        mbar_init(bar(kBarPVDone), 1);
-        mbar_init(bar(kBarDrain), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
         tmem_relinquish();
     }
@@ -170,235 +217,302 @@ __global__ void __launch_bounds__(192, 1) fa_fwd_kernel(const __grid_constant__ 
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0 && n_kv > 0) {
+    if (warp == kWarpProducer) {
+        // ============================================================ producer
+        if (lane == 0) {
             prefetch_tensormap(&p.tm_q);
             prefetch_tensormap(&p.tm_k);
             prefetch_tensormap(&p.tm_v);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
-            int last_issued[2] = {-1, -1};
-            mbar_arrive_expect_tx(bar(kBarQFull), C::kTileBytes);
-#pragma unroll
-            for (int cb = 0; cb < C::kNumCB; ++cb)
-                tma_load_3d(sbase + C::kOffQ + cb * C::kBlkBytes, &p.tm_q, bar(kBarQFull), cb * C::kCB,
-                            i0, bh, pol_q);
+            int q_loads[2] = {0, 0};  // loads issued into each Q buffer
+            long long g = 0;          // K/V tiles issued so far (ring position)
             bool ok = true;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j & 1;
-                if (j >= 2 && !mbar_wait(bar(kBarKVEmpty + s), ((j >> 1) + 1) & 1, limit, abort_flag)) {
-                    ok = false;
-                    break;
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+                const Item it = decode_item(p, item, CAUSAL);
+                for (int i = 0; i < 2 && ok; ++i) {
+                    if (it.n[i] == 0) continue;
+                    if (q_loads[i] > 0 &&
+                        !mbar_wait(bar(kBarQEmpty + i), (q_loads[i] - 1) & 1, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(kBarQFull + i), C::kTileBytes);
+#pragma unroll
+                    for (int cb = 0; cb < C::kNumCB; ++cb)
+                        tma_load_3d(sbase + C::kOffQ + i * C::kTileBytes + cb * C::kBlkBytes, &p.tm_q,
+                                    bar(kBarQFull + i), cb * C::kCB, it.i0 + i * kBlockM, it.bh, pol_q);
+                    ++q_loads[i];
                 }
-                mbar_arrive_expect_tx(bar(kBarKFull + s), C::kTileBytes);
+                for (int j = 0; ok && j < it.n_kv; ++j, ++g) {
+                    const int s = static_cast<int>(g % S);
+                    const uint32_t round = static_cast<uint32_t>(g / S);
+                    if (g >= S && !mbar_wait(bar(kBarKVEmpty + s), (round - 1) & 1, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(bar(kBarKFull + s), C::kTileBytes);
 #pragma unroll
-                for (int cb = 0; cb < C::kNumCB; ++cb)
-                    tma_load_3d(sbase + C::kOffK + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_k,
-                                bar(kBarKFull + s), cb * C::kCB, j * kBlockN, bh, pol_kv);
-                mbar_arrive_expect_tx(bar(kBarVFull + s), C::kTileBytes);
+                    for (int cb = 0; cb < C::kNumCB; ++cb)
+                        tma_load_3d(sbase + C::kOffK + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_k,
+                                    bar(kBarKFull + s), cb * C::kCB, j * kBlockN, it.bh, pol_kv);
+                    mbar_arrive_expect_tx(bar(kBarVFull + s), C::kTileBytes);
 #pragma unroll
-                for (int cb = 0; cb < C::kNumCB; ++cb)
-                    tma_load_3d(sbase + C::kOffV + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_v,
-                                bar(kBarVFull + s), cb * C::kCB, j * kBlockN, bh, pol_kv);
-                last_issued[s] = j;
+                    for (int cb = 0; cb < C::kNumCB; ++cb)
+                        tma_load_3d(sbase + C::kOffV + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_v,
+                                    bar(kBarVFull + s), cb * C::kCB, j * kBlockN, it.bh, pol_kv);
+                }
             }
-            if (!ok) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
-            // Every issued copy must have landed before the CTA may exit.
-            mbar_wait(bar(kBarQFull), 0, kDrainLimitNs, nullptr);
-            for (int s = 0; s < 2; ++s) {
-                if (last_issued[s] < 0) continue;
-                const uint32_t par = (last_issued[s] >> 1) & 1;
+            if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+            // Every issued copy must land before the CTA may exit (its last phase per barrier).
+            for (int i = 0; i < 2; ++i)
+                if (q_loads[i] > 0) mbar_wait(bar(kBarQFull + i), (q_loads[i] - 1) & 1, kDrainLimitNs, nullptr);
+            for (long long t = g - S < 0 ? 0 : g - S; t < g; ++t) {
+                const int s = static_cast<int>(t % S);
+                const uint32_t par = static_cast<uint32_t>(t / S) & 1;
                 mbar_wait(bar(kBarKFull + s), par, kDrainLimitNs, nullptr);
                 mbar_wait(bar(kBarVFull + s), par, kDrainLimitNs, nullptr);
             }
         }
-    } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kWarpMma) {
+        // ============================================================ MMA issuer
         if (lane == 0) {
-            auto issue_s = [&](int j) {
-                const int s = j & 1;
-                const uint32_t d_tmem = tmem + C::kColS0 + 128u * static_cast<uint32_t>(s);
+            int q_uses[2] = {0, 0};   // items in which Q buffer i was used
+            int tiles[2] = {0, 0};    // (query tile, key tile) pairs processed, per query tile
+            long long g = 0;          // K/V ring position
+            bool ok = true;
+
+            auto issue_s = [&](int i, int stage) {
+                const uint32_t d_tmem = tmem + C::col_s(i);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const int cb = (kk * 16) / C::kCB;
                     const int within = ((kk * 16) % C::kCB) * 2;
-                    const uint64_t a = smem_desc(sbase + C::kOffQ + cb * C::kBlkBytes + within, 16,
-                                                 C::kAtomBytes, C::kLayout);
-                    const uint64_t b = smem_desc(
-                        sbase + C::kOffK + s * C::kTileBytes + cb * C::kBlkBytes + within, 16,
-                        C::kAtomBytes, C::kLayout);
+                    const uint64_t a = smem_desc(sbase + C::kOffQ + i * C::kTileBytes + cb * C::kBlkBytes + within,
+                                                 16, C::kAtomBytes, C::kLayout);
+                    const uint64_t b = smem_desc(sbase + C::kOffK + stage * C::kTileBytes + cb * C::kBlkBytes + within,
+                                                 16, C::kAtomBytes, C::kLayout);
                     umma_ss(d_tmem, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int j) {
-                const int s = j & 1;
+            auto issue_pv = [&](int i, int stage, bool accumulate) {
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint64_t a = smem_desc(sbase + C::kOffP + (kk >> 2) * C::kPBlkBytes + (kk & 3) * 32,
-                                                 16, 1024, kSwizzle128B);
-                    const uint64_t b = smem_desc(
-                        sbase + C::kOffV + s * C::kTileBytes + kk * 16 * C::kRowBytes, C::kBlkBytes,
-                        C::kAtomBytes, C::kLayout);
-                    umma_ss(tmem + C::kColO, a, b, C::kIdescO, (j > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t b = smem_desc(sbase + C::kOffV + stage * C::kTileBytes + kk * 16 * C::kRowBytes,
+                                                 C::kBlkBytes, C::kAtomBytes, C::kLayout);
+                    umma_ts(tmem + C::col_o(i), tmem + C::col_p(i) + 8u * kk, b, C::kIdescO,
+                            (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
-            bool ok = true;
-            if (n_kv > 0) {
-                ok = mbar_wait(bar(kBarQFull), 0, limit, abort_flag) &&
-                     mbar_wait(bar(kBarKFull + 0), 0, limit, abort_flag);
-                if (ok) {
-                    tc_fence_after_sync();
-                    issue_s(0);
-                    umma_commit(bar(kBarSFull + 0));
+            // S_i for key tile j of the item (K stage `stage`); with P aliased into S_i the
+            // previous P_i V must have completed first.
+            auto do_s = [&](int i, int j, const Item& it, int stage) -> bool {
+                if (C::kAliasP && tiles[i] > 0 &&
+                    !mbar_wait(bar(kBarPVDone + i), (tiles[i] - 1) & 1, limit, abort_flag))
+                    return false;
+                tc_fence_after_sync();
+                issue_s(i, stage);
+                umma_commit(bar(kBarSFull + i));
+                if (j == it.n[i] - 1) umma_commit(bar(kBarQEmpty + i));  // Q_i no longer read
+                return true;
+            };
+
+            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+                const Item it = decode_item(p, item, CAUSAL);
+                if (it.n_kv == 0) continue;
+                for (int i = 0; i < 2 && ok; ++i)
+                    if (it.n[i] > 0) ok = mbar_wait(bar(kBarQFull + i), q_uses[i] & 1, limit, abort_flag);
+                if (!ok) break;
+                // prologue: S_0, S_1 for key tile 0
+                {
+                    const int s0 = static_cast<int>(g % S);
+                    if (!mbar_wait(bar(kBarKFull + s0), static_cast<uint32_t>(g / S) & 1, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int i = 0; i < 2 && ok; ++i)
+                        if (it.n[i] > 0) ok = do_s(i, 0, it, s0);
+                    if (!ok) break;
                 }
-                for (int j = 0; ok && j < n_kv; ++j) {
-                    if (j + 1 < n_kv) {
-                        // buffer (j+1)&1 last held S_{j-1}, read before P_{j-1} was signalled
-                        if (!mbar_wait(bar(kBarKFull + ((j + 1) & 1)), ((j + 1) >> 1) & 1, limit,
-                                       abort_flag)) {
+                for (int j = 0; ok && j < it.n_kv; ++j) {
+                    const long long gj = g + j;
+                    const int sj = static_cast<int>(gj % S);
+                    const long long gn = gj + 1;
+                    const int sn = static_cast<int>(gn % S);
+                    bool next_k_ready = false;
+                    if (!mbar_wait(bar(kBarVFull + sj), static_cast<uint32_t>(gj / S) & 1, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    for (int i = 0; i < 2; ++i) {
+                        if (j >= it.n[i]) continue;
+                        if (!mbar_wait(bar(kBarPFull + i), tiles[i] & 1, limit, abort_flag)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after_sync();
-                        issue_s(j + 1);
-                        umma_commit(bar(kBarSFull + ((j + 1) & 1)));
+                        issue_pv(i, sj, j > 0);
+                        umma_commit(bar(kBarPVDone + i));
+                        if (j == it.n[i] - 1) umma_commit(bar(kBarOReady + i));
+                        ++tiles[i];
+                        if (j + 1 < it.n[i]) {
+                            if (!next_k_ready) {
+                                if (!mbar_wait(bar(kBarKFull + sn), static_cast<uint32_t>(gn / S) & 1, limit,
+                                               abort_flag)) {
+                                    ok = false;
+                                    break;
+                                }
+                                next_k_ready = true;
+                            }
+                            if (!do_s(i, j + 1, it, sn)) {
+                                ok = false;
+                                break;
+                            }
+                        }
                     }
-                    if (!mbar_wait(bar(kBarPFull), j & 1, limit, abort_flag) ||
-                        !mbar_wait(bar(kBarVFull + (j & 1)), (j >> 1) & 1, limit, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    issue_pv(j);
-                    umma_commit(bar(kBarPVDone));
-                    umma_commit(bar(kBarKVEmpty + (j & 1)));
+                    if (!ok) break;
+                    umma_commit(bar(kBarKVEmpty + sj));  // every MMA reading K_j / V_j is issued
                 }
+                for (int i = 0; i < 2; ++i)
+                    if (it.n[i] > 0) ++q_uses[i];
+                g += it.n_kv;
             }
-            if (!ok) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+            if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
             // Wait for every tensor-core operation this thread issued.
             umma_commit(bar(kBarDrain));
             mbar_wait(bar(kBarDrain), 0, kDrainLimitNs, nullptr);
         }
     } else {
-        // ------------------------------------------------------------ softmax + epilogue
-        const int r = threadIdx.x;  // query row within the tile == TMEM lane
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const int qpos = off + i0 + r;
+        // ============================================================ softmax + epilogue
+        const int wg = warp >> 2;               // query tile of this warpgroup
+        const int r = threadIdx.x & 127;        // row within the tile == TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t t_s = tmem + lane_base + C::col_s(wg);
+        const uint32_t t_o = tmem + lane_base + C::col_o(wg);
+        const uint32_t t_p = tmem + lane_base + C::col_p(wg);
         const float sl2 = p.scale_log2;
-        float m_ref = -INFINITY;  // running max of scale*log2(e)*S over the visible keys
-        float l = 0.f;
+        const int off = p.Nk - p.N;
+        int tiles = 0;   // (query tile, key tile) pairs processed by this warpgroup
+        int items = 0;   // items in which this warpgroup had key tiles
         bool ok = true;
-        const uint32_t p_row = sbase + C::kOffP + static_cast<uint32_t>(r) * 128u;
-        const uint32_t swz = static_cast<uint32_t>(r & 7);
 
-        for (int j = 0; j < n_kv; ++j) {
-            const int sb = j & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + sb), (j >> 1) & 1, limit, abort_flag));
-            if (!ok) break;
-            tc_fence_after_sync();
-            float s[kBlockN];
-            {
-                uint32_t u[32];
-#pragma unroll
-                for (int c = 0; c < kBlockN / 32; ++c) {
-                    tmem_ld32(tmem + lane_base + C::kColS0 + 128u * sb + 32u * c, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(u[i]);
-                }
-            }
-            const int k0 = j * kBlockN;
-            const bool need_mask = (k0 + kBlockN > p.Nk) || (CAUSAL && k0 + kBlockN - 1 > off + i0);
-            if (need_mask) {
-                const int last = CAUSAL ? min(qpos, p.Nk - 1) : p.Nk - 1;  // last visible key
-#pragma unroll
-                for (int c = 0; c < kBlockN; ++c)
-                    if (k0 + c > last) s[c] = -INFINITY;
-            }
-            float mx = s[0];
-#pragma unroll
-            for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
-            const float mt = mx * sl2;
-            const bool grow = mt > m_ref;
-            float alpha = 1.f;
-            if (grow) {
-                alpha = ex2(m_ref - mt);  // 0 when m_ref = -inf
-                m_ref = mt;
-            }
-            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float rs = 0.f;
-            uint32_t pk[kBlockN / 2];
-#pragma unroll
-            for (int c = 0; c < kBlockN; c += 2) {
-                const float p0 = ex2(fmaf(s[c], sl2, -m_use));
-                const float p1 = ex2(fmaf(s[c + 1], sl2, -m_use));
-                rs += p0 + p1;
-                pk[c / 2] = pack_bf16x2(p0, p1);
-            }
-            // P_{j-1} V_{j-1} must have finished before P is overwritten or O rescaled.
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPVDone), (j - 1) & 1, limit, abort_flag));
+        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            const Item it = decode_item(p, item, CAUSAL);
+            const int n = wg ? it.n[1] : it.n[0];
+            const int rows = wg ? it.rows[1] : it.rows[0];
+            const int row0 = it.i0 + wg * kBlockM;  // first query row of this tile
+            const int qpos = off + row0 + r;
+            float m_run = -INFINITY;  // running max of scale*log2(e)*S over visible keys
+            float l = 0.f;
+            for (int j = 0; j < n; ++j) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarSFull + wg), tiles & 1, limit, abort_flag));
                 if (!ok) break;
                 tc_fence_after_sync();
-            }
+                uint32_t u[kBlockN];
+                tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+                tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+                tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]));
+                tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
+                tmem_ld_wait();
+                float s[kBlockN];
 #pragma unroll
-            for (int ch = 0; ch < 16; ++ch) {
-                const uint32_t addr = p_row + static_cast<uint32_t>(ch >> 3) * C::kPBlkBytes +
-                                      ((static_cast<uint32_t>(ch & 7) ^ swz) << 4);
-                st_shared_v4(addr, pk[ch * 4 + 0], pk[ch * 4 + 1], pk[ch * 4 + 2], pk[ch * 4 + 3]);
-            }
-            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(u[c]);
+                const int k0 = j * kBlockN;
+                const bool need_mask = (k0 + kBlockN > p.Nk) || (CAUSAL && k0 + kBlockN - 1 > off + row0);
+                if (need_mask) {
+                    const int last = CAUSAL ? min(qpos, p.Nk - 1) : p.Nk - 1;  // last visible key
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t u[32];
-                    const uint32_t ta = tmem + lane_base + C::kColO + 32u * c;
-                    tmem_ld32(ta, u);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-                    tmem_st32(ta, u);
+                    for (int c = 0; c < kBlockN; ++c)
+                        if (k0 + c > last) s[c] = -INFINITY;
                 }
+                float mq[4];  // row max: four independent 3-input max chains of 32 columns
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float* t = s + 32 * q;
+                    float a = max3(t[0], t[1], t[2]);
+#pragma unroll
+                    for (int c = 3; c < 31; c += 2) a = max3(a, t[c], t[c + 1]);
+                    mq[q] = fmaxf(a, t[31]);
+                }
+                const float mt = max3(mq[0], mq[1], fmaxf(mq[2], mq[3])) * sl2;
+                const bool grow = mt > m_run;
+                float alpha = 1.f;
+                if (grow) {
+                    alpha = ex2(m_run - mt);  // 0 when m_run = -inf
+                    m_run = mt;
+                }
+                const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+                uint32_t pk[kBlockN / 2];
+#pragma unroll
+                for (int c = 0; c < kBlockN; c += 4) {
+                    const float p0 = ex2(fmaf(s[c + 0], sl2, -m_use));
+                    const float p1 = ex2(fmaf(s[c + 1], sl2, -m_use));
+                    const float p2 = ex2(fmaf(s[c + 2], sl2, -m_use));
+                    const float p3 = ex2(fmaf(s[c + 3], sl2, -m_use));
+                    rs0 += p0;
+                    rs1 += p1;
+                    rs2 += p2;
+                    rs3 += p3;
+                    pk[c / 2] = pack_bf16x2(p0, p1);
+                    pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+                }
+                // S_i(j) arrived, so P_i(j-1) V_{j-1} has completed: O_i and the P slot are free.
+                if (j > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        tmem_ld32(t_o + 32u * c, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                        tmem_st32(t_o + 32u * c, o);
+                    }
+                }
+                tmem_st32(t_p + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
+                tmem_st32(t_p + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
                 tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(bar(kBarPFull + wg));
+                l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
+                ++tiles;
             }
-            l = l * alpha + rs;
-            fence_proxy_async_shared();
-            tc_fence_before_sync();
-            mbar_arrive(bar(kBarPFull));
-        }
-        if (ok && n_kv > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPVDone), (n_kv - 1) & 1, limit, abort_flag));
-        }
-        if (!ok) {
-            record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
-        } else {
-            tc_fence_after_sync();
+            if (!ok) break;
+            if (rows == 0) continue;  // tile lies past N: nothing to write
+            if (n > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOReady + wg), items & 1, limit, abort_flag));
+                if (!ok) break;
+                ++items;
+                tc_fence_after_sync();
+            }
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const size_t row = static_cast<size_t>(bh) * p.N + static_cast<size_t>(i0 + r);
+            const size_t row = static_cast<size_t>(it.bh) * p.N + static_cast<size_t>(row0 + r);
+            const bool valid = r < rows;
             OutT* orow = reinterpret_cast<OutT*>(p.o) + row * D;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 float v[32];
-                if (n_kv > 0) {
-                    uint32_t u[32];
-                    tmem_ld32(tmem + lane_base + C::kColO + 32u * c, u);
+                if (n > 0) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + 32u * c, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]) * inv;
+                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    for (int e = 0; e < 32; ++e) v[e] = 0.f;
                 }
-                if (r < br) store_row32<OutT>(orow + 32 * c, v);
+                if (valid) store_row32<OutT>(orow + 32 * c, v);
             }
-            if (p.lse != nullptr && r < br)
-                p.lse[row] = l > 0.f ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+            if (p.lse != nullptr && valid)
+                p.lse[row] = l > 0.f ? (m_run + log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
+        if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
     }
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == kWarpMma) {
         __syncwarp();
         tc_fence_after_sync();
         tmem_dealloc(tmem, C::kTmemCols);
@@ -419,8 +533,8 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    const unsigned grid = static_cast<unsigned>(p.BH) * static_cast<unsigned>(p.n_qtiles);
-    kern<<<grid, 192, C::kSmemBytes, st>>>(p);
+    const int grid = p.n_items < p.num_ctas ? p.n_items : p.num_ctas;
+    kern<<<grid, kFwdThreads, C::kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 

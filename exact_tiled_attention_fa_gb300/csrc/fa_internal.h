@@ -23,7 +23,9 @@ struct FwdParams {
     float* lse;        // [B*H][N] or nullptr
     int* status;       // device status word
     int BH, N, Nk;
-    int n_qtiles;       // ceil(N / 128)
+    int n_qp;           // query tile pairs per head: ceil(N / 256)
+    int n_items;        // BH * n_qp work items
+    int num_ctas;       // persistent CTAs (one per SM)
     float scale_log2;   // scale * log2(e)
     unsigned long long wait_limit_ns;
 };

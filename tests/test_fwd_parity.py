@@ -146,3 +146,20 @@ def test_long_causal_sampled():
     """B=2, H=32, N=Nk=16384, d=128, causal: 4 heads x first 2048 rows, and the last 128 rows of one head."""
     _sampled_check(2, 32, 16384, 16384, 128, 1.0, True, 4, rows=[(0, 2048)])
     _sampled_check(2, 32, 16384, 16384, 128, 1.0, True, 1, rows=[(16256, 16384)])
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A 1 ns wait limit makes the kernel's first barrier wait run out: the kernel records
+    FA_ERR_TIMEOUT, drains its copies and MMAs, frees tensor memory and returns; the
+    context stays usable and the next call (default limit) is correct."""
+    q, k, v = attention_inputs(2, 4, 1024, 1024, 64, 64, seed=8, device=DEV)
+    fa().set_wait_timeout_ns(1)
+    try:
+        fa().fwd(q, k, v, causal=False, out_dtype=torch.float32)
+        status = fa().get_device_error()
+    finally:
+        fa().set_wait_timeout_ns(0)
+    assert status == fa().FA_ERR_TIMEOUT
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, scale=0.125)
+    o, lse = run(q, k, v, True, 0.125, torch.float32)
+    assert_close(o, lse, o_ref, lse_ref, what="after a timed-out launch")
