@@ -12,8 +12,8 @@
 // GB300 mapping.  A persistent grid (one CTA per SM) walks work items; an item is
 // one head and a pair of 128-row query tiles Q0, Q1 that share every K/V tile.
 // Items are ordered head-major (the query pairs of one head run on neighbouring
-// CTAs, so that head's K and V are read from HBM once and then hit in L2), with
-// the heaviest pair of a head first.  Ten warps per CTA:
+// CTAs, so that head's K and V are read from HBM once and then hit in L2) and are
+// handed out two at a time, a heavy and a light one (see cta_item).  Ten warps:
 //   warps 0-3 / 4-7  softmax warpgroups for Q0 / Q1: thread t owns query row t
 //                    (= TMEM lane t): it reads its score row from TMEM, masks,
 //                    updates m and l in base 2 with a log2(e)-prescaled scale,
@@ -149,11 +149,24 @@ struct Item {
     int n_kv;     // max(n[0], n[1])
 };
 
+// k-th work item of this CTA, or -1 past the end.  A CTA takes pairs of consecutive
+// items (pair blockIdx.x + t * gridDim.x).  Within a head the query pairs run heaviest,
+// lightest, second heaviest, second lightest, ... (see decode_item), so under a causal
+// mask the two items of a pair together carry about the same work as any other pair
+// and the static assignment stays balanced without a global work counter.
+__device__ __forceinline__ int cta_item(const FwdParams& p, int k)
+{
+    const long long pair = blockIdx.x + static_cast<long long>(k >> 1) * gridDim.x;
+    const long long item = 2 * pair + (k & 1);
+    return item < p.n_items ? static_cast<int>(item) : -1;
+}
+
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int item, bool causal)
 {
     Item it;
     it.bh = item / p.n_qp;
-    const int qp = p.n_qp - 1 - (item - it.bh * p.n_qp);  // heaviest pair of the head first
+    const int t = item - it.bh * p.n_qp;
+    const int qp = (t & 1) ? (t >> 1) : p.n_qp - 1 - (t >> 1);  // heavy, light, heavy, light, ...
     it.i0 = qp * 2 * kBlockM;
     const int n_all = (p.Nk + kBlockN - 1) / kBlockN;
     const int off = p.Nk - p.N;
@@ -228,7 +241,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             int q_loads[2] = {0, 0};  // loads issued into each Q buffer
             long long g = 0;          // K/V tiles issued so far (ring position)
             bool ok = true;
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            for (int k = 0; ok; ++k) {
+                const int item = cta_item(p, k);
+                if (item < 0) break;
                 const Item it = decode_item(p, item, CAUSAL);
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (it.n[i] == 0) continue;
@@ -317,7 +332,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 return true;
             };
 
-            for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+            for (int k = 0; ok; ++k) {
+                const int item = cta_item(p, k);
+                if (item < 0) break;
                 const Item it = decode_item(p, item, CAUSAL);
                 if (it.n_kv == 0) continue;
                 for (int i = 0; i < 2 && ok; ++i)
@@ -396,7 +413,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         int items = 0;   // items in which this warpgroup had key tiles
         bool ok = true;
 
-        for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        for (int k = 0; ok; ++k) {
+            const int item = cta_item(p, k);
+            if (item < 0) break;
             const Item it = decode_item(p, item, CAUSAL);
             const int n = wg ? it.n[1] : it.n[0];
             const int rows = wg ? it.rows[1] : it.rows[0];
@@ -533,7 +552,8 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
-    const int grid = p.n_items < p.num_ctas ? p.n_items : p.num_ctas;
+    const int pairs = (p.n_items + 1) / 2;
+    const int grid = pairs < p.num_ctas ? pairs : p.num_ctas;
     kern<<<grid, kFwdThreads, C::kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
