@@ -19,11 +19,15 @@
 //                    updates m and l in base 2 with a log2(e)-prescaled scale,
 //                    writes P (bf16) back to TMEM, rescales its O row when the max
 //                    grew, and at the end of the item writes O / l and LSE.
-//   warp 8           TMA producer: Q0, Q1 per item, K_j / V_j into a ring of stages.
-//   warp 9           tcgen05 issuer: S_i = Q_i K_j^T (both operands in shared memory)
-//                    and O_i += P_i V_j (P from tensor memory, V from shared memory),
-//                    in the order PV0(j), S0(j+1), PV1(j), S1(j+1): while one
+//   warp 8           TMA producer: Q0, Q1 per item (double-buffered for d <= 64),
+//                    K_j / V_j into a ring of stages.
+//   warps 9, 10      tcgen05 issuers for Q0 and Q1: S_i = Q_i K_j^T (both operands in
+//                    shared memory) and O_i += P_i V_j (P from tensor memory, V from
+//                    shared memory), each issuing PV_i(j) then S_i(j+1): while one
 //                    warpgroup exponentiates, the tensor core runs the other's MMAs.
+//                    Every barrier wait or commit stalls the issuing thread for a few
+//                    hundred cycles, so each issuer handles only its own query tile,
+//                    and K_j / V_j share one barrier.
 // Tensor memory (512 columns): S0, S1 (128 fp32 columns each), O0, O1 (d each) and
 // P0, P1 (64 columns of packed bf16 each).  For d = 128 there is no room left, so
 // P_i overwrites the first half of S_i (already read into registers); S_i(j+1) is
@@ -53,9 +57,24 @@
 namespace fa {
 
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;  // 1 s for draining after a failure
-constexpr int kFwdThreads = 320;                             // 10 warps
+constexpr int kFwdThreads = 352;                             // 11 warps
 constexpr int kWarpProducer = 8;
-constexpr int kWarpMma = 9;
+constexpr int kWarpMma = 9;  // warps 9 and 10 issue the MMAs of Q0 and Q1
+
+// barrier slots
+constexpr int kMaxStages = 8;
+enum : int {
+    kBarQFull = 0,                         // +2 * buffer + tile (4)
+    kBarQEmpty = 4,                        // +2 * buffer + tile (4)
+    kBarSFull = 8,                         // +tile (2)
+    kBarPFull = 10,                        // +tile (2)
+    kBarPVDone = 12,                       // +tile (2)
+    kBarOReady = 14,                       // +tile (2)
+    kBarDrain = 16,                         // +tile (2)
+    kBarKVFull = 18,                        // +stage: K_j and V_j landed
+    kBarKVEmpty = kBarKVFull + kMaxStages,  // +stage: both issuers are done with the stage
+    kBarCount = kBarKVEmpty + kMaxStages
+};
 
 template <int D>
 struct FwdCfg {
@@ -68,11 +87,15 @@ struct FwdCfg {
     static constexpr int kBlkBytes = kBlockM * kRowBytes;  // one 128-row column block
     static constexpr int kTileBytes = kNumCB * kBlkBytes;  // 128 x D bf16
     static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);  // K/V ring depth
-    static constexpr int kOffQ = 0;                                    // Q0, Q1
-    static constexpr int kOffK = 2 * kTileBytes;
+    // Q buffers per query tile: two for d <= 64, so the next item's Q loads while the
+    // current item runs (an item there spans few key tiles); one for d = 128 (no room).
+    static constexpr int kQBuf = D == 128 ? 1 : 2;
+    static constexpr int kOffQ = 0;  // Q buffer (b, i) at kOffQ + (2 * b + i) * kTileBytes
+    static constexpr int kOffK = 2 * kQBuf * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     static constexpr int kOffBar = kOffV + kStages * kTileBytes;
-    static constexpr int kNumBars = 32;
+    static constexpr int kNumBars = 48;
+    static_assert(kStages <= kMaxStages && kBarCount <= kNumBars, "barrier slots");
     static constexpr int kUsedBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
     // At least 120 KB so that a second CTA (which would wait for the 512 TMEM columns
     // this persistent CTA holds) never shares the SM.
@@ -89,19 +112,6 @@ struct FwdCfg {
     static constexpr uint32_t kIdescO = idesc_bf16(kBlockM, D, true);
 };
 
-// barrier slots
-enum : int {
-    kBarQFull = 0,    // +tile (2)
-    kBarQEmpty = 2,   // +tile (2)
-    kBarSFull = 4,    // +tile (2)
-    kBarPFull = 6,    // +tile (2)
-    kBarPVDone = 8,   // +tile (2)
-    kBarOReady = 10,  // +tile (2)
-    kBarDrain = 12,
-    kBarKFull = 13,   // +stage (<= 4)
-    kBarVFull = 17,   // +stage
-    kBarKVEmpty = 21  // +stage
-};
 
 __device__ __forceinline__ void record_failure(int* status, volatile int* abort_flag, int code)
 {
@@ -204,19 +214,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     const unsigned long long limit = p.wait_limit_ns;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
             mbar_init(bar(kBarQFull + i), 1);
             mbar_init(bar(kBarQEmpty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(kBarSFull + i), 1);
             mbar_init(bar(kBarPFull + i), kBlockM);
             mbar_init(bar(kBarPVDone + i), 1);
             mbar_init(bar(kBarOReady + i), 1);
+            mbar_init(bar(kBarDrain + i), 1);
         }
-        mbar_init(bar(kBarDrain), 1);
         for (int s = 0; s < S; ++s) {
-            mbar_init(bar(kBarKFull + s), 1);
-            mbar_init(bar(kBarVFull + s), 1);
-            mbar_init(bar(kBarKVEmpty + s), 1);
+            mbar_init(bar(kBarKVFull + s), 1);
+            mbar_init(bar(kBarKVEmpty + s), 2);  // one arrival from each MMA issuer
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -247,16 +258,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 const Item it = decode_item(p, item, CAUSAL);
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (it.n[i] == 0) continue;
-                    if (q_loads[i] > 0 &&
-                        !mbar_wait(bar(kBarQEmpty + i), (q_loads[i] - 1) & 1, limit, abort_flag)) {
+                    const int b = q_loads[i] % C::kQBuf;  // buffer of this load
+                    const int q_bar = 2 * b + i;
+                    if (q_loads[i] >= C::kQBuf &&
+                        !mbar_wait(bar(kBarQEmpty + q_bar), (q_loads[i] / C::kQBuf - 1) & 1, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(kBarQFull + i), C::kTileBytes);
+                    mbar_arrive_expect_tx(bar(kBarQFull + q_bar), C::kTileBytes);
 #pragma unroll
                     for (int cb = 0; cb < C::kNumCB; ++cb)
-                        tma_load_3d(sbase + C::kOffQ + i * C::kTileBytes + cb * C::kBlkBytes, &p.tm_q,
-                                    bar(kBarQFull + i), cb * C::kCB, it.i0 + i * kBlockM, it.bh, pol_q);
+                        tma_load_3d(sbase + C::kOffQ + q_bar * C::kTileBytes + cb * C::kBlkBytes, &p.tm_q,
+                                    bar(kBarQFull + q_bar), cb * C::kCB, it.i0 + i * kBlockM, it.bh, pol_q);
                     ++q_loads[i];
                 }
                 for (int j = 0; ok && j < it.n_kv; ++j, ++g) {
@@ -266,69 +279,69 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(bar(kBarKFull + s), C::kTileBytes);
+                    mbar_arrive_expect_tx(bar(kBarKVFull + s), 2 * C::kTileBytes);
 #pragma unroll
                     for (int cb = 0; cb < C::kNumCB; ++cb)
                         tma_load_3d(sbase + C::kOffK + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_k,
-                                    bar(kBarKFull + s), cb * C::kCB, j * kBlockN, it.bh, pol_kv);
-                    mbar_arrive_expect_tx(bar(kBarVFull + s), C::kTileBytes);
+                                    bar(kBarKVFull + s), cb * C::kCB, j * kBlockN, it.bh, pol_kv);
 #pragma unroll
                     for (int cb = 0; cb < C::kNumCB; ++cb)
                         tma_load_3d(sbase + C::kOffV + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_v,
-                                    bar(kBarVFull + s), cb * C::kCB, j * kBlockN, it.bh, pol_kv);
+                                    bar(kBarKVFull + s), cb * C::kCB, j * kBlockN, it.bh, pol_kv);
                 }
             }
             if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
             // Every issued copy must land before the CTA may exit (its last phase per barrier).
             for (int i = 0; i < 2; ++i)
-                if (q_loads[i] > 0) mbar_wait(bar(kBarQFull + i), (q_loads[i] - 1) & 1, kDrainLimitNs, nullptr);
+                for (int t = q_loads[i] - C::kQBuf < 0 ? 0 : q_loads[i] - C::kQBuf; t < q_loads[i]; ++t)
+                    mbar_wait(bar(kBarQFull + 2 * (t % C::kQBuf) + i), (t / C::kQBuf) & 1, kDrainLimitNs, nullptr);
             for (long long t = g - S < 0 ? 0 : g - S; t < g; ++t) {
                 const int s = static_cast<int>(t % S);
                 const uint32_t par = static_cast<uint32_t>(t / S) & 1;
-                mbar_wait(bar(kBarKFull + s), par, kDrainLimitNs, nullptr);
-                mbar_wait(bar(kBarVFull + s), par, kDrainLimitNs, nullptr);
+                mbar_wait(bar(kBarKVFull + s), par, kDrainLimitNs, nullptr);
             }
         }
-    } else if (warp == kWarpMma) {
-        // ============================================================ MMA issuer
+    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+        // ============================================================ MMA issuers
+        // Warp 9 issues every MMA of query tile 0, warp 10 those of query tile 1, so the
+        // fixed cost of barrier waits and commits on the issuing thread is split in two.
         if (lane == 0) {
-            int q_uses[2] = {0, 0};   // items in which Q buffer i was used
-            int tiles[2] = {0, 0};    // (query tile, key tile) pairs processed, per query tile
-            long long g = 0;          // K/V ring position
+            const int i = warp - kWarpMma;  // query tile of this issuer
+            int q_uses = 0;                 // items in which this query tile had key tiles
+            int tiles = 0;                  // (query tile, key tile) pairs processed
+            long long g = 0;                // K/V ring position
             bool ok = true;
+            const uint32_t d_s = tmem + C::col_s(i);
+            const uint32_t d_o = tmem + C::col_o(i);
+            const uint32_t a_p = tmem + C::col_p(i);
 
-            auto issue_s = [&](int i, int stage) {
-                const uint32_t d_tmem = tmem + C::col_s(i);
+            // S_i = Q_i K^T from Q buffer q_bar and K stage `stage`.  Descriptors are built
+            // once per group and advanced by the byte offset (>> 4) of each 16-wide K step.
+            auto issue_s = [&](int q_bar, int stage) {
+                const uint64_t a0 = smem_desc(sbase + C::kOffQ + q_bar * C::kTileBytes, 16, C::kAtomBytes, C::kLayout);
+                const uint64_t b0 = smem_desc(sbase + C::kOffK + stage * C::kTileBytes, 16, C::kAtomBytes, C::kLayout);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const int cb = (kk * 16) / C::kCB;
-                    const int within = ((kk * 16) % C::kCB) * 2;
-                    const uint64_t a = smem_desc(sbase + C::kOffQ + i * C::kTileBytes + cb * C::kBlkBytes + within,
-                                                 16, C::kAtomBytes, C::kLayout);
-                    const uint64_t b = smem_desc(sbase + C::kOffK + stage * C::kTileBytes + cb * C::kBlkBytes + within,
-                                                 16, C::kAtomBytes, C::kLayout);
-                    umma_ss(d_tmem, a, b, C::kIdescS, kk > 0 ? 1u : 0u);
+                    const uint32_t off = ((kk * 16) / C::kCB * C::kBlkBytes + ((kk * 16) % C::kCB) * 2) >> 4;
+                    umma_ss(d_s, a0 + off, b0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](int i, int stage, bool accumulate) {
+            auto issue_pv = [&](int stage, bool accumulate) {
+                const uint64_t b0 = smem_desc(sbase + C::kOffV + stage * C::kTileBytes, C::kBlkBytes, C::kAtomBytes,
+                                              C::kLayout);
 #pragma unroll
-                for (int kk = 0; kk < kBlockN / 16; ++kk) {
-                    const uint64_t b = smem_desc(sbase + C::kOffV + stage * C::kTileBytes + kk * 16 * C::kRowBytes,
-                                                 C::kBlkBytes, C::kAtomBytes, C::kLayout);
-                    umma_ts(tmem + C::col_o(i), tmem + C::col_p(i) + 8u * kk, b, C::kIdescO,
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    umma_ts(d_o, a_p + 8u * kk, b0 + ((kk * 16 * C::kRowBytes) >> 4), C::kIdescO,
                             (accumulate || kk > 0) ? 1u : 0u);
-                }
             };
-            // S_i for key tile j of the item (K stage `stage`); with P aliased into S_i the
-            // previous P_i V must have completed first.
-            auto do_s = [&](int i, int j, const Item& it, int stage) -> bool {
-                if (C::kAliasP && tiles[i] > 0 &&
-                    !mbar_wait(bar(kBarPVDone + i), (tiles[i] - 1) & 1, limit, abort_flag))
+            // Next S_i; with P aliased into S_i the previous P_i V must have completed first.
+            auto do_s = [&](int q_bar, int stage, bool last) -> bool {
+                if (C::kAliasP && tiles > 0 && !mbar_wait(bar(kBarPVDone + i), (tiles - 1) & 1, limit, abort_flag))
                     return false;
                 tc_fence_after_sync();
-                issue_s(i, stage);
+                issue_s(q_bar, stage);
                 umma_commit(bar(kBarSFull + i));
-                if (j == it.n[i] - 1) umma_commit(bar(kBarQEmpty + i));  // Q_i no longer read
+                if (last) umma_commit(bar(kBarQEmpty + q_bar));  // Q_i no longer read
                 return true;
             };
 
@@ -336,68 +349,58 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 const int item = cta_item(p, k);
                 if (item < 0) break;
                 const Item it = decode_item(p, item, CAUSAL);
-                if (it.n_kv == 0) continue;
-                for (int i = 0; i < 2 && ok; ++i)
-                    if (it.n[i] > 0) ok = mbar_wait(bar(kBarQFull + i), q_uses[i] & 1, limit, abort_flag);
-                if (!ok) break;
-                // prologue: S_0, S_1 for key tile 0
-                {
-                    const int s0 = static_cast<int>(g % S);
-                    if (!mbar_wait(bar(kBarKFull + s0), static_cast<uint32_t>(g / S) & 1, limit, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    for (int i = 0; i < 2 && ok; ++i)
-                        if (it.n[i] > 0) ok = do_s(i, 0, it, s0);
-                    if (!ok) break;
+                const int n = i ? it.n[1] : it.n[0];
+                const int q_bar = 2 * (q_uses % C::kQBuf) + i;
+                if (n > 0 && !mbar_wait(bar(kBarQFull + q_bar), (q_uses / C::kQBuf) & 1, limit, abort_flag)) {
+                    ok = false;
+                    break;
                 }
                 for (int j = 0; ok && j < it.n_kv; ++j) {
                     const long long gj = g + j;
                     const int sj = static_cast<int>(gj % S);
-                    const long long gn = gj + 1;
-                    const int sn = static_cast<int>(gn % S);
-                    bool next_k_ready = false;
-                    if (!mbar_wait(bar(kBarVFull + sj), static_cast<uint32_t>(gj / S) & 1, limit, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    for (int i = 0; i < 2; ++i) {
-                        if (j >= it.n[i]) continue;
-                        if (!mbar_wait(bar(kBarPFull + i), tiles[i] & 1, limit, abort_flag)) {
+                    if (j >= n) {
+                        // key tile this query tile does not visit: release the stage once it is loaded
+                        if (!mbar_wait(bar(kBarKVFull + sj), static_cast<uint32_t>(gj / S) & 1, limit, abort_flag)) {
                             ok = false;
                             break;
                         }
-                        tc_fence_after_sync();
-                        issue_pv(i, sj, j > 0);
-                        umma_commit(bar(kBarPVDone + i));
-                        if (j == it.n[i] - 1) umma_commit(bar(kBarOReady + i));
-                        ++tiles[i];
-                        if (j + 1 < it.n[i]) {
-                            if (!next_k_ready) {
-                                if (!mbar_wait(bar(kBarKFull + sn), static_cast<uint32_t>(gn / S) & 1, limit,
-                                               abort_flag)) {
-                                    ok = false;
-                                    break;
-                                }
-                                next_k_ready = true;
-                            }
-                            if (!do_s(i, j + 1, it, sn)) {
-                                ok = false;
-                                break;
-                            }
+                        mbar_arrive(bar(kBarKVEmpty + sj));
+                        continue;
+                    }
+                    if (j == 0) {
+                        if (!mbar_wait(bar(kBarKVFull + sj), static_cast<uint32_t>(gj / S) & 1, limit, abort_flag) ||
+                            !do_s(q_bar, sj, n == 1)) {
+                            ok = false;
+                            break;
                         }
                     }
-                    if (!ok) break;
-                    umma_commit(bar(kBarKVEmpty + sj));  // every MMA reading K_j / V_j is issued
+                    if (!mbar_wait(bar(kBarPFull + i), tiles & 1, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    issue_pv(sj, j > 0);
+                    if (C::kAliasP) umma_commit(bar(kBarPVDone + i));
+                    if (j == n - 1) umma_commit(bar(kBarOReady + i));
+                    umma_commit(bar(kBarKVEmpty + sj));
+                    ++tiles;
+                    if (j + 1 < n) {
+                        const long long gn = gj + 1;
+                        const int sn = static_cast<int>(gn % S);
+                        if (!mbar_wait(bar(kBarKVFull + sn), static_cast<uint32_t>(gn / S) & 1, limit, abort_flag) ||
+                            !do_s(q_bar, sn, j + 1 == n - 1)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                 }
-                for (int i = 0; i < 2; ++i)
-                    if (it.n[i] > 0) ++q_uses[i];
+                if (n > 0) ++q_uses;
                 g += it.n_kv;
             }
             if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
             // Wait for every tensor-core operation this thread issued.
-            umma_commit(bar(kBarDrain));
-            mbar_wait(bar(kBarDrain), 0, kDrainLimitNs, nullptr);
+            umma_commit(bar(kBarDrain + i));
+            mbar_wait(bar(kBarDrain + i), 0, kDrainLimitNs, nullptr);
         }
     } else {
         // ============================================================ softmax + epilogue
