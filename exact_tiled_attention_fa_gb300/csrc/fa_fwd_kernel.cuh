@@ -57,9 +57,15 @@
 namespace fa {
 
 constexpr unsigned long long kDrainLimitNs = 1000000000ull;  // 1 s for draining after a failure
-constexpr int kFwdThreads = 352;                             // 11 warps
+constexpr int kFwdThreads = 384;  // 12 warps = 3 warpgroups
 constexpr int kWarpProducer = 8;
-constexpr int kWarpMma = 9;  // warps 9 and 10 issue the MMAs of Q0 and Q1
+constexpr int kWarpMma = 9;       // warps 9 and 10 issue the MMAs of Q0 and Q1; warp 11 idles
+// Registers per thread after the split: the producer / MMA warpgroup gives registers to the
+// two softmax warpgroups.  The split needs kFwdThreads * (registers at launch) >=
+// 256 * kSoftmaxRegs + 128 * kControlRegs; the launcher checks this before every launch,
+// because an increase that the pool cannot satisfy would wait forever.
+constexpr int kSoftmaxRegs = 224;
+constexpr int kControlRegs = 56;
 
 // barrier slots
 constexpr int kMaxStages = 8;
@@ -71,7 +77,8 @@ enum : int {
     kBarPVDone = 12,                       // +tile (2)
     kBarOReady = 14,                       // +tile (2)
     kBarDrain = 16,                         // +tile (2)
-    kBarKVFull = 18,                        // +stage: K_j and V_j landed
+    kBarSFree = 18,                         // +tile (2): the softmax has read S_i out of TMEM
+    kBarKVFull = 20,                        // +stage: K_j and V_j landed
     kBarKVEmpty = kBarKVFull + kMaxStages,  // +stage: both issuers are done with the stage
     kBarCount = kBarKVEmpty + kMaxStages
 };
@@ -224,6 +231,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             mbar_init(bar(kBarPVDone + i), 1);
             mbar_init(bar(kBarOReady + i), 1);
             mbar_init(bar(kBarDrain + i), 1);
+            mbar_init(bar(kBarSFree + i), kBlockM);
         }
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(kBarKVFull + s), 1);
@@ -241,7 +249,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kWarpProducer) {
+    if (warp >= kWarpProducer) {
+      regs_decrease<kControlRegs>();
+      if (warp == kWarpProducer) {
         // ============================================================ producer
         if (lane == 0) {
             prefetch_tensormap(&p.tm_q);
@@ -301,7 +311,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 mbar_wait(bar(kBarKVFull + s), par, kDrainLimitNs, nullptr);
             }
         }
-    } else if (warp == kWarpMma || warp == kWarpMma + 1) {
+      } else if (warp == kWarpMma || warp == kWarpMma + 1) {
         // ============================================================ MMA issuers
         // Warp 9 issues every MMA of query tile 0, warp 10 those of query tile 1, so the
         // fixed cost of barrier waits and commits on the issuing thread is split in two.
@@ -309,6 +319,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             const int i = warp - kWarpMma;  // query tile of this issuer
             int q_uses = 0;                 // items in which this query tile had key tiles
             int tiles = 0;                  // (query tile, key tile) pairs processed
+            int s_issued = 0;               // S_i tiles issued so far
             long long g = 0;                // K/V ring position
             bool ok = true;
             const uint32_t d_s = tmem + C::col_s(i);
@@ -334,10 +345,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                     umma_ts(d_o, a_p + 8u * kk, b0 + ((kk * 16 * C::kRowBytes) >> 4), C::kIdescO,
                             (accumulate || kk > 0) ? 1u : 0u);
             };
-            // Next S_i; with P aliased into S_i the previous P_i V must have completed first.
+            // Next S_i.  The S_i columns must have been read by the softmax; with P aliased
+            // into them the previous P_i V must also have completed.
             auto do_s = [&](int q_bar, int stage, bool last) -> bool {
-                if (C::kAliasP && tiles > 0 && !mbar_wait(bar(kBarPVDone + i), (tiles - 1) & 1, limit, abort_flag))
-                    return false;
+                if (C::kAliasP) {
+                    if (tiles > 0 && !mbar_wait(bar(kBarPVDone + i), (tiles - 1) & 1, limit, abort_flag)) return false;
+                } else {
+                    if (s_issued > 0 && !mbar_wait(bar(kBarSFree + i), (s_issued - 1) & 1, limit, abort_flag))
+                        return false;
+                }
+                ++s_issued;
                 tc_fence_after_sync();
                 issue_s(q_bar, stage);
                 umma_commit(bar(kBarSFull + i));
@@ -374,17 +391,28 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                             break;
                         }
                     }
+                    // Without aliasing, S_i(j+1) only needs S_i(j) read: issue it before P_i(j) V_j,
+                    // so that it runs while the softmax of tile j is still exponentiating.
+                    if (!C::kAliasP && j + 1 < n) {
+                        const long long gn = gj + 1;
+                        const int sn = static_cast<int>(gn % S);
+                        if (!mbar_wait(bar(kBarKVFull + sn), static_cast<uint32_t>(gn / S) & 1, limit, abort_flag) ||
+                            !do_s(q_bar, sn, j + 1 == n - 1)) {
+                            ok = false;
+                            break;
+                        }
+                    }
                     if (!mbar_wait(bar(kBarPFull + i), tiles & 1, limit, abort_flag)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     issue_pv(sj, j > 0);
-                    if (C::kAliasP) umma_commit(bar(kBarPVDone + i));
+                    umma_commit(bar(kBarPVDone + i));
                     if (j == n - 1) umma_commit(bar(kBarOReady + i));
                     umma_commit(bar(kBarKVEmpty + sj));
                     ++tiles;
-                    if (j + 1 < n) {
+                    if (C::kAliasP && j + 1 < n) {
                         const long long gn = gj + 1;
                         const int sn = static_cast<int>(gn % S);
                         if (!mbar_wait(bar(kBarKVFull + sn), static_cast<uint32_t>(gn / S) & 1, limit, abort_flag) ||
@@ -402,7 +430,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             umma_commit(bar(kBarDrain + i));
             mbar_wait(bar(kBarDrain + i), 0, kDrainLimitNs, nullptr);
         }
+      }
     } else {
+        regs_increase<kSoftmaxRegs>();
         // ============================================================ softmax + epilogue
         const int wg = warp >> 2;               // query tile of this warpgroup
         const int r = threadIdx.x & 127;        // row within the tile == TMEM lane
@@ -436,6 +466,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]));
                 tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
                 tmem_ld_wait();
+                if constexpr (!C::kAliasP) {  // S_i is in registers: its columns may be overwritten
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(kBarSFree + wg));
+                }
                 float s[kBlockN];
 #pragma unroll
                 for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(u[c]);
@@ -479,16 +513,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                     pk[c / 2] = pack_bf16x2(p0, p1);
                     pk[c / 2 + 1] = pack_bf16x2(p2, p3);
                 }
-                // S_i(j) arrived, so P_i(j-1) V_{j-1} has completed: O_i and the P slot are free.
+                // O_i and the P_i columns are free once P_i(j-1) V_{j-1} has completed.  With P
+                // aliased into S_i this is implied by the arrival of S_i(j); otherwise wait for it.
+                if (!C::kAliasP && j > 0) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPVDone + wg), (tiles - 1) & 1, limit, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                }
                 if (j > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        tmem_ld32(t_o + 32u * c, o);
+                        uint32_t oc[32];
+                        tmem_ld32(t_o + 32u * c, oc);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                        tmem_st32(t_o + 32u * c, o);
+                        for (int e = 0; e < 32; ++e) oc[e] = __float_as_uint(__uint_as_float(oc[e]) * alpha);
+                        tmem_st32(t_o + 32u * c, oc);
                     }
                 }
                 tmem_st32(t_p + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
@@ -555,6 +595,16 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = true;
     }
+    static int regs[64] = {};  // registers per thread at launch, per device
+    if (dev >= 0 && dev < 64 && regs[dev] == 0) {
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, kern);
+        if (e != cudaSuccess) return e;
+        regs[dev] = attr.numRegs;
+    }
+    const int launch_regs = (dev >= 0 && dev < 64) ? regs[dev] : 0;
+    if (launch_regs * kFwdThreads < 256 * kSoftmaxRegs + 128 * kControlRegs)
+        return cudaErrorLaunchOutOfResources;  // the register split would not fit
     const int pairs = (p.n_items + 1) / 2;
     const int grid = pairs < p.num_ctas ? pairs : p.num_ctas;
     kern<<<grid, kFwdThreads, C::kSmemBytes, st>>>(p);
