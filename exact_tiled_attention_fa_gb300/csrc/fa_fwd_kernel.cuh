@@ -498,20 +498,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                     m_run = mt;
                 }
                 const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-                float rs0 = 0.f, rs1 = 0.f, rs2 = 0.f, rs3 = 0.f;
+                // Packed two-wide FP32 arithmetic (scale-and-subtract, row sums) halves the
+                // non-exponential instructions of this loop.
+                const float2 sl2x2 = make_float2(sl2, sl2);
+                const float2 negm = make_float2(-m_use, -m_use);
+                float2 rs01 = make_float2(0.f, 0.f), rs23 = make_float2(0.f, 0.f);
                 uint32_t pk[kBlockN / 2];
 #pragma unroll
                 for (int c = 0; c < kBlockN; c += 4) {
-                    const float p0 = ex2(fmaf(s[c + 0], sl2, -m_use));
-                    const float p1 = ex2(fmaf(s[c + 1], sl2, -m_use));
-                    const float p2 = ex2(fmaf(s[c + 2], sl2, -m_use));
-                    const float p3 = ex2(fmaf(s[c + 3], sl2, -m_use));
-                    rs0 += p0;
-                    rs1 += p1;
-                    rs2 += p2;
-                    rs3 += p3;
-                    pk[c / 2] = pack_bf16x2(p0, p1);
-                    pk[c / 2 + 1] = pack_bf16x2(p2, p3);
+                    const float2 x01 = __ffma2_rn(make_float2(s[c + 0], s[c + 1]), sl2x2, negm);
+                    const float2 x23 = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), sl2x2, negm);
+                    const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+                    const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+                    rs01 = __fadd2_rn(rs01, p01);
+                    rs23 = __fadd2_rn(rs23, p23);
+                    pk[c / 2] = pack_bf16x2(p01.x, p01.y);
+                    pk[c / 2 + 1] = pack_bf16x2(p23.x, p23.y);
                 }
                 // O_i and the P_i columns are free once P_i(j-1) V_{j-1} has completed.  With P
                 // aliased into S_i this is implied by the arrival of S_i(j); otherwise wait for it.
@@ -526,8 +528,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                         uint32_t oc[32];
                         tmem_ld32(t_o + 32u * c, oc);
                         tmem_ld_wait();
+                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) oc[e] = __float_as_uint(__uint_as_float(oc[e]) * alpha);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 v = __fmul2_rn(make_float2(__uint_as_float(oc[e]), __uint_as_float(oc[e + 1])), a2);
+                            oc[e] = __float_as_uint(v.x);
+                            oc[e + 1] = __float_as_uint(v.y);
+                        }
                         tmem_st32(t_o + 32u * c, oc);
                     }
                 }
@@ -536,7 +543,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 tmem_st_wait();
                 tc_fence_before_sync();
                 mbar_arrive(bar(kBarPFull + wg));
-                l = l * alpha + ((rs0 + rs1) + (rs2 + rs3));
+                l = l * alpha + ((rs01.x + rs01.y) + (rs23.x + rs23.y));
                 ++tiles;
             }
             if (!ok) break;
