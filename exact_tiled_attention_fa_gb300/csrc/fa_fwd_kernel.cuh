@@ -461,10 +461,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 if (!ok) break;
                 tc_fence_after_sync();
                 uint32_t u[kBlockN];
-                tmem_ld32(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-                tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-                tmem_ld32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]));
-                tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]));
+                float mq[4];  // per 32-column maxima, reduced by the TMEM load itself
+                tmem_ld32_max(t_s + 0, *reinterpret_cast<uint32_t(*)[32]>(&u[0]), mq[0]);
+                tmem_ld32_max(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]), mq[1]);
+                tmem_ld32_max(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(&u[64]), mq[2]);
+                tmem_ld32_max(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]), mq[3]);
                 tmem_ld_wait();
                 if constexpr (!C::kAliasP) {  // S_i is in registers: its columns may be overwritten
                     tc_fence_before_sync();
@@ -475,20 +476,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(u[c]);
                 const int k0 = j * kBlockN;
                 const bool need_mask = (k0 + kBlockN > p.Nk) || (CAUSAL && k0 + kBlockN - 1 > off + row0);
-                if (need_mask) {
+                if (need_mask) {  // diagonal or ragged tile: mask, then take the max in registers
                     const int last = CAUSAL ? min(qpos, p.Nk - 1) : p.Nk - 1;  // last visible key
 #pragma unroll
                     for (int c = 0; c < kBlockN; ++c)
                         if (k0 + c > last) s[c] = -INFINITY;
-                }
-                float mq[4];  // row max: four independent 3-input max chains of 32 columns
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float* t = s + 32 * q;
-                    float a = max3(t[0], t[1], t[2]);
+                    for (int q = 0; q < 4; ++q) {
+                        const float* t = s + 32 * q;
+                        float a = max3(t[0], t[1], t[2]);
 #pragma unroll
-                    for (int c = 3; c < 31; c += 2) a = max3(a, t[c], t[c + 1]);
-                    mq[q] = fmaxf(a, t[31]);
+                        for (int c = 3; c < 31; c += 2) a = max3(a, t[c], t[c + 1]);
+                        mq[q] = fmaxf(a, t[31]);
+                    }
                 }
                 const float mt = max3(mq[0], mq[1], fmaxf(mq[2], mq[3])) * sl2;
                 const bool grow = mt > m_run;
@@ -498,6 +498,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                     m_run = mt;
                 }
                 const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+                // Test now whether P_i(j-1) V_{j-1} has completed; the answer is needed only
+                // after the exponentials, so the barrier's latency overlaps them.
+                const bool pv_ready = C::kAliasP || j == 0 || mbar_test(bar(kBarPVDone + wg), (tiles - 1) & 1);
                 // Packed two-wide FP32 arithmetic (scale-and-subtract, row sums) halves the
                 // non-exponential instructions of this loop.
                 const float2 sl2x2 = make_float2(sl2, sl2);
@@ -518,7 +521,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 // O_i and the P_i columns are free once P_i(j-1) V_{j-1} has completed.  With P
                 // aliased into S_i this is implied by the arrival of S_i(j); otherwise wait for it.
                 if (!C::kAliasP && j > 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarPVDone + wg), (tiles - 1) & 1, limit, abort_flag));
+                    ok = __all_sync(0xffffffffu,
+                                    pv_ready || mbar_wait(bar(kBarPVDone + wg), (tiles - 1) & 1, limit, abort_flag));
                     if (!ok) break;
                     tc_fence_after_sync();
                 }
