@@ -46,7 +46,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture, keyed by
 # the SHA-256 of the kernel source it was taken on; reported only while the source is unchanged.
-KERNEL_TRAFFIC = {}
+KERNEL_TRAFFIC = {
+    # profiles/fa_fwd_kernel_d64_gpt2medium_prefill.md: non-causal launch, 402.87 MB read + 108.18 MB written
+    "5edcc810dbab2d56202fac3f0222a8491a770d00cc9650288296e487cd453b08": 511.05e6,
+}
 
 
 def fwd_flops(B, H, N, Nk, d, causal):
