@@ -144,7 +144,8 @@ def max_over_ranks(x, world):
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -294,6 +295,8 @@ def run_ours(args, world, rank, local):
     }
     if decode is not None:
         line["decode"] = decode
+    if not args.no_extra:
+        line["other_fwd_configs"] = run_other_fwd(fa, dev, stream, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, fl, threads, desc = oracle_sample(args.cpu_slices)
         line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -342,6 +345,45 @@ def run_e2e(fa, dev, stream, args, world, inputs, outputs, scale, flops_per_step
     return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+# The other forward configurations of the parity suite, timed the same way (not the headline):
+# (name, B, H, N, Nk, d, input multiplier, causal)
+OTHER_FWD = (
+    ("single head 256x256 d=64", 1, 1, 256, 256, 64, 1.0, False),
+    ("single head 256x256 d=64 causal", 1, 1, 256, 256, 64, 1.0, True),
+    ("ragged 4097 d=128 x2", 4, 16, 4097, 4097, 128, 2.0, False),
+    ("ragged 4097 d=128 x2 causal", 4, 16, 4097, 4097, 128, 2.0, True),
+    ("ragged 77x513 d=32 x2 causal", 8, 8, 77, 513, 32, 2.0, True),
+    ("long causal 16384 d=128", 2, 32, 16384, 16384, 128, 1.0, True),
+)
+
+
+def run_other_fwd(fa, dev, stream, args, world):
+    pk, _ = peaks()
+    peak = float(pk["bf16_tflops"])
+    out = {}
+    for name, B, H, N, Nk, d, mult, causal in OTHER_FWD:
+        q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=0, mult=mult, device=dev)
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        for _ in range(max(args.warmup, 3)):
+            fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
+        steps = max(5, args.steps // 10)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(steps):
+            fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+        fl = fwd_flops(B, H, N, Nk, d, causal)
+        out[name] = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12, "frac_of_peak": fl / (ms / 1e3) / 1e12 / peak,
+                     "flops": fl}
+        del q, k, v, o, lse
+    assert fa.get_device_error(dev) == fa.FA_OK
+    return out
+
+
 def run_decode(fa, dev, stream, args, world):
     B, H, Nk_max, d = DEC["B"], DEC["H"], DEC["Nk_max"], DEC["d"]
     q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=0, lo=DEC["lo"], hi=DEC["hi"], device=dev)
@@ -382,6 +424,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true", help="skip the split-KV decode measurement")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end (host buffers) measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other forward configurations")
     ap.add_argument("--decode-only", action="store_true", help="only the split-KV decode (profiling)")
     ap.add_argument("--decode-batch", type=int, default=DEC["B"], help="decode batch (smaller cache for profiling)")
     ap.add_argument("--cpu-slices", type=int, default=1024)
