@@ -52,6 +52,8 @@ def open_library(path):
     lib.oracle_decode.restype = i
     lib.oracle_merge_lse.argtypes = [dp, dp, L, L, L, dp, dp]
     lib.oracle_merge_lse.restype = i
+    lib.oracle_attention_bwd.argtypes = [vp, vp, vp, vp, i, L, L, L, L, L, i, d, dp, dp, dp, i]
+    lib.oracle_attention_bwd.restype = i
     return lib
 
 
@@ -117,6 +119,34 @@ def attention(q, k, v, causal=False, scale=None, rows=None, threads=None, lib=No
     if rc != 0:
         raise RuntimeError(f"oracle_attention failed with code {rc}")
     return O.reshape(lead + (nr, dv)), LSE.reshape(lead + (nr,))
+
+
+def attention_bwd(q, k, v, do, causal=False, scale=None, threads=None, lib=None):
+    """Gradients (dQ, dK, dV) of standard attention for the upstream gradient ``do``.
+
+    Shapes [..., N, d] / [..., Nk, d] / [..., Nk, dv] / [..., N, dv]; leading
+    dimensions are independent heads.  Returns float64 numpy arrays.
+    """
+    qs, vs = tuple(q.shape), tuple(v.shape)
+    lead = qs[:-2]
+    N, d = qs[-2], qs[-1]
+    Nk, dv = vs[-2], vs[-1]
+    assert tuple(k.shape) == lead + (Nk, d) and tuple(do.shape) == lead + (N, dv)
+    BH = int(np.prod(lead)) if lead else 1
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    ins = [_as_input(t) for t in (q, k, v, do)]
+    if len({f for _, _, f in ins}) != 1:  # mixed input types: widen everything to float64
+        ins = [_as_input(np.asarray(_widen(t))) for t in (q, k, v, do)]
+    (bq, pq, fq), (bk, pk, _), (bv, pv, _), (bg, pg, _) = ins
+    dQ = np.zeros((BH, N, d))
+    dK = np.zeros((BH, Nk, d))
+    dV = np.zeros((BH, Nk, dv))
+    rc = (lib or _load()).oracle_attention_bwd(pq, pk, pv, pg, fq, BH, N, Nk, d, dv, int(bool(causal)), scale,
+                                               dQ.ctypes.data, dK.ctypes.data, dV.ctypes.data,
+                                               threads or cores())
+    if rc != 0:
+        raise RuntimeError(f"oracle_attention_bwd failed with code {rc}")
+    return dQ.reshape(lead + (N, d)), dK.reshape(lead + (Nk, d)), dV.reshape(lead + (Nk, dv))
 
 
 def decode(q, k_cache, v_cache, seqlens, scale=None, threads=None, lib=None):

@@ -15,6 +15,9 @@
  *                section 1 `softmax_3pass`, section 2 `_causal_mask` and
  *                `standard_attention`, section 3 `flash_fwd` (L = m + log l),
  *                section 4 `split_kv_decode` (lse merge).
+ *                section 2 `standard_attention_bwd` (dV = P^T dO, dP = dO V^T,
+ *                dS = P o (dP - D) with D_i = sum dO_i o O_i, dQ = dS K scale,
+ *                dK = dS^T Q scale).
  *   [fwd_demo]   "02_flash_forward.py -- FlashAttention forward" (CS349E
  *                lecture 11), demo 1: causal position convention for N != Nk.
  *
@@ -337,4 +340,164 @@ int oracle_merge_lse(const double* o_parts, const double* lse_parts, long P, lon
         }
     }
     return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------- */
+/* backward of standard attention                                          */
+/* ---------------------------------------------------------------------- */
+typedef struct {
+    const void *Q, *K, *V, *dO;
+    int bf16;
+    long BH, N, Nk, d, dv;
+    int causal;
+    double scale;
+    double *dQ, *dK, *dV;
+    long next;
+    pthread_mutex_t lock;
+    int failed;
+} bwd_job_t;
+
+static long bwd_take(bwd_job_t* jb)
+{
+    pthread_mutex_lock(&jb->lock);
+    long it = jb->next < jb->BH ? jb->next++ : -1;
+    pthread_mutex_unlock(&jb->lock);
+    return it;
+}
+
+static const double* bwd_fetch(const bwd_job_t* jb, const void* src, long off, long n, double* buf)
+{
+    if (jb->bf16) {
+        widen_bf16((const uint16_t*)src + off, buf, n);
+        return buf;
+    }
+    return (const double*)src + off;
+}
+
+/*
+ * One head of [flash_lab] section 2 `standard_attention_bwd`, one query row
+ * at a time.  For row i:
+ *   P[i, :] from the forward definition (masked scores, 3-pass softmax);
+ *   O[i, :]  = sum_j P[i, j] V[j, :]
+ *   D[i]     = sum_c dO[i, c] O[i, c]
+ *   dP[i, j] = sum_c dO[i, c] V[j, c]
+ *   dS[i, j] = P[i, j] (dP[i, j] - D[i])
+ *   dQ[i, :] = scale sum_j dS[i, j] K[j, :]
+ *   dK[j, :] += scale dS[i, j] Q[i, :]      (summed over all rows i)
+ *   dV[j, :] += P[i, j] dO[i, :]            (summed over all rows i)
+ * A row with no visible key has a zero P row and contributes nothing.
+ */
+static void bwd_head(const double* Q, const double* K, const double* V, const double* dO, long N, long Nk,
+                     long d, long dv, int causal, double scale, double* p, double* orow, double* dQ,
+                     double* dK, double* dV)
+{
+    for (long j = 0; j < Nk * d; ++j) dK[j] = 0.0;
+    for (long j = 0; j < Nk * dv; ++j) dV[j] = 0.0;
+    for (long i = 0; i < N; ++i) {
+        const double* q = Q + i * d;
+        const double* g = dO + i * dv;
+        double* dq = dQ + i * d;
+        for (long c = 0; c < d; ++c) dq[c] = 0.0;
+        long qpos = causal ? Nk - N + i : Nk; /* [fwd_demo] demo 1 */
+        /* scores, masked */
+        for (long j = 0; j < Nk; ++j) {
+            if (j > qpos) {
+                p[j] = -INFINITY;
+                continue;
+            }
+            double acc = 0.0;
+            for (long c = 0; c < d; ++c) acc += q[c] * K[j * d + c];
+            p[j] = acc * scale;
+        }
+        /* 3-pass softmax: max, sum of exp, divide */
+        double m = -INFINITY;
+        for (long j = 0; j < Nk; ++j)
+            if (p[j] > m) m = p[j];
+        if (m == -INFINITY) continue; /* no visible key */
+        double l = 0.0;
+        for (long j = 0; j < Nk; ++j) {
+            p[j] = exp(p[j] - m);
+            l += p[j];
+        }
+        for (long j = 0; j < Nk; ++j) p[j] /= l;
+        /* O row and D */
+        for (long c = 0; c < dv; ++c) orow[c] = 0.0;
+        for (long j = 0; j < Nk; ++j)
+            for (long c = 0; c < dv; ++c) orow[c] += p[j] * V[j * dv + c];
+        double D = 0.0;
+        for (long c = 0; c < dv; ++c) D += g[c] * orow[c];
+        /* dP, dS and the three products */
+        for (long j = 0; j < Nk; ++j) {
+            if (j > qpos) continue; /* masked key: P = 0 and dS = 0 */
+            double dp = 0.0;
+            for (long c = 0; c < dv; ++c) dp += g[c] * V[j * dv + c];
+            double ds = p[j] * (dp - D);
+            for (long c = 0; c < d; ++c) dq[c] += scale * ds * K[j * d + c];
+            for (long c = 0; c < d; ++c) dK[j * d + c] += scale * ds * q[c];
+            for (long c = 0; c < dv; ++c) dV[j * dv + c] += p[j] * g[c];
+        }
+    }
+}
+
+static void* bwd_worker(void* arg)
+{
+    bwd_job_t* jb = (bwd_job_t*)arg;
+    long nq = jb->N * jb->d, nk = jb->Nk * jb->d, nv = jb->Nk * jb->dv, ng = jb->N * jb->dv;
+    double* p = malloc(sizeof(double) * (size_t)(jb->Nk + 1));
+    double* orow = malloc(sizeof(double) * (size_t)jb->dv);
+    double* buf = jb->bf16 ? malloc(sizeof(double) * (size_t)(nq + nk + nv + ng + 1)) : NULL;
+    if (!p || !orow || (jb->bf16 && !buf)) {
+        pthread_mutex_lock(&jb->lock);
+        jb->failed = 1;
+        pthread_mutex_unlock(&jb->lock);
+        free(p); free(orow); free(buf);
+        return NULL;
+    }
+    long bh;
+    while ((bh = bwd_take(jb)) >= 0) {
+        const double* Q = bwd_fetch(jb, jb->Q, bh * nq, nq, buf);
+        const double* K = bwd_fetch(jb, jb->K, bh * nk, nk, buf ? buf + nq : NULL);
+        const double* V = bwd_fetch(jb, jb->V, bh * nv, nv, buf ? buf + nq + nk : NULL);
+        const double* G = bwd_fetch(jb, jb->dO, bh * ng, ng, buf ? buf + nq + nk + nv : NULL);
+        bwd_head(Q, K, V, G, jb->N, jb->Nk, jb->d, jb->dv, jb->causal, jb->scale, p, orow,
+                 jb->dQ + bh * nq, jb->dK + bh * nk, jb->dV + bh * nv);
+    }
+    free(p); free(orow); free(buf);
+    return NULL;
+}
+
+/*
+ * Gradients of standard attention over BH independent heads for the upstream
+ * gradient dO ([flash_lab] section 2 `standard_attention_bwd`).  Q [BH,N,d],
+ * K [BH,Nk,d], V [BH,Nk,dv], dO [BH,N,dv], all float64 (bf16 = 0) or all bf16
+ * bit patterns (bf16 = 1).  dQ [BH,N,d], dK [BH,Nk,d], dV [BH,Nk,dv] float64.
+ * One head per work item; heads run on `nthreads` threads.
+ */
+int oracle_attention_bwd(const void* Q, const void* K, const void* V, const void* dO, int bf16, long BH,
+                         long N, long Nk, long d, long dv, int causal, double scale, double* dQ,
+                         double* dK, double* dV, int nthreads)
+{
+    if (!Q || !K || !V || !dO || !dQ || !dK || !dV || BH < 0 || N < 0 || Nk < 0 || d <= 0 || dv <= 0)
+        return ORACLE_ERR_ARG;
+    if (BH == 0) return ORACLE_OK;
+    bwd_job_t jb;
+    memset(&jb, 0, sizeof jb);
+    jb.Q = Q; jb.K = K; jb.V = V; jb.dO = dO; jb.bf16 = bf16;
+    jb.BH = BH; jb.N = N; jb.Nk = Nk; jb.d = d; jb.dv = dv;
+    jb.causal = causal; jb.scale = scale;
+    jb.dQ = dQ; jb.dK = dK; jb.dV = dV;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    if (BH < nthreads) nthreads = (int)BH;
+    pthread_t th[256];
+    pthread_mutex_init(&jb.lock, NULL);
+    int started = 0;
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&th[t], NULL, bwd_worker, &jb) != 0) break;
+        ++started;
+    }
+    bwd_worker(&jb);
+    for (int t = 1; t <= started; ++t) pthread_join(th[t], NULL);
+    pthread_mutex_destroy(&jb.lock);
+    return jb.failed ? ORACLE_ERR_NOMEM : ORACLE_OK;
 }

@@ -10,6 +10,7 @@ It restates, in float64 and in the pages' own notation, the algorithms of
 * section 1 (online softmax): ``softmax_3pass``, ``softmax_online``,
   ``partial_state``, ``merge_states``;
 * section 2 (standard attention): ``causal_mask``, ``standard_attention``;
+* section 2 (standard attention backward): ``standard_attention_bwd``;
 * section 3 (FlashAttention): ``flash_fwd_tiled`` -- the FlashAttention-2 loop
   order (outer loop over query tiles, inner loop over key/value tiles, the
   running max m and sum l rescaled by exp(m_old - m_new), one division by l
@@ -112,6 +113,23 @@ def standard_attention(Q, K, V, causal=False, scale=None):
     return O, lse, P
 
 
+def standard_attention_bwd(Q, K, V, dO, causal=False, scale=None):
+    """Backward of standard attention with the full P materialised.
+
+    dV = P^T dO; dP = dO V^T; D_i = sum_c dO_ic O_ic; dS = P o (dP - D);
+    dQ = dS K scale; dK = dS^T Q scale.  Returns (dQ, dK, dV).
+    """
+    Q, K, V, dO = (np.asarray(t, dtype=np.float64) for t in (Q, K, V, dO))
+    d = Q.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    O, _, P = standard_attention(Q, K, V, causal, scale)
+    D = np.sum(dO * O, axis=1)
+    dV = P.T @ dO
+    dP = dO @ V.T
+    dS = P * (dP - D[:, None])
+    return dS @ K * scale, dS.T @ Q * scale, dV
+
+
 # --------------------------------------------------------------------------
 # section 3: FlashAttention, FlashAttention-2 loop order (tiled model)
 # --------------------------------------------------------------------------
@@ -161,6 +179,52 @@ def flash_fwd_tiled(Q, K, V, Br, Bc, causal=False, scale=None):
             O[i0:i0 + br] = np.where(seen[:, None], acc / np.where(seen, l, 1.0)[:, None], 0.0)
             L[i0:i0 + br] = np.where(seen, m + np.log(np.where(seen, l, 1.0)), -np.inf)
     return O, L, visited
+
+
+def flash_bwd_tiled(Q, K, V, O, dO, L, Br, Bc, causal=False, scale=None):
+    """Tiled backward in the FlashAttention-2 order (recompute S and P from L).
+
+    D_i = sum dO_i o O_i first.  The outer loop walks key/value tiles j (their
+    dK_j, dV_j accumulate on chip), the inner loop walks query tiles i, skipping
+    a tile whose last query position lies before the key tile's first key.
+    Per (i, j): S = Q_i K_j^T scale (masked), P = exp(S - L_i),
+    dV_j += P^T dO_i, dP = dO_i V_j^T, dS = P o (dP - D_i),
+    dQ_i += dS K_j scale, dK_j += dS^T Q_i scale.
+
+    Returns (dQ, dK, dV, visited) with ``visited`` the (query tile, key tile)
+    pairs computed.  A row with L = -inf (no visible key) gets P = 0.
+    """
+    Q, K, V, O, dO = (np.asarray(t, dtype=np.float64) for t in (Q, K, V, O, dO))
+    L = np.asarray(L, dtype=np.float64)
+    N, d = Q.shape
+    Nk, dv = V.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    off = Nk - N
+    D = (dO * O).sum(axis=1)
+    dQ, dK, dV = np.zeros((N, d)), np.zeros((Nk, d)), np.zeros((Nk, dv))
+    visited = []
+    for j0 in range(0, Nk, Bc):
+        bc = min(Bc, Nk - j0)
+        dKj, dVj = np.zeros((bc, d)), np.zeros((bc, dv))
+        for i0 in range(0, N, Br):
+            br = min(Br, N - i0)
+            if causal and off + i0 + br - 1 < j0:
+                continue
+            visited.append((i0 // Br, j0 // Bc))
+            S = (Q[i0:i0 + br] @ K[j0:j0 + bc].T) * scale
+            if causal:
+                S = np.where(causal_mask(br, bc, i0, j0, off), S, -np.inf)
+            Li = L[i0:i0 + br, None]
+            with np.errstate(invalid="ignore"):
+                P = np.where(np.isneginf(Li), 0.0, np.exp(S - np.where(np.isneginf(Li), 0.0, Li)))
+            dVj += P.T @ dO[i0:i0 + br]
+            dP = dO[i0:i0 + br] @ V[j0:j0 + bc].T
+            dS = P * (dP - D[i0:i0 + br, None])
+            dQ[i0:i0 + br] += dS @ K[j0:j0 + bc] * scale
+            dKj += dS.T @ Q[i0:i0 + br] * scale
+        dK[j0:j0 + bc] = dKj
+        dV[j0:j0 + bc] = dVj
+    return dQ, dK, dV, visited
 
 
 # --------------------------------------------------------------------------

@@ -165,3 +165,111 @@ def check_one_hot(attention, seed=5):
 def run_all(attention):
     return (check_golden(attention) + check_brute(attention, shapes=((77, 513, 32), (7, 33, 8), (1, 1000, 64)))
             + check_q_zero(attention) + check_causal_first_row(attention) + check_one_hot(attention))
+
+
+# --------------------------------------------------------------------------
+# backward pins
+# --------------------------------------------------------------------------
+# Each check takes ``bwd(q, k, v, do, causal, scale) -> (dQ, dK, dV)``.  None of
+# them re-runs the oracle's own formula:
+#   * hand-derived fixtures under ``tests/golden/`` (bwd_*.json);
+#   * central finite differences of f = sum(O o dO), with O from the pure-Python
+#     brute-force forward above, for every input entry (the flash_lab.py
+#     self-test checks one entry of dQ this way with eps 1e-6 and tolerance 1e-7);
+#   * invariants that follow from softmax rows summing to 1 and from f being
+#     bilinear in (Q, K) and linear in V;
+#   * torch autograd through the plain float64 forward (an independent library).
+BWD_GOLDEN = ("bwd_two_keys.json", "bwd_causal_uniform.json", "bwd_no_visible_key.json")
+
+
+def check_bwd_golden(bwd):
+    bad = []
+    for name in BWD_GOLDEN:
+        g = load_golden(name)
+        dQ, dK, dV = bwd(g["Q"], g["K"], g["V"], g["dO"], g["causal"], g["scale"])
+        if not (_close(dQ, g["dQ"], g["tol"]) and _close(dK, g["dK"], g["tol"]) and _close(dV, g["dV"], g["tol"])):
+            bad.append(f"bwd golden {name}")
+    return bad
+
+
+def _objective(Q, K, V, dO, causal, scale):
+    O, _ = brute_attention(Q, K, V, causal, scale)
+    return math.fsum((O * dO).ravel().tolist())
+
+
+def check_bwd_finite_differences(bwd, seed=21, eps=1e-6, tol=1e-7):
+    """Every entry of dQ, dK, dV against a central difference of sum(O o dO)."""
+    bad = []
+    rng = np.random.default_rng(seed)
+    for (N, Nk, d, dv, causal) in ((5, 7, 3, 2, False), (5, 7, 3, 2, True), (6, 4, 3, 2, True)):
+        Q, K, V = rng.standard_normal((N, d)), rng.standard_normal((Nk, d)), rng.standard_normal((Nk, dv))
+        dO = rng.standard_normal((N, dv))
+        scale = 0.7
+        grads = bwd(Q, K, V, dO, causal, scale)
+        for which, (X, G) in enumerate(zip((Q, K, V), grads)):
+            num = np.zeros_like(X)
+            for idx in np.ndindex(X.shape):
+                args_p = [Q.copy(), K.copy(), V.copy()]
+                args_m = [Q.copy(), K.copy(), V.copy()]
+                args_p[which][idx] += eps
+                args_m[which][idx] -= eps
+                num[idx] = (_objective(*args_p, dO, causal, scale) - _objective(*args_m, dO, causal, scale)) / (2 * eps)
+            if not _close(G, num, tol):
+                bad.append(f"finite difference {'QKV'[which]} N={N} Nk={Nk} causal={causal}")
+    return bad
+
+
+def check_bwd_invariants(bwd, seed=22):
+    """Rows of dS sum to 0 (so sum_j dK_j = 0); sum_j dV_j = sum_i dO_i; Euler identities
+    sum dQ o Q = sum dK o K (scores bilinear in Q, K) and sum dV o V = sum O o dO (O linear in V);
+    equal key rows give dQ = 0."""
+    bad = []
+    rng = np.random.default_rng(seed)
+    for (N, Nk, d, dv, causal) in ((19, 41, 16, 6, False), (23, 23, 8, 8, True), (9, 30, 4, 5, True)):
+        Q, K, V = rng.standard_normal((N, d)), rng.standard_normal((Nk, d)), rng.standard_normal((Nk, dv))
+        dO = rng.standard_normal((N, dv))
+        scale = 0.4
+        dQ, dK, dV = (np.asarray(x) for x in bwd(Q, K, V, dO, causal, scale))
+        O, _ = brute_attention(Q, K, V, causal, scale)
+        tag = f"N={N} Nk={Nk} causal={causal}"
+        if not _close(dK.sum(axis=0), np.zeros(d), 1e-12):
+            bad.append(f"sum dK {tag}")
+        if not _close(dV.sum(axis=0), dO.sum(axis=0), 1e-12):
+            bad.append(f"sum dV {tag}")
+        if abs(float((dQ * Q).sum() - (dK * K).sum())) > 1e-11:
+            bad.append(f"euler QK {tag}")
+        if abs(float((dV * V).sum() - (O * dO).sum())) > 1e-11:
+            bad.append(f"euler V {tag}")
+        Kc = np.repeat(rng.standard_normal((1, d)), Nk, axis=0)
+        dQc, _, _ = bwd(Q, Kc, V, dO, causal, scale)
+        if not _close(dQc, np.zeros((N, d)), 1e-12):
+            bad.append(f"equal keys dQ {tag}")
+    return bad
+
+
+def check_bwd_autograd(bwd, seed=23):
+    """torch autograd (float64, CPU) through S = Q K^T scale, mask, softmax, O = P V."""
+    import torch
+    bad = []
+    g = torch.Generator().manual_seed(seed)
+    for (N, Nk, d, dv, causal) in ((33, 33, 16, 16, True), (20, 45, 8, 12, False), (1, 300, 32, 32, False)):
+        Q, K, V = (torch.randn(s, generator=g, dtype=torch.float64, requires_grad=True)
+                   for s in ((N, d), (Nk, d), (Nk, dv)))
+        dO = torch.randn((N, dv), generator=g, dtype=torch.float64)
+        scale = 1.0 / math.sqrt(d)
+        S = Q @ K.T * scale
+        if causal:
+            S = S.masked_fill(torch.arange(Nk)[None, :] > (Nk - N + torch.arange(N))[:, None], float("-inf"))
+        O = torch.softmax(S, dim=-1) @ V
+        O.backward(dO)
+        ref = [t.grad.numpy() for t in (Q, K, V)]
+        got = bwd(Q.detach().numpy(), K.detach().numpy(), V.detach().numpy(), dO.numpy(), causal, scale)
+        for name, a, b in zip("QKV", got, ref):
+            if not _close(a, b, 1e-12):
+                bad.append(f"autograd d{name} N={N} Nk={Nk} causal={causal}")
+    return bad
+
+
+def run_all_bwd(bwd):
+    return (check_bwd_golden(bwd) + check_bwd_finite_differences(bwd) + check_bwd_invariants(bwd)
+            + check_bwd_autograd(bwd))

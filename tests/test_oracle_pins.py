@@ -211,7 +211,7 @@ def test_row_subset_matches_full():
 # Mistakes a hand-written attention is likely to contain, planted in a copy of
 # the oracle's C source.  Every one of them must make at least one pin fail.
 MUTATIONS = {
-    "mask_off_by_one": ("if (j > qpos) {", "if (j >= qpos) {"),
+    "mask_off_by_one": ("if (j > qpos) {\n            s[j] = -INFINITY;", "if (j >= qpos) {\n            s[j] = -INFINITY;"),
     "dropped_scale": ("s[j] = acc * scale;", "s[j] = acc;"),
     "wrong_sign_in_exp": ("s[j] = exp(s[j] - m);", "s[j] = exp(s[j] + m);"),
     "dropped_max_in_lse": ("*lse = m + log(l);", "*lse = log(l);"),
@@ -255,4 +255,82 @@ def test_planted_mistakes_are_caught(tmp_path):
                 return [] if pins._close(Om, Ob, 1e-12) and pins._close(Lm, Lb, 1e-12) else ["bf16 brute"]
             failures = bf16_pin()
         assert failures, f"planted mistake {name} was not caught by any pin"
+    shutil.rmtree(tmp_path, ignore_errors=True)
+
+
+# --------------------------------------------------------------------------
+# backward
+# --------------------------------------------------------------------------
+def c_attention_bwd(Q, K, V, dO, causal, scale, lib=None):
+    return oracle.attention_bwd(np.asarray(Q), np.asarray(K), np.asarray(V), np.asarray(dO), causal=causal,
+                                scale=scale, lib=lib)
+
+
+def np_attention_bwd(Q, K, V, dO, causal, scale):
+    return no.standard_attention_bwd(Q, K, V, dO, causal, scale)
+
+
+@pytest.mark.parametrize("impl", [c_attention_bwd, np_attention_bwd], ids=["c", "numpy"])
+def test_bwd_pins(impl):
+    assert pins.run_all_bwd(impl) == []
+
+
+@pytest.mark.parametrize("N,Nk,Br,Bc", [(12, 12, 4, 5), (77, 513, 128, 128), (300, 200, 128, 128),
+                                         (200, 300, 37, 64)])
+def test_tiled_bwd_model_matches_oracle_and_skips_exactly_masked_tiles(N, Nk, Br, Bc):
+    """The FlashAttention-2-order backward (recompute P from L) equals the definition; the
+    (query tile, key tile) pairs it skips are exactly those with no visible pair."""
+    rng = np.random.default_rng(31)
+    d = dv = 8
+    Q, K, V = rng.standard_normal((N, d)), rng.standard_normal((Nk, d)), rng.standard_normal((Nk, dv))
+    dO = rng.standard_normal((N, dv))
+    for causal in (False, True):
+        O, L = oracle.attention(Q, K, V, causal=causal, scale=0.3)
+        dQ, dK, dV, visited = no.flash_bwd_tiled(Q, K, V, O, dO, L, Br, Bc, causal, 0.3)
+        ref = oracle.attention_bwd(Q, K, V, dO, causal=causal, scale=0.3)
+        for a, b in zip((dQ, dK, dV), ref):
+            assert np.abs(a - b).max() < 1e-12
+        mask = no.causal_mask(N, Nk, offset=Nk - N) if causal else np.ones((N, Nk), bool)
+        want = {(i, j) for i in range(-(-N // Br)) for j in range(-(-Nk // Bc))
+                if mask[i * Br:(i + 1) * Br, j * Bc:(j + 1) * Bc].any()}
+        assert set(visited) == want
+
+
+def test_bwd_bf16_inputs_are_widened_exactly():
+    rng = np.random.default_rng(32)
+    t = [torch.tensor(rng.standard_normal(s)).to(torch.bfloat16) for s in ((2, 9, 16), (2, 14, 16), (2, 14, 8),
+                                                                          (2, 9, 8))]
+    got = oracle.attention_bwd(*t, causal=True, scale=0.25)
+    want = oracle.attention_bwd(*(x.double() for x in t), causal=True, scale=0.25)
+    for a, b in zip(got, want):
+        assert np.array_equal(a, b)
+
+
+BWD_MUTATIONS = {
+    "dropped_D": ("double ds = p[j] * (dp - D);", "double ds = p[j] * dp;"),
+    "D_sign": ("double ds = p[j] * (dp - D);", "double ds = p[j] * (dp + D);"),
+    "dq_without_scale": ("dq[c] += scale * ds * K[j * d + c];", "dq[c] += ds * K[j * d + c];"),
+    "dk_from_k": ("dK[j * d + c] += scale * ds * q[c];", "dK[j * d + c] += scale * ds * K[j * d + c];"),
+    "dv_from_ds": ("dV[j * dv + c] += p[j] * g[c];", "dV[j * dv + c] += ds * g[c];"),
+    "dp_from_k": ("dp += g[c] * V[j * dv + c];", "dp += g[c] * K[j * d + c % d];"),
+    "mask_off_by_one": ("            if (j > qpos) {\n                p[j] = -INFINITY;",
+                        "            if (j >= qpos) {\n                p[j] = -INFINITY;"),
+    "top_left_causal": ("long qpos = causal ? Nk - N + i : Nk;", "long qpos = causal ? i : Nk;"),
+    "unnormalised_p": ("for (long j = 0; j < Nk; ++j) p[j] /= l;", "(void)l;"),
+}
+
+
+def test_bwd_planted_mistakes_are_caught(tmp_path):
+    src = os.path.join(os.path.dirname(oracle.__file__), "fa_oracle.c")
+    text = open(src).read()
+    for name, (old, new) in BWD_MUTATIONS.items():
+        assert text.count(old) == 1, name
+        path = tmp_path / f"mutbwd_{name}.c"
+        path.write_text(text.replace(old, new))
+        lib = oracle.open_library(oracle.compile_library(str(path), str(tmp_path / f"libmutbwd_{name}.so")))
+
+        def mutated(Q, K, V, dO, causal, scale, _lib=lib):
+            return c_attention_bwd(Q, K, V, dO, causal, scale, lib=_lib)
+
+        assert pins.run_all_bwd(mutated), f"planted mistake {name} was not caught by any pin"
     shutil.rmtree(tmp_path, ignore_errors=True)
