@@ -7,6 +7,7 @@ missing or cannot be loaded, every entry point raises.
 
 Entry points (same names as the C ABI, without the ``fa_`` prefix):
   fwd              exact attention forward (tiled, online softmax)
+  bwd              exact attention backward (dQ, dK, dV; P recomputed from LSE)
   decode_splitkv   split-KV single-query decode with log-sum-exp combine
   merge_states     log-sum-exp combine of partial states
   decode_default_splits, decode_workspace_size, get_device_error,
@@ -47,6 +48,10 @@ def _load():
     vp, i, f, sz, ull = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_ulonglong
     lib.fa_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
     lib.fa_fwd.restype = i
+    lib.fa_bwd_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_bwd_workspace_size.restype = sz
+    lib.fa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, i, f, i, i, vp]
+    lib.fa_bwd.restype = i
     lib.fa_decode_default_splits.argtypes = [i, i, i, i]
     lib.fa_decode_default_splits.restype = i
     lib.fa_decode_workspace_size.argtypes = [i, i, i, i]
@@ -139,6 +144,52 @@ def fwd(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, out=None, l
                         scale, _odt(out.dtype), _stream(dev))
     _check(st, "fa_fwd")
     return out, lse
+
+
+def bwd_workspace_size(B, H, N, d):
+    return int(_load().fa_bwd_workspace_size(B, H, N, d))
+
+
+def bwd(q, k, v, o, lse, do, causal=False, scale=None, out_dtype=torch.bfloat16, grads=None, workspace=None):
+    """Exact attention backward for the upstream gradient ``do`` of the forward output ``o``.
+
+    q [B,H,N,d], k [B,H,Nk,d], v [B,H,Nk,dv], do [B,H,N,dv] bf16; o [B,H,N,dv] bf16 or fp32 and
+    lse fp32 [B,H,N] as returned by ``fwd`` with the same ``causal`` and ``scale``.  ``grads`` is an
+    optional (dq, dk, dv) triple to write into; ``workspace`` a uint8 CUDA tensor of at least
+    ``bwd_workspace_size`` bytes (allocated here when omitted).  Returns (dq, dk, dv) of ``out_dtype``.
+    """
+    lib = _load()
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    _need(k, "k", torch.bfloat16, dev)
+    _need(v, "v", torch.bfloat16, dev)
+    _need(do, "do", torch.bfloat16, dev)
+    _need(o, "o", o.dtype, dev)
+    _need(lse, "lse", torch.float32, dev)
+    B, H, N, d = q.shape
+    Nk, dv = v.shape[2], v.shape[3]
+    if (tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape[:2]) != (B, H) or tuple(o.shape) != (B, H, N, dv)
+            or tuple(do.shape) != (B, H, N, dv) or tuple(lse.shape) != (B, H, N)):
+        raise ValueError("shape mismatch between q, k, v, o, lse, do")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if grads is None:
+        grads = (torch.empty((B, H, N, d), dtype=out_dtype, device=dev),
+                 torch.empty((B, H, Nk, d), dtype=out_dtype, device=dev),
+                 torch.empty((B, H, Nk, dv), dtype=out_dtype, device=dev))
+    dq, dk, dv_ = grads
+    for t, name in ((dq, "dq"), (dk, "dk"), (dv_, "dv")):
+        _need(t, name, dq.dtype, dev)
+    if tuple(dq.shape) != (B, H, N, d) or tuple(dk.shape) != (B, H, Nk, d) or tuple(dv_.shape) != (B, H, Nk, dv):
+        raise ValueError("gradient buffers have the wrong shape")
+    if workspace is None:
+        workspace = torch.empty(bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    with torch.cuda.device(dev):
+        st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv_),
+                        _ptr(workspace), workspace.numel(), B, H, N, Nk, d, dv, int(bool(causal)), scale,
+                        _odt(o.dtype), _odt(dq.dtype), _stream(dev))
+    _check(st, "fa_bwd")
+    return dq, dk, dv_
 
 
 def decode_default_splits(B, H, Nk_max, num_sms):

@@ -23,6 +23,19 @@ cudaError_t launch_fwd(const FwdParams& p, int d, bool causal, fa_dtype o_dtype,
     default: return cudaErrorInvalidValue;
     }
 }
+cudaError_t launch_bwd_32(const BwdParams& p, bool causal, fa_dtype grad_dtype, cudaStream_t st);
+cudaError_t launch_bwd_64(const BwdParams& p, bool causal, fa_dtype grad_dtype, cudaStream_t st);
+cudaError_t launch_bwd_128(const BwdParams& p, bool causal, fa_dtype grad_dtype, cudaStream_t st);
+
+cudaError_t launch_bwd(const BwdParams& p, int d, bool causal, fa_dtype grad_dtype, cudaStream_t st)
+{
+    switch (d) {
+    case 32: return launch_bwd_32(p, causal, grad_dtype, st);
+    case 64: return launch_bwd_64(p, causal, grad_dtype, st);
+    case 128: return launch_bwd_128(p, causal, grad_dtype, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
 }  // namespace fa
 
 namespace {
@@ -171,6 +184,89 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     p.wait_limit_ns = g_wait_ns.load();
     cudaError_t e = fa::launch_fwd(p, d, causal != 0, o_dtype, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d)
+{
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return 0;
+    const size_t rows = static_cast<size_t>(B) * H * ((static_cast<size_t>(N) + fa::kBlockM - 1) / fa::kBlockM) *
+                        fa::kBlockM;
+    return round_up(rows * d * sizeof(float), kAlign) + 2 * round_up(rows * sizeof(float), kAlign);
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* grad_o,
+                 void* grad_q, void* grad_k, void* grad_v, void* workspace, size_t ws_bytes, int B, int H, int N,
+                 int Nk, int d, int dv, int causal, float scale, fa_dtype o_dtype, fa_dtype grad_dtype, void* stream)
+{
+    if (q == nullptr || k == nullptr || v == nullptr || o == nullptr || lse == nullptr || grad_o == nullptr ||
+        grad_q == nullptr || grad_k == nullptr || grad_v == nullptr || workspace == nullptr)
+        return FA_ERR_INVALID_ARG;
+    if (B <= 0 || H <= 0 || N <= 0 || Nk <= 0 || d <= 0 || dv <= 0) return FA_ERR_INVALID_ARG;
+    if ((causal != 0 && causal != 1) || !dtype_ok(o_dtype) || !dtype_ok(grad_dtype) || !scale_ok(scale))
+        return FA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4) ||
+        !aligned(grad_o, 16) || !aligned(grad_q, 16) || !aligned(grad_k, 16) || !aligned(grad_v, 16) ||
+        !aligned(workspace, kAlign))
+        return FA_ERR_INVALID_ARG;
+    const long long BH = static_cast<long long>(B) * H;
+    const long long Tr = (static_cast<long long>(N) + fa::kBlockM - 1) / fa::kBlockM;
+    const long long Tc = (static_cast<long long>(Nk) + fa::kBlockN - 1) / fa::kBlockN;
+    if (BH * Tc > 0x7fffffffLL || BH > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    if (!head_ok(d) || dv != d) return FA_ERR_UNSUPPORTED;
+    if (ws_bytes < fa_bwd_workspace_size(B, H, N, d)) return FA_ERR_WORKSPACE;
+
+    int* status = nullptr;
+    if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
+    const size_t rows = static_cast<size_t>(BH) * Tr * fa::kBlockM;
+    char* ws = static_cast<char*>(workspace);
+    float* dq_acc = reinterpret_cast<float*>(ws);
+    float* lse2 = reinterpret_cast<float*>(ws + round_up(rows * d * sizeof(float), kAlign));
+    float* dsc = reinterpret_cast<float*>(reinterpret_cast<char*>(lse2) + round_up(rows * sizeof(float), kAlign));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+    fa::BwdPrepParams pp;
+    pp.o = o;
+    pp.d_o = grad_o;
+    pp.lse = lse;
+    pp.lse2 = lse2;
+    pp.dsc = dsc;
+    pp.dq_acc = dq_acc;
+    pp.BH = static_cast<int>(BH);
+    pp.N = N;
+    pp.Tr = static_cast<int>(Tr);
+    pp.d = d;
+    pp.scale = scale;
+    if (fa::launch_bwd_prep(pp, o_dtype, st) != cudaSuccess) return FA_ERR_CUDA;
+
+    fa::BwdParams p;
+    if (!make_map(&p.tm_q, q, static_cast<int>(BH), N, d) || !make_map(&p.tm_k, k, static_cast<int>(BH), Nk, d) ||
+        !make_map(&p.tm_v, v, static_cast<int>(BH), Nk, dv) ||
+        !make_map(&p.tm_do, grad_o, static_cast<int>(BH), N, dv))
+        return FA_ERR_CUDA;
+    p.lse2 = lse2;
+    p.dsc = dsc;
+    p.dq_acc = dq_acc;
+    p.dk = grad_k;
+    p.dv = grad_v;
+    p.status = status;
+    p.BH = static_cast<int>(BH);
+    p.N = N;
+    p.Nk = Nk;
+    p.Tr = static_cast<int>(Tr);
+    p.Tc = static_cast<int>(Tc);
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale = scale;
+    p.wait_limit_ns = g_wait_ns.load();
+    if (fa::launch_bwd(p, d, causal != 0, grad_dtype, st) != cudaSuccess) return FA_ERR_CUDA;
+
+    fa::BwdDqParams dp;
+    dp.dq_acc = dq_acc;
+    dp.dq = grad_q;
+    dp.BH = static_cast<int>(BH);
+    dp.N = N;
+    dp.Tr = static_cast<int>(Tr);
+    dp.d = d;
+    return fa::launch_bwd_dq(dp, grad_dtype, st) == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
 
 int fa_decode_default_splits(int B, int H, int Nk_max, int num_sms)

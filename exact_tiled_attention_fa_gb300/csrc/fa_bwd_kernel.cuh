@@ -1,0 +1,486 @@
+// fa_bwd_kernel.cuh -- exact attention backward for sm_103a.
+//
+// Algorithm: "flash_lab.py -- FlashAttention, flash-decoding and megakernel in
+// numpy", section 3 `flash_bwd` (the FlashAttention-2 form of the backward): P is
+// not stored by the forward but recomputed on chip from Q, K and the forward's
+// log-sum-exp L, P = exp(S - L).  With D_i = sum dO_i o O_i (one number per row,
+// computed by the preparation kernel), for a key tile j and every query tile i
+// that sees one of its keys:
+//   S = Q_i K_j^T scale (causal mask),  P = exp(S - L_i)
+//   dV_j += P^T dO_i,  dP = dO_i V_j^T,  dS = P o (dP - D_i)
+//   dQ_i += dS K_j scale,  dK_j += dS^T Q_i scale
+// The skipped tiles are those whose last query position lies before the key tile's
+// first key (query i sits at position Nk - N + i).
+//
+// GB300 mapping.  One CTA per (head, 128-key tile j).  It computes the transposed
+// products S^T = K_j Q_i^T and dP^T = V_j dO_i^T, so that a TMEM lane is a key:
+// the rows of P^T and dS^T that a thread produces are exactly the A operand rows
+// the tensor core needs for dV_j += P^T dO_i and dK_j += dS^T Q_i, both issued with
+// A read from tensor memory.  dV_j and dK_j stay in tensor memory for the whole
+// walk.  dQ_i = dS K_j needs dS with the queries as rows: the threads write their
+// dS^T rows to shared memory, which is dS in the MN-major (M-contiguous) operand
+// layout, and the tensor core reads it from there.  dQ_i (fp32, TMEM) is added
+// into a zeroed fp32 accumulator in global memory with vector atomics; a final
+// kernel converts it.  The scale is folded into dS (both dQ and dK carry it).
+//
+// Sixteen warps (four warpgroups):
+//   warps 0-3 / 4-7  compute: thread t of the warpgroup owns key row t (TMEM lane t)
+//                    and half of the query columns (warpgroup 0: queries 0-63,
+//                    warpgroup 1: queries 64-127 of the tile).  Per query tile it
+//                    reads S^T, writes P^T (bf16) over the S^T columns it has read,
+//                    then reads dP^T and writes dS^T (bf16) over its dP^T columns and
+//                    into shared memory.  At the end it writes dK_j and dV_j.
+//   warp 8           TMA producer: K_j and V_j once; Q_i, dO_i, L_i and D_i into a
+//                    ring of two stages.
+//   warp 9           tcgen05 issuer, software-pipelined per query tile t:
+//                    dV(t), S(t+1), dK(t), dQ(t), dP(t+1), so the tensor core works
+//                    on tile t's products while the compute warps exponentiate t+1.
+//   warps 12-15      dQ reduction: thread t owns query row t of the dQ tile.
+// Tensor memory (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+d),
+// dK [256+d,256+2d), dQ [384,384+d) for d <= 64.  For d = 128 there is no room for a
+// separate dQ, so dQ(t) overwrites the dP^T columns (already read), and dP(t+1)
+// waits until the dQ reduction warps have read dQ(t) out.
+//
+// Ordering: every commit tracks all earlier tensor-core operations of the issuing
+// thread, so the arrival of S(t+1) also means dV(t) has read P^T(t), and the arrival
+// of dP(t+1) means dK(t) and dQ(t) have read dS(t) from tensor and shared memory:
+// the compute warps may then overwrite both without further barriers.
+//
+// Every barrier wait is bounded (BwdParams::wait_limit_ns); a role whose wait runs
+// out records FA_ERR_TIMEOUT and raises the CTA's abort flag, each role drains what
+// it has in flight, and the CTA frees its tensor memory and exits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "fa_kernel_common.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int kBwdThreads = 512;
+constexpr int kBwdWarpProducer = 8;
+constexpr int kBwdWarpMma = 9;
+constexpr int kBwdWarpDq = 12;  // warps 12-15
+// Register split after launch (setmaxnreg): the two compute warpgroups grow, the
+// control and dQ warpgroups shrink.  The launcher checks kBwdThreads * (registers at
+// launch) >= 256 * kBwdComputeRegs + 128 * (kBwdControlRegs + kBwdDqRegs).
+constexpr int kBwdComputeRegs = 192;
+constexpr int kBwdControlRegs = 56;
+constexpr int kBwdDqRegs = 64;
+
+enum : int {
+    kBbKV = 0,        // K_j and V_j landed
+    kBbQFull = 1,     // +stage (2): Q_i, dO_i, L_i, D_i landed
+    kBbQEmpty = 3,    // +stage (2): the tensor core is done with the stage
+    kBbSFull = 5,     // S^T(t) in TMEM
+    kBbDPFull = 6,    // dP^T(t) in TMEM
+    kBbPReady = 7,    // P^T(t) written (256 arrivals)
+    kBbDSReady = 8,   // dS^T(t) written to TMEM and shared memory (256 arrivals)
+    kBbDQFull = 9,    // dQ(t) in TMEM
+    kBbDQFree = 10,   // dQ(t) read out of TMEM (128 arrivals)
+    kBbDone = 11,     // every product of the walk has completed
+    kBbDrain = 12,
+    kBbCount = 13
+};
+
+template <int D>
+struct BwdCfg {
+    static_assert(D == 32 || D == 64 || D == 128, "head size");
+    static constexpr int kCB = D < 64 ? D : 64;            // elements per column block
+    static constexpr int kNumCB = D / kCB;
+    static constexpr int kRowBytes = kCB * 2;
+    static constexpr uint32_t kLayout = kRowBytes == 128 ? kSwizzle128B : kSwizzle64B;
+    static constexpr int kAtomBytes = 8 * kRowBytes;
+    static constexpr int kBlkBytes = kBlockM * kRowBytes;
+    static constexpr int kTileBytes = kNumCB * kBlkBytes;  // 128 x D bf16
+    static constexpr int kDSBlk = kBlockM * 128;           // dS: 128 keys x 64 queries (128 B rows)
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kTileBytes;
+    static constexpr int kOffQ = 2 * kTileBytes;           // + stage * kTileBytes
+    static constexpr int kOffDO = 4 * kTileBytes;          // + stage * kTileBytes
+    static constexpr int kOffDS = 6 * kTileBytes;          // two query halves of kDSBlk
+    static constexpr int kOffL = kOffDS + 2 * kDSBlk;      // + stage * 512
+    static constexpr int kOffDsc = kOffL + 2 * 512;        // + stage * 512
+    static constexpr int kOffBar = kOffDsc + 2 * 512;
+    static constexpr int kNumBars = 16;
+    static_assert(kBbCount <= kNumBars, "barrier slots");
+    static constexpr int kUsedBytes = kOffBar + kNumBars * 8 + 16;
+    static constexpr int kMaxSmem = 232448;                // 227 KB per CTA
+    // Up to 1 KB of slack to align the base to the 1024-byte swizzle atom.
+    static constexpr int kSmemBytes = kUsedBytes + 1024 <= kMaxSmem ? kUsedBytes + 1024 : kMaxSmem;
+    static_assert(kUsedBytes <= kMaxSmem, "shared memory");
+    static constexpr int kTmemCols = 512;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    static constexpr uint32_t kColDQ = D == 128 ? 128 : 384;
+    static constexpr bool kDQAlias = D == 128;
+    static constexpr uint32_t kIdescT = idesc_bf16(kBlockN, kBlockM, false);  // S^T, dP^T
+    static constexpr uint32_t kIdescAcc = idesc_bf16(kBlockN, D, true);     // dV, dK
+    static constexpr uint32_t kIdescDQ = idesc_bf16(kBlockM, D, true) | (1u << 15);  // A MN-major
+};
+
+template <int D, bool CAUSAL, typename GradT>
+__global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_constant__ BwdParams p)
+{
+    using C = BwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t bwd_smem_raw[];
+    const uint32_t raw = smem_u32(bwd_smem_raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+    if (pad + C::kUsedBytes > static_cast<uint32_t>(C::kSmemBytes)) {  // cannot align the swizzled tiles
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, FA_ERR_UNSUPPORTED);
+        return;
+    }
+    uint8_t* smem = bwd_smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+    auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + C::kNumBars * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const unsigned long long limit = p.wait_limit_ns;
+
+    // work item: head bh, key tile j; query tiles [i_first, Tr)
+    const int bh = blockIdx.x / p.Tc;
+    const int j = blockIdx.x - bh * p.Tc;
+    const int off = p.Nk - p.N;
+    const int j0 = j * kBlockN;
+    int i_first = 0;
+    if (CAUSAL) {
+        const int a = j0 - off - (kBlockM - 1);  // first tile whose last row position reaches j0
+        i_first = a <= 0 ? 0 : (a + kBlockM - 1) / kBlockM;
+    }
+    const int n = p.Tr > i_first ? p.Tr - i_first : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(kBbKV), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(kBbQFull + s), 1);
+            mbar_init(bar(kBbQEmpty + s), 1);
+        }
+        mbar_init(bar(kBbSFull), 1);
+        mbar_init(bar(kBbDPFull), 1);
+        mbar_init(bar(kBbPReady), 256);
+        mbar_init(bar(kBbDSReady), 256);
+        mbar_init(bar(kBbDQFull), 1);
+        mbar_init(bar(kBbDQFree), 128);
+        mbar_init(bar(kBbDone), 1);
+        mbar_init(bar(kBbDrain), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kBwdWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp >= 8 && warp < 12) {
+        regs_decrease<kBwdControlRegs>();
+        if (warp == kBwdWarpProducer && lane == 0) {
+            // ============================================================ producer
+            prefetch_tensormap(&p.tm_q);
+            prefetch_tensormap(&p.tm_k);
+            prefetch_tensormap(&p.tm_v);
+            prefetch_tensormap(&p.tm_do);
+            const uint64_t pol_keep = policy_evict_last();  // Q_i, dO_i: read by every key tile of the head
+            const uint64_t pol_once = policy_evict_first(); // K_j, V_j: read by this CTA only
+            mbar_arrive_expect_tx(bar(kBbKV), 2 * C::kTileBytes);
+#pragma unroll
+            for (int cb = 0; cb < C::kNumCB; ++cb) {
+                tma_load_3d(sbase + C::kOffK + cb * C::kBlkBytes, &p.tm_k, bar(kBbKV), cb * C::kCB, j0, bh, pol_once);
+                tma_load_3d(sbase + C::kOffV + cb * C::kBlkBytes, &p.tm_v, bar(kBbKV), cb * C::kCB, j0, bh, pol_once);
+            }
+            int issued = 0;
+            bool ok = true;
+            for (int t = 0; t < n; ++t) {
+                const int s = t & 1;
+                if (t >= 2 && !mbar_wait(bar(kBbQEmpty + s), ((t >> 1) - 1) & 1, limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int i0 = (i_first + t) * kBlockM;
+                mbar_arrive_expect_tx(bar(kBbQFull + s), 2 * C::kTileBytes + 2 * 512);
+#pragma unroll
+                for (int cb = 0; cb < C::kNumCB; ++cb) {
+                    tma_load_3d(sbase + C::kOffQ + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_q, bar(kBbQFull + s),
+                                cb * C::kCB, i0, bh, pol_keep);
+                    tma_load_3d(sbase + C::kOffDO + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_do,
+                                bar(kBbQFull + s), cb * C::kCB, i0, bh, pol_keep);
+                }
+                const size_t row = static_cast<size_t>(bh) * p.Tr * kBlockM + i0;
+                bulk_load(sbase + C::kOffL + s * 512, p.lse2 + row, 512, bar(kBbQFull + s));
+                bulk_load(sbase + C::kOffDsc + s * 512, p.dsc + row, 512, bar(kBbQFull + s));
+                ++issued;
+            }
+            if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+            // every issued copy lands before the CTA may exit
+            mbar_wait(bar(kBbKV), 0, kDrainLimitNs, nullptr);
+            for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t)
+                mbar_wait(bar(kBbQFull + (t & 1)), (t >> 1) & 1, kDrainLimitNs, nullptr);
+        } else if (warp == kBwdWarpMma && lane == 0) {
+            // ============================================================ MMA issuer
+            bool ok = true;
+            auto wait = [&](int b, int parity) -> bool {
+                ok = ok && mbar_wait(bar(b), static_cast<uint32_t>(parity) & 1, limit, abort_flag);
+                return ok;
+            };
+            // S^T(t) = K_j Q_i^T or dP^T(t) = V_j dO_i^T: both operands K-major in shared memory.
+            auto issue_t = [&](uint32_t d_col, int a_off, int b_off) {
+                const uint64_t a0 = smem_desc(sbase + a_off, 16, C::kAtomBytes, C::kLayout);
+                const uint64_t b0 = smem_desc(sbase + b_off, 16, C::kAtomBytes, C::kLayout);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t o = ((kk * 16) / C::kCB * C::kBlkBytes + ((kk * 16) % C::kCB) * 2) >> 4;
+                    umma_ss(tmem + d_col, a0 + o, b0 + o, C::kIdescT, kk > 0 ? 1u : 0u);
+                }
+            };
+            // dV += P^T dO_i or dK += dS^T Q_i: A (bf16, packed two per column) from TMEM with the
+            // query halves at columns a_col and a_col + 64; B MN-major in shared memory.
+            auto issue_acc = [&](uint32_t d_col, uint32_t a_col, int b_off, bool accumulate) {
+                const uint64_t b0 = smem_desc(sbase + b_off, C::kBlkBytes, C::kAtomBytes, C::kLayout);
+#pragma unroll
+                for (int kk = 0; kk < kBlockM / 16; ++kk)
+                    umma_ts(tmem + d_col, tmem + a_col + 64u * (kk >> 2) + 8u * (kk & 3),
+                            b0 + ((kk * 16 * C::kRowBytes) >> 4), C::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
+            };
+            // dQ(t) = dS K_j: A = dS (MN-major, two 64-query blocks), B = K_j (MN-major).
+            auto issue_dq = [&]() {
+                const uint64_t a0 = smem_desc(sbase + C::kOffDS, C::kDSBlk, 1024, kSwizzle128B);
+                const uint64_t b0 = smem_desc(sbase + C::kOffK, C::kBlkBytes, C::kAtomBytes, C::kLayout);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk)
+                    umma_ss(tmem + C::kColDQ, a0 + ((kk * 16 * 128) >> 4), b0 + ((kk * 16 * C::kRowBytes) >> 4),
+                            C::kIdescDQ, kk > 0 ? 1u : 0u);
+            };
+            if (n > 0 && wait(kBbKV, 0) && wait(kBbQFull, 0)) {
+                tc_fence_after_sync();
+                issue_t(C::kColS, C::kOffK, C::kOffQ);
+                umma_commit(bar(kBbSFull));
+                issue_t(C::kColDP, C::kOffV, C::kOffDO);
+                umma_commit(bar(kBbDPFull));
+            }
+            for (int t = 0; ok && t < n; ++t) {
+                const int s = t & 1;
+                if (!wait(kBbPReady, t)) break;
+                tc_fence_after_sync();
+                issue_acc(C::kColDV, C::kColS, C::kOffDO + s * C::kTileBytes, t > 0);
+                if (t + 1 < n) {
+                    if (!wait(kBbQFull + (s ^ 1), (t + 1) >> 1)) break;
+                    tc_fence_after_sync();
+                    issue_t(C::kColS, C::kOffK, C::kOffQ + (s ^ 1) * C::kTileBytes);
+                    umma_commit(bar(kBbSFull));
+                }
+                if (!wait(kBbDSReady, t)) break;
+                tc_fence_after_sync();
+                issue_acc(C::kColDK, C::kColDP, C::kOffQ + s * C::kTileBytes, t > 0);
+                umma_commit(bar(kBbQEmpty + s));
+                if (!C::kDQAlias && t > 0 && !wait(kBbDQFree, t - 1)) break;
+                tc_fence_after_sync();
+                issue_dq();
+                umma_commit(bar(kBbDQFull));
+                if (t + 1 < n) {
+                    if (C::kDQAlias && !wait(kBbDQFree, t)) break;
+                    tc_fence_after_sync();
+                    issue_t(C::kColDP, C::kOffV, C::kOffDO + (s ^ 1) * C::kTileBytes);
+                    umma_commit(bar(kBbDPFull));
+                }
+            }
+            umma_commit(bar(kBbDone));
+            if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+            umma_commit(bar(kBbDrain));
+            mbar_wait(bar(kBbDrain), 0, kDrainLimitNs, nullptr);
+        }
+    } else if (warp >= kBwdWarpDq) {
+        regs_decrease<kBwdDqRegs>();
+        // ============================================================ dQ reduction
+        const int r = threadIdx.x & 127;  // query row of the tile == TMEM lane
+        const uint32_t t_dq = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kColDQ;
+        bool ok = true;
+        for (int t = 0; t < n; ++t) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDQFull), t & 1, limit, abort_flag));
+            if (!ok) break;
+            tc_fence_after_sync();
+            float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.Tr + (i_first + t)) * (D / 4) * (kBlockM * 4) + r * 4;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(t_dq + 32u * c, v);
+                tmem_ld_wait();
+                if (c == D / 32 - 1) {  // the whole dQ(t) row is in registers: release the columns
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(kBbDQFree));
+                }
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    red_add_v4(acc + static_cast<size_t>(c * 8 + e / 4) * (kBlockM * 4), __uint_as_float(v[e]),
+                               __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+            }
+        }
+        if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+    } else {
+        regs_increase<kBwdComputeRegs>();
+        // ============================================================ compute
+        const int h = warp >> 2;                 // query half of the tile
+        const int k = threadIdx.x & 127;         // key row of the tile == TMEM lane
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t t_s = tmem + lane_base + C::kColS + 64u * h;
+        const uint32_t t_dp = tmem + lane_base + C::kColDP + 64u * h;
+        const uint32_t ds_row = sbase + C::kOffDS + h * C::kDSBlk + k * 128;  // this thread's dS^T row
+        const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
+        const float2 sc2 = make_float2(p.scale, p.scale);
+        bool ok = true;
+        for (int t = 0; t < n; ++t) {
+            const int s = t & 1;
+            const int i0 = (i_first + t) * kBlockM;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbSFull), t & 1, limit, abort_flag));
+            if (!ok) break;
+            tc_fence_after_sync();
+            uint32_t u[64];
+            tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+            tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+            tmem_ld_wait();
+            // P = exp2(S scale log2(e) - L log2(e)); L = +inf gives 0 (row past N or with no key)
+            const uint32_t l_addr = sbase + C::kOffL + s * 512 + h * 256;
+            float pf[64];
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+                const float4 l4 = ld_shared_f4(l_addr + c * 4);
+                const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2,
+                                              make_float2(-l4.x, -l4.y));
+                const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sl2,
+                                              make_float2(-l4.z, -l4.w));
+                pf[c] = ex2(x01.x);
+                pf[c + 1] = ex2(x01.y);
+                pf[c + 2] = ex2(x23.x);
+                pf[c + 3] = ex2(x23.y);
+            }
+            if (CAUSAL && off + i0 < j0 + kBlockN - 1) {
+                // key j0 + k is hidden from query i0 + q when j0 + k > off + i0 + q
+                const int thr = j0 + k - off - i0 - 64 * h;  // my columns c < thr are masked
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (c < thr) pf[c] = 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) pk[c / 2] = pack_bf16x2(pf[c], pf[c + 1]);
+            tmem_st32(t_s, pk);
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(bar(kBbPReady));
+
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDPFull), t & 1, limit, abort_flag));
+            if (!ok) break;
+            tc_fence_after_sync();
+            tmem_ld32(t_dp, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+            tmem_ld32(t_dp + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+            tmem_ld_wait();
+            // dS' = scale dS = P o (dP scale - scale D)
+            const uint32_t d_addr = sbase + C::kOffDsc + s * 512 + h * 256;
+#pragma unroll
+            for (int c = 0; c < 64; c += 4) {
+                const float4 d4 = ld_shared_f4(d_addr + c * 4);
+                const float2 y01 = __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sc2,
+                                              make_float2(-d4.x, -d4.y));
+                const float2 y23 = __ffma2_rn(make_float2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sc2,
+                                              make_float2(-d4.z, -d4.w));
+                const float2 g01 = __fmul2_rn(y01, make_float2(pf[c], pf[c + 1]));
+                const float2 g23 = __fmul2_rn(y23, make_float2(pf[c + 2], pf[c + 3]));
+                pk[c / 2] = pack_bf16x2(g01.x, g01.y);
+                pk[c / 2 + 1] = pack_bf16x2(g23.x, g23.y);
+            }
+            tmem_st32(t_dp, pk);
+            // dS^T row k into the MN-major dS operand: 16-byte chunk q8 of the 128-byte row goes
+            // to chunk q8 ^ (k mod 8) (128-byte swizzle).
+#pragma unroll
+            for (int q8 = 0; q8 < 8; ++q8)
+                st_shared_v4(ds_row + ((q8 ^ (k & 7)) << 4), pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
+            fence_proxy_async_shared();
+            tmem_st_wait();
+            tc_fence_before_sync();
+            mbar_arrive(bar(kBbDSReady));
+        }
+        // dK_j and dV_j: this thread writes key row j0 + k, columns of its half
+        if (ok) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDone), 0, limit, abort_flag));
+            if (ok) {
+                tc_fence_after_sync();
+                const int key = j0 + k;
+                const bool valid = key < p.Nk;
+                const size_t row = (static_cast<size_t>(bh) * p.Nk + (valid ? key : 0)) * D + h * (D / 2);
+                GradT* dk = reinterpret_cast<GradT*>(p.dk) + row;
+                GradT* dv = reinterpret_cast<GradT*>(p.dv) + row;
+#pragma unroll
+                for (int c = 0; c < D / 2; c += 16) {
+                    uint32_t a[16], b[16];
+                    tmem_ld16(tmem + lane_base + C::kColDV + h * (D / 2) + c, a);
+                    tmem_ld16(tmem + lane_base + C::kColDK + h * (D / 2) + c, b);
+                    tmem_ld_wait();
+                    float fa[16], fb[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        fa[e] = n > 0 ? __uint_as_float(a[e]) : 0.f;
+                        fb[e] = n > 0 ? __uint_as_float(b[e]) : 0.f;
+                    }
+                    if (valid) {
+                        store_row16<GradT>(dv + c, fa);
+                        store_row16<GradT>(dk + c, fb);
+                    }
+                }
+            }
+        }
+        if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kBwdWarpMma) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int D, bool CAUSAL, typename GradT>
+cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st)
+{
+    using C = BwdCfg<D>;
+    auto kern = fa_bwd_kernel<D, CAUSAL, GradT>;
+    static bool configured[64] = {};
+    static int regs[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        cudaFuncAttributes attr;
+        e = cudaFuncGetAttributes(&attr, kern);
+        if (e != cudaSuccess) return e;
+        regs[dev] = attr.numRegs;
+        configured[dev] = true;
+    }
+    if (regs[dev] * kBwdThreads < 256 * kBwdComputeRegs + 128 * (kBwdControlRegs + kBwdDqRegs))
+        return cudaErrorLaunchOutOfResources;  // the register split would not fit
+    const long long grid = static_cast<long long>(p.BH) * p.Tc;
+    if (grid <= 0) return cudaSuccess;
+    kern<<<static_cast<unsigned>(grid), kBwdThreads, C::kSmemBytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BwdParams& p, bool causal, fa_dtype grad_dtype, cudaStream_t st)
+{
+    if (grad_dtype == FA_F32)
+        return causal ? launch_bwd_t<D, true, float>(p, st) : launch_bwd_t<D, false, float>(p, st);
+    return causal ? launch_bwd_t<D, true, __nv_bfloat16>(p, st) : launch_bwd_t<D, false, __nv_bfloat16>(p, st);
+}
+
+}  // namespace fa

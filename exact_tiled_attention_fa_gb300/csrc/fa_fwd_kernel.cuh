@@ -52,11 +52,11 @@
 #include <cstdint>
 
 #include "fa_internal.h"
+#include "fa_kernel_common.cuh"
 #include "ptx.cuh"
 
 namespace fa {
 
-constexpr unsigned long long kDrainLimitNs = 1000000000ull;  // 1 s for draining after a failure
 constexpr int kFwdThreads = 384;  // 12 warps = 3 warpgroups
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;       // warps 9 and 10 issue the MMAs of Q0 and Q1; warp 11 idles
@@ -119,37 +119,6 @@ struct FwdCfg {
     static constexpr uint32_t kIdescO = idesc_bf16(kBlockM, D, true);
 };
 
-
-__device__ __forceinline__ void record_failure(int* status, volatile int* abort_flag, int code)
-{
-    *abort_flag = 1;
-    atomicCAS(status, 0, code);
-}
-
-template <typename OutT>
-__device__ __forceinline__ void store_row32(OutT* dst, const float (&v)[32]);
-
-template <>
-__device__ __forceinline__ void store_row32<float>(float* dst, const float (&v)[32])
-{
-#pragma unroll
-    for (int i = 0; i < 32; i += 4)
-        *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
-}
-
-template <>
-__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, const float (&v)[32])
-{
-#pragma unroll
-    for (int i = 0; i < 32; i += 8) {
-        uint4 u;
-        u.x = pack_bf16x2(v[i + 0], v[i + 1]);
-        u.y = pack_bf16x2(v[i + 2], v[i + 3]);
-        u.z = pack_bf16x2(v[i + 4], v[i + 5]);
-        u.w = pack_bf16x2(v[i + 6], v[i + 7]);
-        *reinterpret_cast<uint4*>(dst + i) = u;
-    }
-}
 
 __device__ __forceinline__ float max3(float a, float b, float c)
 {

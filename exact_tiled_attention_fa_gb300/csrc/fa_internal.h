@@ -33,6 +33,47 @@ struct FwdParams {
 // Launch the forward kernel for head size d (= dv), causal flag and output type.
 cudaError_t launch_fwd(const FwdParams& p, int d, bool causal, fa_dtype o_dtype, cudaStream_t st);
 
+// Backward.  Work item: one head and one 128-key tile; the CTA walks every query tile
+// that sees a key of it.  Per-row vectors and the dQ accumulator are padded to whole
+// query tiles (Tr * 128 rows per head).
+struct BwdParams {
+    CUtensorMap tm_q;   // bf16 [B*H][N][d], box {min(d,64), 128, 1}
+    CUtensorMap tm_k;   // bf16 [B*H][Nk][d]
+    CUtensorMap tm_v;   // bf16 [B*H][Nk][d]
+    CUtensorMap tm_do;  // bf16 [B*H][N][d]
+    const float* lse2;  // [B*H][Tr*128]: LSE * log2(e); +inf past N and where no key is visible
+    const float* dsc;   // [B*H][Tr*128]: scale * sum_c dO[c] O[c]; 0 past N
+    float* dq_acc;      // [B*H][Tr][d/4][128][4] fp32, zeroed before the kernel
+    void* dk;           // [B*H][Nk][d], gradient dtype
+    void* dv;           // [B*H][Nk][d]
+    int* status;
+    int BH, N, Nk, Tr, Tc;
+    float scale_log2;   // scale * log2(e)
+    float scale;
+    unsigned long long wait_limit_ns;
+};
+
+struct BwdPrepParams {
+    const void* o;      // [B*H][N][d], bf16 or fp32 (forward output)
+    const void* d_o;    // bf16 [B*H][N][d]
+    const float* lse;   // [B*H][N] (forward output, natural log)
+    float* lse2;
+    float* dsc;
+    float* dq_acc;
+    int BH, N, Tr, d;
+    float scale;
+};
+
+struct BwdDqParams {
+    const float* dq_acc;
+    void* dq;           // [B*H][N][d], gradient dtype
+    int BH, N, Tr, d;
+};
+
+cudaError_t launch_bwd(const BwdParams& p, int d, bool causal, fa_dtype grad_dtype, cudaStream_t st);
+cudaError_t launch_bwd_prep(const BwdPrepParams& p, fa_dtype o_dtype, cudaStream_t st);
+cudaError_t launch_bwd_dq(const BwdDqParams& p, fa_dtype grad_dtype, cudaStream_t st);
+
 // Decode: keys per block of the split kernel's inner loop; a split is a whole
 // number of such blocks.
 constexpr int kDecodeKeyBlock = 64;

@@ -1,0 +1,70 @@
+// fa_kernel_common.cuh -- small device helpers shared by the forward and backward
+// kernels: failure recording and row stores in the output element type.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr unsigned long long kDrainLimitNs = 1000000000ull;  // 1 s for draining after a failure
+
+__device__ __forceinline__ void record_failure(int* status, volatile int* abort_flag, int code)
+{
+    *abort_flag = 1;
+    atomicCAS(status, 0, code);
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_row32(OutT* dst, const float (&v)[32]);
+
+template <>
+__device__ __forceinline__ void store_row32<float>(float* dst, const float (&v)[32])
+{
+#pragma unroll
+    for (int i = 0; i < 32; i += 4)
+        *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+
+template <>
+__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, const float (&v)[32])
+{
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) {
+        uint4 u;
+        u.x = pack_bf16x2(v[i + 0], v[i + 1]);
+        u.y = pack_bf16x2(v[i + 2], v[i + 3]);
+        u.z = pack_bf16x2(v[i + 4], v[i + 5]);
+        u.w = pack_bf16x2(v[i + 6], v[i + 7]);
+        *reinterpret_cast<uint4*>(dst + i) = u;
+    }
+}
+
+template <typename OutT>
+__device__ __forceinline__ void store_row16(OutT* dst, const float (&v)[16]);
+
+template <>
+__device__ __forceinline__ void store_row16<float>(float* dst, const float (&v)[16])
+{
+#pragma unroll
+    for (int i = 0; i < 16; i += 4)
+        *reinterpret_cast<float4*>(dst + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+}
+
+template <>
+__device__ __forceinline__ void store_row16<__nv_bfloat16>(__nv_bfloat16* dst, const float (&v)[16])
+{
+#pragma unroll
+    for (int i = 0; i < 16; i += 8) {
+        uint4 u;
+        u.x = pack_bf16x2(v[i + 0], v[i + 1]);
+        u.y = pack_bf16x2(v[i + 2], v[i + 3]);
+        u.z = pack_bf16x2(v[i + 4], v[i + 5]);
+        u.w = pack_bf16x2(v[i + 6], v[i + 7]);
+        *reinterpret_cast<uint4*>(dst + i) = u;
+    }
+}
+
+}  // namespace fa

@@ -38,6 +38,12 @@ def attention_inputs(B, H, N, Nk, d, dv, seed=0, mult=1.0, device="cpu"):
     return tuple(out)
 
 
+def grad_output(B, H, N, dv, seed=0, device="cpu"):
+    """Upstream gradient dO [B,H,N,dv] for the backward: bf16, iid N(0,1), its own generator stream."""
+    g = _gen(device, int(seed) + 7919)
+    return torch.randn((B, H, N, dv), generator=g, device=device, dtype=torch.float32).to(BF16).contiguous()
+
+
 def decode_lengths(B, lo, hi, seed=0):
     """Per-sequence cached lengths drawn uniformly from the closed interval [lo, hi] (int32, CPU)."""
     g = torch.Generator(device="cpu").manual_seed(int(seed))

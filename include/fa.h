@@ -10,6 +10,10 @@
  *   fa_decode_splitkv   single-query decode split over the key/value length, each
  *                       split's normalised output and log-sum-exp merged afterwards
  *                       ("flash_lab.py", section 4 `split_kv_decode`).
+ *   fa_bwd              gradients dQ, dK, dV of exact attention, P recomputed tile by
+ *                       tile from the forward's log-sum-exp ("flash_lab.py", section 3
+ *                       `flash_bwd`, FlashAttention-2 form; the value it reaches is
+ *                       section 2 `standard_attention_bwd`).
  *   fa_merge_states     the log-sum-exp combine of partial states on its own
  *                       ("flash_lab.py", section 4 `split_kv_decode` combine, the
  *                       lse form of section 1 `merge_states`).
@@ -77,6 +81,41 @@ typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                  int N, int Nk, int d, int dv, int causal, float scale, fa_dtype o_dtype,
                  void* stream);
+
+/*
+ * Bytes of workspace fa_bwd needs: with Tr = ceil(N / 128), an fp32 dQ accumulator of
+ * B*H*Tr*128*d values, then fp32 base-2 log-sum-exps and fp32 scaled row terms of
+ * B*H*Tr*128 values each, every region 256-byte aligned.  Returns 0 on invalid arguments.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Exact attention backward ("flash_lab.py" section 3 `flash_bwd`).  For the upstream
+ * gradient dO of the forward's output O, with P the attention weights of fa_fwd (same
+ * mask and scale) and D_i = sum_c dO[i,c] O[i,c]:
+ *   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  dQ = dS K scale,  dK = dS^T Q scale
+ * for every (b, h).  P is recomputed tile by tile as exp(scale q.k - lse); it never reaches
+ * memory.  Rows with no visible key (lse = -inf) contribute nothing.
+ *
+ *   q, k, v      bf16 [B, H, N, d], [B, H, Nk, d], [B, H, Nk, dv]  (device; the forward inputs)
+ *   o            o_dtype [B, H, N, dv]   (device; the forward output, used only for D)
+ *   lse          fp32 [B, H, N]          (device; the forward's log-sum-exp)
+ *   grad_o       bf16 [B, H, N, dv]      (device; dO)
+ *   grad_q, grad_k, grad_v   grad_dtype [B, H, N, d], [B, H, Nk, d], [B, H, Nk, dv]
+ *                (device, written; every element is written)
+ *   workspace    device scratch of ws_bytes >= fa_bwd_workspace_size(B, H, N, d) bytes,
+ *                256-byte aligned; its contents on entry do not matter.
+ *   B, H, N, Nk >= 1; d = dv in {32, 64, 128}; causal 0 or 1; scale > 0 and finite, the
+ *   value the forward used.
+ * Three kernels are enqueued on `stream`: a preparation pass (D, lse in base 2, zeroing the
+ * dQ accumulator), the tensor-core pass (one CTA per (b, h, 128-key tile), dK and dV
+ * written directly, dQ added into the accumulator) and the dQ conversion.
+ * Returns FA_ERR_WORKSPACE if ws_bytes is too small (nothing launched).
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                 const void* grad_o, void* grad_q, void* grad_k, void* grad_v, void* workspace,
+                 size_t ws_bytes, int B, int H, int N, int Nk, int d, int dv, int causal,
+                 float scale, fa_dtype o_dtype, fa_dtype grad_dtype, void* stream);
 
 /*
  * Split count fa_decode_splitkv uses when asked for n_splits = 0, for a device with
@@ -180,7 +219,7 @@ fa_status fa_get_device_error(void* stream);
 
 /*
  * Upper bound, in nanoseconds of the GPU global timer, on every wait for a barrier inside
- * the forward kernel (default 2e9).  When a wait runs out the kernel records FA_ERR_TIMEOUT,
+ * the forward and backward tensor-core kernels (default 2e9).  When a wait runs out the kernel records FA_ERR_TIMEOUT,
  * drains its own copies in flight, frees its tensor memory and returns.  0 restores the
  * default.  Applies to launches made after the call.
  */

@@ -113,11 +113,12 @@ def standard_attention(Q, K, V, causal=False, scale=None):
     return O, lse, P
 
 
-def standard_attention_bwd(Q, K, V, dO, causal=False, scale=None):
+def standard_attention_bwd(Q, K, V, dO, causal=False, scale=None, return_terms=False):
     """Backward of standard attention with the full P materialised.
 
     dV = P^T dO; dP = dO V^T; D_i = sum_c dO_ic O_ic; dS = P o (dP - D);
-    dQ = dS K scale; dK = dS^T Q scale.  Returns (dQ, dK, dV).
+    dQ = dS K scale; dK = dS^T Q scale.  Returns (dQ, dK, dV), followed by
+    (P, dS) when ``return_terms``.
     """
     Q, K, V, dO = (np.asarray(t, dtype=np.float64) for t in (Q, K, V, dO))
     d = Q.shape[1]
@@ -127,6 +128,8 @@ def standard_attention_bwd(Q, K, V, dO, causal=False, scale=None):
     dV = P.T @ dO
     dP = dO @ V.T
     dS = P * (dP - D[:, None])
+    if return_terms:
+        return dS @ K * scale, dS.T @ Q * scale, dV, P, dS
     return dS @ K * scale, dS.T @ Q * scale, dV
 
 
