@@ -35,7 +35,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from fa_inputs import attention_inputs, decode_inputs, sample_slices  # noqa: E402
+from fa_inputs import attention_inputs, decode_inputs, grad_output, sample_slices  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (% of BF16 peak); decode KV GB/s (% of HBM peak)"
 UNIT = "TFLOP/s"
@@ -215,6 +215,11 @@ def run_ours(args, world, rank, local):
         if rank == 0:
             print(json.dumps({"decode": decode}), flush=True)
         return 0
+    if args.bwd_only:
+        backward = run_bwd(fa, dev, stream, args, world)
+        if rank == 0:
+            print(json.dumps({"backward": backward}), flush=True)
+        return 0
     B, H, N, Nk, d = FWD["B"], FWD["H"], FWD["N"], FWD["Nk"], FWD["d"]
     q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=rank, device=dev)
     o_nc = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
@@ -297,6 +302,8 @@ def run_ours(args, world, rank, local):
         line["decode"] = decode
     if not args.no_extra:
         line["other_fwd_configs"] = run_other_fwd(fa, dev, stream, args, world)
+    if not args.no_bwd:
+        line["backward"] = run_bwd(fa, dev, stream, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, fl, threads, desc = oracle_sample(args.cpu_slices)
         line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -384,6 +391,45 @@ def run_other_fwd(fa, dev, stream, args, world):
     return out
 
 
+def bwd_flops(B, H, N, Nk, d, causal):
+    """Five products of 2*N*Nk*d each per head (S, dP, dV, dK, dQ), halved for causal."""
+    f = 10.0 * B * H * N * Nk * d
+    return f / 2 if causal else f
+
+
+def run_bwd(fa, dev, stream, args, world):
+    """fa_bwd on the GPT-2-medium shape (dO given, O and LSE from fa_fwd), bf16 gradients."""
+    B, H, N, Nk, d = FWD["B"], FWD["H"], FWD["N"], FWD["Nk"], FWD["d"]
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=0, device=dev)
+    do = grad_output(B, H, N, d, seed=0, device=dev)
+    ws = torch.empty(fa.bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    grads = tuple(torch.empty((B, H, n, d), dtype=torch.bfloat16, device=dev) for n in (N, Nk, Nk))
+    pk, src = peaks()
+    peak = float(pk["bf16_tflops"])
+    out = {"workload": f"backward B={B} H={H} N=Nk={N} d=dv={d}, bf16 dQ/dK/dV, 3 launches per call",
+           "peak_source": f"{src} bf16_tflops"}
+    for causal in (False, True):
+        o, lse = fa.fwd(q, k, v, causal=causal)
+        for _ in range(max(args.warmup, 3)):
+            fa.bwd(q, k, v, o, lse, do, causal=causal, grads=grads, workspace=ws)
+        steps = max(5, args.steps // 10)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e0.record(stream)
+        for _ in range(steps):
+            fa.bwd(q, k, v, o, lse, do, causal=causal, grads=grads, workspace=ws)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+        fl = bwd_flops(B, H, N, Nk, d, causal)
+        tf = world * fl / (ms / 1e3) / 1e12
+        out["causal" if causal else "non-causal"] = {"ms": ms, "tflops": tf, "frac_of_peak": tf / peak / world,
+                                                     "flops": fl}
+    assert fa.get_device_error(dev) == fa.FA_OK
+    return out
+
+
 def run_decode(fa, dev, stream, args, world):
     B, H, Nk_max, d = DEC["B"], DEC["H"], DEC["Nk_max"], DEC["d"]
     q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=0, lo=DEC["lo"], hi=DEC["hi"], device=dev)
@@ -428,6 +474,8 @@ def main():
     ap.add_argument("--decode-only", action="store_true", help="only the split-KV decode (profiling)")
     ap.add_argument("--decode-batch", type=int, default=DEC["B"], help="decode batch (smaller cache for profiling)")
     ap.add_argument("--cpu-slices", type=int, default=1024)
+    ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
+    ap.add_argument("--bwd-only", action="store_true", help="only the backward (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -27,24 +27,32 @@
 //   warps 0-3 / 4-7  compute: thread t of the warpgroup owns key row t (TMEM lane t)
 //                    and half of the query columns (warpgroup 0: queries 0-63,
 //                    warpgroup 1: queries 64-127 of the tile).  Per query tile it
-//                    reads S^T, writes P^T (bf16) over the S^T columns it has read,
-//                    then reads dP^T and writes dS^T (bf16) over its dP^T columns and
-//                    into shared memory.  At the end it writes dK_j and dV_j.
+//                    reads S^T and writes P^T (bf16), then reads dP^T and writes dS^T
+//                    (bf16) to tensor memory and to shared memory.  At the end it writes
+//                    dK_j and dV_j.
 //   warp 8           TMA producer: K_j and V_j once; Q_i, dO_i, L_i and D_i into a
-//                    ring of two stages.
-//   warp 9           tcgen05 issuer, software-pipelined per query tile t:
-//                    dV(t), S(t+1), dK(t), dQ(t), dP(t+1), so the tensor core works
-//                    on tile t's products while the compute warps exponentiate t+1.
+//                    ring of three stages (two for d = 128).
+//   warps 9, 10      tcgen05 issuers.  Every barrier wait or commit stalls the issuing
+//                    thread for a few hundred cycles while the tensor core queues only a
+//                    few of these small MMAs, so the work is split: warp 9 issues
+//                    S^T(t+1) and dP^T(t+1) as soon as the compute warps have loaded S^T(t)
+//                    and dP^T(t) (d <= 64; for d = 128 once dV(t) has read P^T(t) and dQ(t)
+//                    has been read out); warp 10 issues dV(t), dK(t), dQ(t) as P^T(t) and
+//                    dS^T(t) become ready.  The tensor core works on tile t's products
+//                    while the compute warps exponentiate t+1.
 //   warps 12-15      dQ reduction: thread t owns query row t of the dQ tile.
 // Tensor memory (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+d),
-// dK [256+d,256+2d), dQ [384,384+d) for d <= 64.  For d = 128 there is no room for a
-// separate dQ, so dQ(t) overwrites the dP^T columns (already read), and dP(t+1)
-// waits until the dQ reduction warps have read dQ(t) out.
+// dK [256+d,256+2d), dQ [384,384+d) and P^T / dS^T [448,512) for d <= 64: P^T(t) is
+// stored once dK(t-1) has read dS^T(t-1), dS^T(t) once dV(t) has read P^T(t).  For
+// d = 128 there is no room for them: P^T(t) overwrites the S^T columns it came from,
+// dS^T(t) the dP^T columns, dQ(t) overwrites those again once dK(t) has read dS^T,
+// and dP(t+1) waits until the dQ reduction warps have read dQ(t) out.
 //
-// Ordering: every commit tracks all earlier tensor-core operations of the issuing
-// thread, so the arrival of S(t+1) also means dV(t) has read P^T(t), and the arrival
-// of dP(t+1) means dK(t) and dQ(t) have read dS(t) from tensor and shared memory:
-// the compute warps may then overwrite both without further barriers.
+// Ordering: a commit tracks every earlier tensor-core operation of its issuing thread.
+// For d = 128, S^T(t+1) is issued only after dV(t) has completed, so its arrival also
+// tells the compute warps that P^T(t) has been read, and the arrival of dP^T(t+1)
+// that dK(t) and dQ(t) have read dS(t).  For d <= 64 the compute warps wait for those
+// completions themselves.
 //
 // Every barrier wait is bounded (BwdParams::wait_limit_ns); a role whose wait runs
 // out records FA_ERR_TIMEOUT and raises the CTA's abort flag, each role drains what
@@ -62,7 +70,7 @@ namespace fa {
 
 constexpr int kBwdThreads = 512;
 constexpr int kBwdWarpProducer = 8;
-constexpr int kBwdWarpMma = 9;
+constexpr int kBwdWarpMma = 9;   // warp 9 issues S and dP, warp 10 issues dV, dK and dQ
 constexpr int kBwdWarpDq = 12;  // warps 12-15
 // Register split after launch (setmaxnreg): the two compute warpgroups grow, the
 // control and dQ warpgroups shrink.  The launcher checks kBwdThreads * (registers at
@@ -71,19 +79,24 @@ constexpr int kBwdComputeRegs = 192;
 constexpr int kBwdControlRegs = 56;
 constexpr int kBwdDqRegs = 64;
 
+constexpr int kBwdMaxQStages = 3;
 enum : int {
     kBbKV = 0,        // K_j and V_j landed
-    kBbQFull = 1,     // +stage (2): Q_i, dO_i, L_i, D_i landed
-    kBbQEmpty = 3,    // +stage (2): the tensor core is done with the stage
-    kBbSFull = 5,     // S^T(t) in TMEM
-    kBbDPFull = 6,    // dP^T(t) in TMEM
-    kBbPReady = 7,    // P^T(t) written (256 arrivals)
-    kBbDSReady = 8,   // dS^T(t) written to TMEM and shared memory (256 arrivals)
-    kBbDQFull = 9,    // dQ(t) in TMEM
-    kBbDQFree = 10,   // dQ(t) read out of TMEM (128 arrivals)
-    kBbDone = 11,     // every product of the walk has completed
-    kBbDrain = 12,
-    kBbCount = 13
+    kBbQFull = 1,     // +stage: Q_i, dO_i, L_i, D_i landed
+    kBbQEmpty = kBbQFull + kBwdMaxQStages,   // +stage: both issuers' tensor-core work on it is done
+    kBbSFull = kBbQEmpty + kBwdMaxQStages,   // S^T(t) in TMEM
+    kBbDPFull,        // dP^T(t) in TMEM
+    kBbPReady,        // P^T(t) written (256 arrivals)
+    kBbDSReady,       // dS^T(t) written to TMEM and shared memory (256 arrivals)
+    kBbDQFull,        // dQ(t) in TMEM
+    kBbDQFree,        // dQ(t) read out of TMEM (128 arrivals)
+    kBbDone,          // every product of the walk has completed (one commit per issuer)
+    kBbDrain,         // +issuer (2)
+    kBbDPFree = kBbDrain + 2,  // dP^T(t) loaded into registers (256 arrivals)
+    kBbDVDone,        // dV(t) has read P^T(t)
+    kBbSFree,         // S^T(t) loaded into registers (256 arrivals; d <= 64)
+    kBbDKDone,        // dK(t) has read dS^T(t) (d <= 64)
+    kBbCount
 };
 
 template <int D>
@@ -97,15 +110,19 @@ struct BwdCfg {
     static constexpr int kBlkBytes = kBlockM * kRowBytes;
     static constexpr int kTileBytes = kNumCB * kBlkBytes;  // 128 x D bf16
     static constexpr int kDSBlk = kBlockM * 128;           // dS: 128 keys x 64 queries (128 B rows)
+    // Q_i / dO_i ring depth: a stage is reloaded only after dK of its tile has completed, so
+    // two stages leave the S^T(t+2) issue waiting for the load; d = 128 has room for two only.
+    static constexpr int kQStages = D == 128 ? 2 : 3;
+    static_assert(kQStages <= kBwdMaxQStages, "barrier slots");
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kTileBytes;
-    static constexpr int kOffQ = 2 * kTileBytes;           // + stage * kTileBytes
-    static constexpr int kOffDO = 4 * kTileBytes;          // + stage * kTileBytes
-    static constexpr int kOffDS = 6 * kTileBytes;          // two query halves of kDSBlk
-    static constexpr int kOffL = kOffDS + 2 * kDSBlk;      // + stage * 512
-    static constexpr int kOffDsc = kOffL + 2 * 512;        // + stage * 512
-    static constexpr int kOffBar = kOffDsc + 2 * 512;
-    static constexpr int kNumBars = 16;
+    static constexpr int kOffQ = 2 * kTileBytes;                          // + stage * kTileBytes
+    static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;          // + stage * kTileBytes
+    static constexpr int kOffDS = kOffDO + kQStages * kTileBytes;         // two query halves of kDSBlk
+    static constexpr int kOffL = kOffDS + 2 * kDSBlk;                     // + stage * 512
+    static constexpr int kOffDsc = kOffL + kQStages * 512;                // + stage * 512
+    static constexpr int kOffBar = kOffDsc + kQStages * 512;
+    static constexpr int kNumBars = 24;
     static_assert(kBbCount <= kNumBars, "barrier slots");
     static constexpr int kUsedBytes = kOffBar + kNumBars * 8 + 16;
     static constexpr int kMaxSmem = 232448;                // 227 KB per CTA
@@ -116,6 +133,12 @@ struct BwdCfg {
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
     static constexpr uint32_t kColDQ = D == 128 ? 128 : 384;
     static constexpr bool kDQAlias = D == 128;
+    // d <= 64: P^T and dS^T share the last 64 columns (dV(t) reads P^T(t) before dS^T(t) is
+    // written), so S^T(t+1) and dP^T(t+1) may start as soon as S^T(t), dP^T(t) are loaded.
+    static constexpr bool kDSOwn = D <= 64;
+    static constexpr uint32_t kColDS = kDSOwn ? 448 : kColDP;
+    static constexpr uint32_t kColP = kDSOwn ? 448 : kColS;
+    static constexpr uint32_t kPHalf = kDSOwn ? 32 : 64;  // columns between the query halves of P^T, dS^T
     static constexpr uint32_t kIdescT = idesc_bf16(kBlockN, kBlockM, false);  // S^T, dP^T
     static constexpr uint32_t kIdescAcc = idesc_bf16(kBlockN, D, true);     // dV, dK
     static constexpr uint32_t kIdescDQ = idesc_bf16(kBlockM, D, true) | (1u << 15);  // A MN-major
@@ -156,18 +179,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
 
     if (threadIdx.x == 0) {
         mbar_init(bar(kBbKV), 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::kQStages; ++s) {
             mbar_init(bar(kBbQFull + s), 1);
-            mbar_init(bar(kBbQEmpty + s), 1);
+            mbar_init(bar(kBbQEmpty + s), 2);
         }
+        mbar_init(bar(kBbDrain), 1);
+        mbar_init(bar(kBbDrain + 1), 1);
         mbar_init(bar(kBbSFull), 1);
         mbar_init(bar(kBbDPFull), 1);
         mbar_init(bar(kBbPReady), 256);
         mbar_init(bar(kBbDSReady), 256);
         mbar_init(bar(kBbDQFull), 1);
         mbar_init(bar(kBbDQFree), 128);
-        mbar_init(bar(kBbDone), 1);
-        mbar_init(bar(kBbDrain), 1);
+        mbar_init(bar(kBbDPFree), 256);
+        mbar_init(bar(kBbDone), 2);
+        mbar_init(bar(kBbDVDone), 1);
+        mbar_init(bar(kBbSFree), 256);
+        mbar_init(bar(kBbDKDone), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -198,9 +226,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             }
             int issued = 0;
             bool ok = true;
+            constexpr int QS = C::kQStages;
             for (int t = 0; t < n; ++t) {
-                const int s = t & 1;
-                if (t >= 2 && !mbar_wait(bar(kBbQEmpty + s), ((t >> 1) - 1) & 1, limit, abort_flag)) {
+                const int s = t % QS;
+                if (t >= QS && !mbar_wait(bar(kBbQEmpty + s), ((t / QS) - 1) & 1, limit, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -221,10 +250,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
             // every issued copy lands before the CTA may exit
             mbar_wait(bar(kBbKV), 0, kDrainLimitNs, nullptr);
-            for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t)
-                mbar_wait(bar(kBbQFull + (t & 1)), (t >> 1) & 1, kDrainLimitNs, nullptr);
-        } else if (warp == kBwdWarpMma && lane == 0) {
-            // ============================================================ MMA issuer
+            for (int t = issued - QS < 0 ? 0 : issued - QS; t < issued; ++t)
+                mbar_wait(bar(kBbQFull + t % QS), (t / QS) & 1, kDrainLimitNs, nullptr);
+        } else if ((warp == kBwdWarpMma || warp == kBwdWarpMma + 1) && lane == 0) {
+            // ============================================================ MMA issuers
+            // Barrier operations stall the issuing thread for a few hundred cycles, and the
+            // tensor core holds only a short queue of these small MMAs: one issuer that also
+            // waits and commits leaves the tensor core idle much of the time.  Warp 9 issues
+            // the transposed products S^T, dP^T; warp 10 the accumulations dV, dK and dQ.
+            const bool issuer_t = warp == kBwdWarpMma;
             bool ok = true;
             auto wait = [&](int b, int parity) -> bool {
                 ok = ok && mbar_wait(bar(b), static_cast<uint32_t>(parity) & 1, limit, abort_flag);
@@ -240,13 +274,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                     umma_ss(tmem + d_col, a0 + o, b0 + o, C::kIdescT, kk > 0 ? 1u : 0u);
                 }
             };
-            // dV += P^T dO_i or dK += dS^T Q_i: A (bf16, packed two per column) from TMEM with the
-            // query halves at columns a_col and a_col + 64; B MN-major in shared memory.
-            auto issue_acc = [&](uint32_t d_col, uint32_t a_col, int b_off, bool accumulate) {
+            // dV += P^T dO_i or dK += dS^T Q_i: A (bf16, packed two per column) from TMEM, the two
+            // query halves half_stride columns apart (64 when each half sits over its own 64
+            // source columns, 32 when packed back to back); B MN-major in shared memory.
+            auto issue_acc = [&](uint32_t d_col, uint32_t a_col, uint32_t half_stride, int b_off, bool accumulate) {
                 const uint64_t b0 = smem_desc(sbase + b_off, C::kBlkBytes, C::kAtomBytes, C::kLayout);
 #pragma unroll
                 for (int kk = 0; kk < kBlockM / 16; ++kk)
-                    umma_ts(tmem + d_col, tmem + a_col + 64u * (kk >> 2) + 8u * (kk & 3),
+                    umma_ts(tmem + d_col, tmem + a_col + half_stride * (kk >> 2) + 8u * (kk & 3),
                             b0 + ((kk * 16 * C::kRowBytes) >> 4), C::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
             };
             // dQ(t) = dS K_j: A = dS (MN-major, two 64-query blocks), B = K_j (MN-major).
@@ -258,43 +293,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                     umma_ss(tmem + C::kColDQ, a0 + ((kk * 16 * 128) >> 4), b0 + ((kk * 16 * C::kRowBytes) >> 4),
                             C::kIdescDQ, kk > 0 ? 1u : 0u);
             };
-            if (n > 0 && wait(kBbKV, 0) && wait(kBbQFull, 0)) {
-                tc_fence_after_sync();
-                issue_t(C::kColS, C::kOffK, C::kOffQ);
-                umma_commit(bar(kBbSFull));
-                issue_t(C::kColDP, C::kOffV, C::kOffDO);
-                umma_commit(bar(kBbDPFull));
-            }
-            for (int t = 0; ok && t < n; ++t) {
-                const int s = t & 1;
-                if (!wait(kBbPReady, t)) break;
-                tc_fence_after_sync();
-                issue_acc(C::kColDV, C::kColS, C::kOffDO + s * C::kTileBytes, t > 0);
-                if (t + 1 < n) {
-                    if (!wait(kBbQFull + (s ^ 1), (t + 1) >> 1)) break;
+            if (issuer_t) {
+                // S^T(t), dP^T(t) for every t; the stage of tile t is released (one of two
+                // arrivals) once dP^T(t) has been issued, its last read by this issuer.
+                if (n > 0 && wait(kBbKV, 0) && wait(kBbQFull, 0)) {
                     tc_fence_after_sync();
-                    issue_t(C::kColS, C::kOffK, C::kOffQ + (s ^ 1) * C::kTileBytes);
+                    issue_t(C::kColS, C::kOffK, C::kOffQ);
                     umma_commit(bar(kBbSFull));
-                }
-                if (!wait(kBbDSReady, t)) break;
-                tc_fence_after_sync();
-                issue_acc(C::kColDK, C::kColDP, C::kOffQ + s * C::kTileBytes, t > 0);
-                umma_commit(bar(kBbQEmpty + s));
-                if (!C::kDQAlias && t > 0 && !wait(kBbDQFree, t - 1)) break;
-                tc_fence_after_sync();
-                issue_dq();
-                umma_commit(bar(kBbDQFull));
-                if (t + 1 < n) {
-                    if (C::kDQAlias && !wait(kBbDQFree, t)) break;
-                    tc_fence_after_sync();
-                    issue_t(C::kColDP, C::kOffV, C::kOffDO + (s ^ 1) * C::kTileBytes);
+                    issue_t(C::kColDP, C::kOffV, C::kOffDO);
                     umma_commit(bar(kBbDPFull));
+                    umma_commit(bar(kBbQEmpty));
+                }
+                for (int t = 0; ok && t + 1 < n; ++t) {
+                    const int s1 = (t + 1) % C::kQStages;
+                    // S^T(t+1) overwrites S^T(t), loaded by the compute warps (d <= 64), or P^T(t)
+                    // (d = 128), which dV(t) must have read
+                    if (!wait(C::kDSOwn ? kBbSFree : kBbDVDone, t) || !wait(kBbQFull + s1, (t + 1) / C::kQStages)) break;
+                    tc_fence_after_sync();
+                    issue_t(C::kColS, C::kOffK, C::kOffQ + s1 * C::kTileBytes);
+                    umma_commit(bar(kBbSFull));
+                    // dP^T(t+1) overwrites dP^T(t): loaded by the compute warps (d <= 64), or, with
+                    // dS^T and dQ in those columns (d = 128), dK(t) and dQ(t) done and dQ(t) read out
+                    if (!wait(C::kDSOwn ? kBbDPFree : kBbDQFree, t)) break;
+                    tc_fence_after_sync();
+                    issue_t(C::kColDP, C::kOffV, C::kOffDO + s1 * C::kTileBytes);
+                    umma_commit(bar(kBbDPFull));
+                    umma_commit(bar(kBbQEmpty + s1));
+                }
+            } else {
+                if (n > 0) wait(kBbKV, 0);
+                for (int t = 0; ok && t < n; ++t) {
+                    const int s = t % C::kQStages;
+                    if (!wait(kBbPReady, t)) break;
+                    tc_fence_after_sync();
+                    issue_acc(C::kColDV, C::kColP, C::kPHalf, C::kOffDO + s * C::kTileBytes, t > 0);
+                    umma_commit(bar(kBbDVDone));
+                    if (!wait(kBbDSReady, t)) break;
+                    tc_fence_after_sync();
+                    issue_acc(C::kColDK, C::kColDS, C::kPHalf, C::kOffQ + s * C::kTileBytes, t > 0);
+                    umma_commit(bar(kBbQEmpty + s));
+                    if (C::kDSOwn) umma_commit(bar(kBbDKDone));
+                    if (!C::kDQAlias && t > 0 && !wait(kBbDQFree, t - 1)) break;
+                    tc_fence_after_sync();
+                    issue_dq();
+                    umma_commit(bar(kBbDQFull));
                 }
             }
             umma_commit(bar(kBbDone));
             if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
-            umma_commit(bar(kBbDrain));
-            mbar_wait(bar(kBbDrain), 0, kDrainLimitNs, nullptr);
+            const int me = issuer_t ? 0 : 1;
+            umma_commit(bar(kBbDrain + me));
+            mbar_wait(bar(kBbDrain + me), 0, kDrainLimitNs, nullptr);
         }
     } else if (warp >= kBwdWarpDq) {
         regs_decrease<kBwdDqRegs>();
@@ -331,12 +380,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t t_s = tmem + lane_base + C::kColS + 64u * h;
         const uint32_t t_dp = tmem + lane_base + C::kColDP + 64u * h;
+        const uint32_t t_ds = tmem + lane_base + C::kColDS + C::kPHalf * h;
+        const uint32_t t_p = tmem + lane_base + C::kColP + C::kPHalf * h;
         const uint32_t ds_row = sbase + C::kOffDS + h * C::kDSBlk + k * 128;  // this thread's dS^T row
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 sc2 = make_float2(p.scale, p.scale);
         bool ok = true;
         for (int t = 0; t < n; ++t) {
-            const int s = t & 1;
+            const int s = t % C::kQStages;
             const int i0 = (i_first + t) * kBlockM;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbSFull), t & 1, limit, abort_flag));
             if (!ok) break;
@@ -345,6 +396,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
             tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
             tmem_ld_wait();
+            if constexpr (C::kDSOwn) {  // the S^T columns may now be overwritten by S^T(t+1)
+                tc_fence_before_sync();
+                mbar_arrive(bar(kBbSFree));
+            }
             // P = exp2(S scale log2(e) - L log2(e)); L = +inf gives 0 (row past N or with no key)
             const uint32_t l_addr = sbase + C::kOffL + s * 512 + h * 256;
             float pf[64];
@@ -370,7 +425,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             }
 #pragma unroll
             for (int c = 0; c < 64; c += 2) pk[c / 2] = pack_bf16x2(pf[c], pf[c + 1]);
-            tmem_st32(t_s, pk);
+            if (C::kDSOwn && t > 0) {  // dK(t-1) must have read dS^T(t-1) from the shared columns
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDKDone), (t - 1) & 1, limit, abort_flag));
+                if (!ok) break;
+                tc_fence_after_sync();
+            }
+            tmem_st32(t_p, pk);
             tmem_st_wait();
             tc_fence_before_sync();
             mbar_arrive(bar(kBbPReady));
@@ -381,6 +441,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             tmem_ld32(t_dp, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
             tmem_ld32(t_dp + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
             tmem_ld_wait();
+            if constexpr (C::kDSOwn) {  // the dP^T columns may now be overwritten by dP(t+1)
+                tc_fence_before_sync();
+                mbar_arrive(bar(kBbDPFree));
+            }
             // dS' = scale dS = P o (dP scale - scale D)
             const uint32_t d_addr = sbase + C::kOffDsc + s * 512 + h * 256;
 #pragma unroll
@@ -395,7 +459,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                 pk[c / 2] = pack_bf16x2(g01.x, g01.y);
                 pk[c / 2 + 1] = pack_bf16x2(g23.x, g23.y);
             }
-            tmem_st32(t_dp, pk);
+            if constexpr (C::kDSOwn) {
+                // dV(t) must have read P^T(t) from the shared columns, and dQ(t-1) dS(t-1) from
+                // shared memory
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDVDone), t & 1, limit, abort_flag) &&
+                                                 (t == 0 || mbar_wait(bar(kBbDQFull), (t - 1) & 1, limit, abort_flag)));
+                if (!ok) break;
+                tc_fence_after_sync();
+            }
+            tmem_st32(t_ds, pk);
             // dS^T row k into the MN-major dS operand: 16-byte chunk q8 of the 128-byte row goes
             // to chunk q8 ^ (k mod 8) (128-byte swizzle).
 #pragma unroll
