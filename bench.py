@@ -35,7 +35,7 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from fa_inputs import attention_inputs, decode_inputs, grad_output, sample_slices  # noqa: E402
+from fa_inputs import attention_inputs, decode_inputs, gqa_decode_inputs, grad_output, sample_slices  # noqa: E402
 
 METRIC = "attention fwd TFLOP/s (% of BF16 peak); decode KV GB/s (% of HBM peak)"
 UNIT = "TFLOP/s"
@@ -212,8 +212,9 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     if args.decode_only:
         decode = run_decode(fa, dev, stream, args, world)
+        gqa = run_decode_gqa(fa, dev, stream, args, world)
         if rank == 0:
-            print(json.dumps({"decode": decode}), flush=True)
+            print(json.dumps({"decode": decode, "decode_gqa": gqa}), flush=True)
         return 0
     if args.bwd_only:
         backward = run_bwd(fa, dev, stream, args, world)
@@ -300,6 +301,7 @@ def run_ours(args, world, rank, local):
     }
     if decode is not None:
         line["decode"] = decode
+        line["decode_gqa"] = run_decode_gqa(fa, dev, stream, args, world)
     if not args.no_extra:
         line["other_fwd_configs"] = run_other_fwd(fa, dev, stream, args, world)
     if not args.no_bwd:
@@ -457,6 +459,41 @@ def run_decode(fa, dev, stream, args, world):
     pk, src = peaks()
     gbs = world * (kv_bytes + other) / (ms / 1e3) / 1e9
     return {"workload": "split-KV decode B=16 H=32 d=128, lengths U[1024,32768] (seed 0), bf16 O",
+            "n_splits": n, "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
+            "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2}
+
+
+GQA = dict(B=16, Hq=32, Hkv=8, Nk_max=32768, d=128, lo=1024, hi=32768)
+
+
+def run_decode_gqa(fa, dev, stream, args, world):
+    """Split-KV decode with 4 query heads per key/value head (Llama-style 32 / 8 grouping)."""
+    B, Hq, Hkv, Nk_max, d = GQA["B"], GQA["Hq"], GQA["Hkv"], GQA["Nk_max"], GQA["d"]
+    q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=GQA["lo"], hi=GQA["hi"], device=dev)
+    lens_d = lens.to(dev)
+    n = fa.decode_default_splits(B, Hkv, Nk_max, fa.num_sms(dev))
+    ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n), dtype=torch.uint8, device=dev)
+    o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
+    for _ in range(max(args.warmup, 3)):
+        fa.decode_splitkv_gqa(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
+    torch.cuda.synchronize(dev)
+    steps = max(args.steps // 4, 5)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    e0.record(stream)
+    for _ in range(steps):
+        fa.decode_splitkv_gqa(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+    assert fa.get_device_error(dev) == fa.FA_OK
+    kv_bytes = sum(2 * Hkv * int(n_b) * d * 2 for n_b in lens.tolist())
+    other = B * Hq * (d * 2 + d * 2 + 4)
+    pk, src = peaks()
+    gbs = world * (kv_bytes + other) / (ms / 1e3) / 1e9
+    return {"workload": f"GQA split-KV decode B={B} Hq={Hq} Hkv={Hkv} d={d}, lengths U[1024,32768] (seed 0), bf16 O",
             "n_splits": n, "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
             "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2}
 

@@ -9,6 +9,7 @@ Entry points (same names as the C ABI, without the ``fa_`` prefix):
   fwd              exact attention forward (tiled, online softmax)
   bwd              exact attention backward (dQ, dK, dV; P recomputed from LSE)
   decode_splitkv   split-KV single-query decode with log-sum-exp combine
+  decode_splitkv_gqa  the same with grouped key/value heads (query heads of a group packed)
   merge_states     log-sum-exp combine of partial states
   decode_default_splits, decode_workspace_size, get_device_error,
   set_wait_timeout_ns, status_string
@@ -58,6 +59,8 @@ def _load():
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, i, vp]
     lib.fa_decode_splitkv.restype = i
+    lib.fa_decode_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i, i, vp]
+    lib.fa_decode_splitkv_gqa.restype = i
     lib.fa_merge_states.argtypes = [vp, vp, i, i, i, vp, vp, i, vp]
     lib.fa_merge_states.restype = i
     lib.fa_get_device_error.argtypes = [vp]
@@ -241,6 +244,47 @@ def decode_splitkv(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out_dty
                                    _ptr(workspace), workspace.numel(), B, H, Nk_max, d, dv, scale, n,
                                    _odt(out.dtype), _stream(dev))
     _check(st, "fa_decode_splitkv")
+    return out, lse
+
+
+def decode_splitkv_gqa(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out_dtype=torch.bfloat16, out=None,
+                       lse=None, workspace=None, return_lse=True):
+    """Split-KV decode with grouped key/value heads: q [B,Hq,1,d], caches [B,Hkv,Nk_max,d|dv] bf16 with Hkv
+    dividing Hq (query head h uses key/value head h // (Hq // Hkv)), seqlens int32 [B] on the same GPU.
+
+    Returns (O [B,Hq,1,dv], LSE fp32 [B,Hq,1] or None).
+    """
+    lib = _load()
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    _need(seqlens, "seqlens", torch.int32, dev)
+    B, Hq, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes a single query per (b, h)")
+    Hkv, Nk_max, dv = k_cache.shape[1], v_cache.shape[2], v_cache.shape[3]
+    if (tuple(k_cache.shape) != (B, Hkv, Nk_max, d) or tuple(v_cache.shape[:2]) != (B, Hkv)
+            or seqlens.numel() != B):
+        raise ValueError("shape mismatch between q, caches and seqlens")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    n = int(n_splits) if n_splits else decode_default_splits(B, Hkv, Nk_max, num_sms(dev))
+    if workspace is None:
+        workspace = torch.empty(max(decode_workspace_size(B, Hq, dv, max(1, min(n, Nk_max))), 256),
+                                dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if out is None:
+        out = torch.empty((B, Hq, 1, dv), dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib.fa_decode_splitkv_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(out), _ptr(lse),
+                                       _ptr(workspace), workspace.numel(), B, Hq, Hkv, Nk_max, d, dv, scale, n,
+                                       _odt(out.dtype), _stream(dev))
+    _check(st, "fa_decode_splitkv_gqa")
     return out, lse
 
 

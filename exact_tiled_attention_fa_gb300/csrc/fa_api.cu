@@ -290,29 +290,36 @@ size_t fa_decode_workspace_size(int B, int H, int dv, int n_splits)
     return round_up(slots * dv * sizeof(float), kAlign) + round_up(slots * sizeof(float), kAlign);
 }
 
-fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,
-                            float* lse, void* workspace, size_t ws_bytes, int B, int H, int Nk_max, int d, int dv,
-                            float scale, int n_splits, fa_dtype o_dtype, void* stream)
+}  // extern "C"
+
+namespace {
+
+// Split-KV decode for Hq query heads over Hkv key/value heads (Hkv = Hq: multi-head).
+fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,
+                      float* lse, void* workspace, size_t ws_bytes, int B, int Hq, int Hkv, int Nk_max, int d, int dv,
+                      float scale, int n_splits, fa_dtype o_dtype, void* stream)
 {
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seqlens_k == nullptr || o == nullptr ||
         workspace == nullptr)
         return FA_ERR_INVALID_ARG;
-    if (B <= 0 || H <= 0 || Nk_max <= 0 || d <= 0 || dv <= 0 || n_splits < 0) return FA_ERR_INVALID_ARG;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nk_max <= 0 || d <= 0 || dv <= 0 || n_splits < 0) return FA_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return FA_ERR_INVALID_ARG;
     if (!dtype_ok(o_dtype) || !scale_ok(scale)) return FA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(o, 16) ||
         !aligned(lse, 4) || !aligned(seqlens_k, 4) || !aligned(workspace, kAlign))
         return FA_ERR_INVALID_ARG;
-    if (static_cast<long long>(B) * H > 0x7fffffffLL || B > 65535 || H > 65535) return FA_ERR_INVALID_ARG;
-    if (!head_ok(d) || dv != d) return FA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * Hq > 0x7fffffffLL || B > 65535 || Hkv > 65535) return FA_ERR_INVALID_ARG;
+    const int R = Hq / Hkv;
+    if (!head_ok(d) || dv != d || (R != 1 && R != 2 && R != 4 && R != 8)) return FA_ERR_UNSUPPORTED;
 
     int n = n_splits;
     if (n == 0) {
         int sms = 0;
         if (sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
-        n = fa_decode_default_splits(B, H, Nk_max, sms);
+        n = fa_decode_default_splits(B, Hkv, Nk_max, sms);  // one CTA per (b, key/value head, split)
     }
     if (n > Nk_max) n = Nk_max;
-    if (ws_bytes < fa_decode_workspace_size(B, H, dv, n)) return FA_ERR_WORKSPACE;
+    if (ws_bytes < fa_decode_workspace_size(B, Hq, dv, n)) return FA_ERR_WORKSPACE;
     // Fixed chunk per split, a whole number of key blocks; trailing splits may be empty.
     long long chunk = (static_cast<long long>(Nk_max) + n - 1) / n;
     chunk = (chunk + fa::kDecodeKeyBlock - 1) / fa::kDecodeKeyBlock * fa::kDecodeKeyBlock;
@@ -325,20 +332,41 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
     p.k = k_cache;
     p.v = v_cache;
     p.seqlens = seqlens_k;
-    const size_t slots = static_cast<size_t>(B) * H * n_eff;
+    const size_t slots = static_cast<size_t>(B) * Hq * n_eff;
     p.o_part = static_cast<float*>(workspace);
     p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(slots * dv * sizeof(float), kAlign));
     p.o = o;
     p.lse = lse;
     p.status = status;
     p.B = B;
-    p.H = H;
+    p.H = Hq;
+    p.Hkv = Hkv;
     p.Nk_max = Nk_max;
     p.n_splits = n_eff;
     p.chunk = static_cast<int>(chunk);
     p.scale_log2 = scale * 1.4426950408889634f;
     cudaError_t e = fa::launch_decode(p, d, o_dtype, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,
+                            float* lse, void* workspace, size_t ws_bytes, int B, int H, int Nk_max, int d, int dv,
+                            float scale, int n_splits, fa_dtype o_dtype, void* stream)
+{
+    return decode_impl(q, k_cache, v_cache, seqlens_k, o, lse, workspace, ws_bytes, B, H, H, Nk_max, d, dv, scale,
+                       n_splits, o_dtype, stream);
+}
+
+fa_status fa_decode_splitkv_gqa(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k,
+                                void* o, float* lse, void* workspace, size_t ws_bytes, int B, int Hq, int Hkv,
+                                int Nk_max, int d, int dv, float scale, int n_splits, fa_dtype o_dtype, void* stream)
+{
+    return decode_impl(q, k_cache, v_cache, seqlens_k, o, lse, workspace, ws_bytes, B, Hq, Hkv, Nk_max, d, dv, scale,
+                       n_splits, o_dtype, stream);
 }
 
 fa_status fa_merge_states(const float* o_parts, const float* lse_parts, int n_parts, int rows, int dv, void* o,

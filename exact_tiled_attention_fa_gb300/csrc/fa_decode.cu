@@ -7,8 +7,8 @@
 // a second kernel merges them (lse = log sum_s exp(lse_s),
 // o = sum_s exp(lse_s - lse) o_s -- the lse form of section 1 `merge_states`).
 //
-// The split kernel is bound by HBM bandwidth (one FMA per key element), so it
-// uses no tensor core: every lane streams 16-byte slices of key rows with
+// The split kernel is bound by HBM bandwidth (R FMAs per key element for R query
+// heads sharing a key/value head), so it uses no tensor core: every lane streams 16-byte slices of key rows with
 // read-only, L1-bypassing loads, D/8 lanes cooperate on one key, eight loads of
 // K and eight of V are in flight per lane before any arithmetic, and the
 // softmax is online per warp in the base-2 domain.  Partial states go to
@@ -48,48 +48,64 @@ __device__ __forceinline__ void unpack8(const uint4 u, float (&f)[8])
     }
 }
 
-template <int D>
+template <int D, int R>
 struct DecCfg {
     static constexpr int kLanesPerKey = D / 8;                    // 8 bf16 (16 B) per lane
     static constexpr int kKeysPerStep = 32 / kLanesPerKey;        // keys one warp-wide load covers
-    static constexpr int kKeysPerIter = kDecSteps * kKeysPerStep; // keys per warp per iteration
+    // 16-byte loads of K (and of V) in flight per lane: fewer as the packed query rows take registers
+    static constexpr int kSteps = R <= 2 ? kDecSteps : (R == 4 ? 4 : 2);
+    static constexpr int kKeysPerIter = kSteps * kKeysPerStep;    // keys per warp per iteration
 };
 
-// One CTA per (split, h, b).  Writes o_part / lse_part of a non-empty split.
-template <int D>
+// One CTA per (split, KV head g, sequence b).  The R query heads g*R .. g*R+R-1 share the
+// KV head ("flash_lab.py" section 4: the query heads of a GQA group are packed as the rows
+// of q), so each K/V element is read once and used R times.  R = 1 is plain multi-head
+// attention.  Writes o_part / lse_part of a non-empty split for each of the R heads.
+template <int D, int R>
 __global__ void __launch_bounds__(kDecWarps * 32) fa_decode_split_kernel(const DecodeParams p)
 {
-    using C = DecCfg<D>;
+    using C = DecCfg<D, R>;
+    constexpr int S = C::kSteps;
     const int s = blockIdx.x;
-    const int h = blockIdx.y;
+    const int g = blockIdx.y;
     const int b = blockIdx.z;
     const int n = clamp_len(p.seqlens[b], p.Nk_max, p.status);
     const int k0 = s * p.chunk;
     if (k0 >= n) return;  // empty split: nothing to write, the combine skips it
     const int k1 = min(n, k0 + p.chunk);
-    const size_t bh = static_cast<size_t>(b) * p.H + h;
+    const size_t bkv = static_cast<size_t>(b) * p.Hkv + g;
+    const size_t bq0 = static_cast<size_t>(b) * p.H + static_cast<size_t>(g) * R;  // first query head
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int grp = lane / C::kLanesPerKey;  // which key of a step this lane serves
     const int sub = lane % C::kLanesPerKey;  // which 8-element slice of the row
 
-    float q[8];
-    unpack8(*reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + bh * D + sub * 8), q);
+    float q[R][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] *= p.scale_log2;  // scores come out in the base-2 domain
+    for (int r = 0; r < R; ++r) {
+        unpack8(*reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(p.q) + (bq0 + r) * D + sub * 8),
+                q[r]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[r][i] *= p.scale_log2;  // scores come out in the base-2 domain
+    }
 
-    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(p.k) + bh * p.Nk_max * D + sub * 8;
-    const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(p.v) + bh * p.Nk_max * D + sub * 8;
+    const __nv_bfloat16* kb = reinterpret_cast<const __nv_bfloat16*>(p.k) + bkv * p.Nk_max * D + sub * 8;
+    const __nv_bfloat16* vb = reinterpret_cast<const __nv_bfloat16*>(p.v) + bkv * p.Nk_max * D + sub * 8;
 
-    float m = -INFINITY;  // running max (warp-uniform)
-    float l = 0.f;        // this lane group's share of the running sum
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float m[R], l[R], acc[R][8];  // per packed row: running max (warp-uniform), this lane group's sum and output
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        m[r] = -INFINITY;
+        l[r] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[r][i] = 0.f;
+    }
 
     for (int base = k0 + warp * C::kKeysPerIter; base < k1; base += kDecWarps * C::kKeysPerIter) {
-        uint4 kr[kDecSteps], vr[kDecSteps];
+        uint4 kr[S], vr[S];
 #pragma unroll
-        for (int t = 0; t < kDecSteps; ++t) {
+        for (int t = 0; t < S; ++t) {
             const int key = base + t * C::kKeysPerStep + grp;
             if (key < k1) {
                 kr[t] = ld_stream_v4(kb + static_cast<size_t>(key) * D);
@@ -99,79 +115,96 @@ __global__ void __launch_bounds__(kDecWarps * 32) fa_decode_split_kernel(const D
                 vr[t] = make_uint4(0, 0, 0, 0);
             }
         }
-        float sc[kDecSteps];
+        float sc[S][R];
 #pragma unroll
-        for (int t = 0; t < kDecSteps; ++t) {
+        for (int t = 0; t < S; ++t) {
             float kf[8];
             unpack8(kr[t], kf);
-            float x = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) x = fmaf(q[i], kf[i], x);
-#pragma unroll
-            for (int o = C::kLanesPerKey / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
             const int key = base + t * C::kKeysPerStep + grp;
-            sc[t] = key < k1 ? x : -INFINITY;
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float x = 0.f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) x = fmaf(q[r][i], kf[i], x);
+#pragma unroll
+                for (int o = C::kLanesPerKey / 2; o >= 1; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                sc[t][r] = key < k1 ? x : -INFINITY;
+            }
         }
-        float bm = sc[0];
+        float m_new[R], alpha[R];
 #pragma unroll
-        for (int t = 1; t < kDecSteps; ++t) bm = fmaxf(bm, sc[t]);
+        for (int r = 0; r < R; ++r) {
+            float bm = sc[0][r];
 #pragma unroll
-        for (int o = C::kLanesPerKey; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-        // key `base` (group 0, step 0) is always visible, so bm is finite
-        const float m_new = fmaxf(m, bm);
-        const float alpha = ex2(m - m_new);  // 0 on the first block (m = -inf)
-        float ps = 0.f;
+            for (int t = 1; t < S; ++t) bm = fmaxf(bm, sc[t][r]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] *= alpha;
+            for (int o = C::kLanesPerKey; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+            // key `base` (group 0, step 0) is always visible, so bm is finite
+            m_new[r] = fmaxf(m[r], bm);
+            alpha[r] = ex2(m[r] - m_new[r]);  // 0 on the first block (m = -inf)
 #pragma unroll
-        for (int t = 0; t < kDecSteps; ++t) {
-            const float pt = ex2(sc[t] - m_new);  // 0 for keys past the split
-            ps += pt;
+            for (int i = 0; i < 8; ++i) acc[r][i] *= alpha[r];
+            l[r] *= alpha[r];
+        }
+#pragma unroll
+        for (int t = 0; t < S; ++t) {
             float vf[8];
             unpack8(vr[t], vf);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(pt, vf[i], acc[i]);
+            for (int r = 0; r < R; ++r) {
+                const float pt = ex2(sc[t][r] - m_new[r]);  // 0 for keys past the split
+                l[r] += pt;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[r][i] = fmaf(pt, vf[i], acc[r][i]);
+            }
         }
-        l = l * alpha + ps;
-        m = m_new;
+#pragma unroll
+        for (int r = 0; r < R; ++r) m[r] = m_new[r];
     }
     // Sum the lane groups of the warp (they share m).
 #pragma unroll
     for (int o = C::kLanesPerKey; o < 32; o <<= 1) {
-        l += __shfl_xor_sync(0xffffffffu, l, o);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+        for (int r = 0; r < R; ++r) {
+            l[r] += __shfl_xor_sync(0xffffffffu, l[r], o);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[r][i] += __shfl_xor_sync(0xffffffffu, acc[r][i], o);
+        }
     }
     // Merge the warps (each with its own max) through shared memory.
-    __shared__ float sm_m[kDecWarps], sm_l[kDecWarps];
-    __shared__ float sm_acc[kDecWarps][D];
+    __shared__ float sm_m[kDecWarps][R], sm_l[kDecWarps][R];
+    __shared__ float sm_acc[kDecWarps][R][D];
     if (lane == 0) {
-        sm_m[warp] = m;
-        sm_l[warp] = l;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            sm_m[warp][r] = m[r];
+            sm_l[warp][r] = l[r];
+        }
     }
     if (grp == 0) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) sm_acc[warp][sub * 8 + i] = acc[i];
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) sm_acc[warp][r][sub * 8 + i] = acc[r][i];
     }
     __syncthreads();
-    float M = sm_m[0];
+    for (int idx = threadIdx.x; idx < R * D; idx += kDecWarps * 32) {
+        const int r = idx / D;
+        const int c = idx - r * D;
+        float M = sm_m[0][r];
 #pragma unroll
-    for (int w = 1; w < kDecWarps; ++w) M = fmaxf(M, sm_m[w]);
-    float f[kDecWarps];
-    float L = 0.f;
+        for (int w = 1; w < kDecWarps; ++w) M = fmaxf(M, sm_m[w][r]);
+        float L = 0.f, o = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
-        f[w] = sm_m[w] == -INFINITY ? 0.f : ex2(sm_m[w] - M);
-        L += sm_l[w] * f[w];
-    }
-    const size_t slot = bh * p.n_splits + s;
-    for (int c = threadIdx.x; c < D; c += kDecWarps * 32) {
-        float o = 0.f;
-#pragma unroll
-        for (int w = 0; w < kDecWarps; ++w) o = fmaf(sm_acc[w][c], f[w], o);
+        for (int w = 0; w < kDecWarps; ++w) {
+            const float f = sm_m[w][r] == -INFINITY ? 0.f : ex2(sm_m[w][r] - M);
+            L += sm_l[w][r] * f;
+            o = fmaf(sm_acc[w][r][c], f, o);
+        }
+        const size_t slot = (bq0 + r) * p.n_splits + s;
         p.o_part[slot * D + c] = o / L;
+        if (c == 0) p.lse_part[slot] = (M + log2f(L)) * kLn2;
     }
-    if (threadIdx.x == 0) p.lse_part[slot] = (M + log2f(L)) * kLn2;
 }
 
 template <typename OutT>
@@ -249,8 +282,15 @@ __global__ void __launch_bounds__(128) fa_merge_kernel(const MergeParams p)
 template <int D>
 cudaError_t launch_decode_d(const DecodeParams& p, fa_dtype o_dtype, cudaStream_t st)
 {
-    dim3 grid(p.n_splits, p.H, p.B);
-    fa_decode_split_kernel<D><<<grid, kDecWarps * 32, 0, st>>>(p);
+    dim3 grid(p.n_splits, p.Hkv, p.B);
+    const int R = p.H / p.Hkv;
+    switch (R) {
+    case 1: fa_decode_split_kernel<D, 1><<<grid, kDecWarps * 32, 0, st>>>(p); break;
+    case 2: fa_decode_split_kernel<D, 2><<<grid, kDecWarps * 32, 0, st>>>(p); break;
+    case 4: fa_decode_split_kernel<D, 4><<<grid, kDecWarps * 32, 0, st>>>(p); break;
+    case 8: fa_decode_split_kernel<D, 8><<<grid, kDecWarps * 32, 0, st>>>(p); break;
+    default: return cudaErrorInvalidValue;
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     MergeParams m{};

@@ -80,8 +80,8 @@ constexpr int kDecodeKeyBlock = 64;
 
 struct DecodeParams {
     const void* q;        // bf16 [B*H][d]
-    const void* k;        // bf16 [B*H][Nk_max][d]
-    const void* v;        // bf16 [B*H][Nk_max][dv]
+    const void* k;        // bf16 [B*Hkv][Nk_max][d]
+    const void* v;        // bf16 [B*Hkv][Nk_max][dv]
     const int* seqlens;   // int32 [B]
     float* o_part;        // fp32 [B*H][n_splits][dv]
     float* lse_part;      // fp32 [B*H][n_splits]
@@ -89,6 +89,7 @@ struct DecodeParams {
     float* lse;           // [B*H] or nullptr
     int* status;
     int B, H, Nk_max, n_splits, chunk;
+    int Hkv;              // key/value heads; query head h reads key/value head h / (H / Hkv)
     float scale_log2;
 };
 

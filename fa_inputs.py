@@ -71,6 +71,25 @@ def decode_inputs(B, H, Nk_max, d, dv, seed=0, lo=1024, hi=None, device="cpu", s
     return q.contiguous(), k.contiguous(), v.contiguous(), seqlens
 
 
+def gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, dv, seed=0, lo=1024, hi=None, device="cpu", seqlens=None):
+    """Single-query decode inputs with grouped key/value heads: q [B,Hq,1,d], k_cache [B,Hkv,Nk_max,d],
+    v_cache [B,Hkv,Nk_max,dv] (bf16, NaN past each sequence's length) and seqlens int32 [B] on the CPU.
+    Drawn like ``decode_inputs`` (q, then K, then V from one generator)."""
+    hi = Nk_max if hi is None else hi
+    if seqlens is None:
+        seqlens = decode_lengths(B, lo, hi, seed)
+    g = _gen(device, seed)
+    q = torch.randn((B, Hq, 1, d), generator=g, device=device, dtype=torch.float32).to(BF16)
+    k = torch.randn((B, Hkv, Nk_max, d), generator=g, device=device, dtype=torch.float32).to(BF16)
+    v = torch.randn((B, Hkv, Nk_max, dv), generator=g, device=device, dtype=torch.float32).to(BF16)
+    nan = float("nan")
+    for b in range(B):
+        n = int(seqlens[b])
+        k[b, :, n:, :] = nan
+        v[b, :, n:, :] = nan
+    return q.contiguous(), k.contiguous(), v.contiguous(), seqlens
+
+
 def sample_slices(total, k, seed=1):
     """k distinct indices in [0, total) drawn with a seeded random permutation (sorted)."""
     g = torch.Generator(device="cpu").manual_seed(int(seed))

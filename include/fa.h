@@ -14,6 +14,9 @@
  *                       tile from the forward's log-sum-exp ("flash_lab.py", section 3
  *                       `flash_bwd`, FlashAttention-2 form; the value it reaches is
  *                       section 2 `standard_attention_bwd`).
+ *   fa_decode_splitkv_gqa  the same with the query heads of a key/value group packed
+ *                       together ("flash_lab.py", section 4: GQA packs a group's query heads
+ *                       as the rows of q; `decode_attention_time` method "fd").
  *   fa_merge_states     the log-sum-exp combine of partial states on its own
  *                       ("flash_lab.py", section 4 `split_kv_decode` combine, the
  *                       lse form of section 1 `merge_states`).
@@ -38,8 +41,8 @@
  *     Failures the device detects (a bounded wait that ran out, a sequence length out
  *     of range) are recorded in a device status word read by fa_get_device_error.
  *   - Supported head sizes: d = dv, d in {32, 64, 128}.  Other sizes return
- *     FA_ERR_UNSUPPORTED.  Heads are independent: the number of key/value heads equals
- *     the number of query heads.
+ *     FA_ERR_UNSUPPORTED.  Heads are independent; the number of key/value heads equals
+ *     the number of query heads except in fa_decode_splitkv_gqa.
  */
 #ifndef FA_H
 #define FA_H
@@ -159,6 +162,29 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
                             const int* seqlens_k, void* o, float* lse, void* workspace,
                             size_t ws_bytes, int B, int H, int Nk_max, int d, int dv, float scale,
                             int n_splits, fa_dtype o_dtype, void* stream);
+
+/*
+ * Split-KV decode with grouped key/value heads (GQA): Hq query heads share Hkv key/value heads,
+ * query head h reading key/value head h / R with R = Hq / Hkv.  The R query heads of a group are
+ * packed together ("flash_lab.py" section 4 `split_kv_decode`, q of shape [R, d]; section 4
+ * `decode_attention_time`, method "fd": one work item per (b, key/value head, split), K and V read
+ * once per group), so each cached key and value is read from memory once for all R heads.  The
+ * split, merge, arguments and errors are those of fa_decode_splitkv, with:
+ *
+ *   q          bf16 [B, Hq, 1, d]          (device)
+ *   k_cache    bf16 [B, Hkv, Nk_max, d]    (device)
+ *   v_cache    bf16 [B, Hkv, Nk_max, dv]   (device)
+ *   o          o_dtype [B, Hq, 1, dv]      (device, written)
+ *   lse        fp32 [B, Hq, 1]             (device, written; may be NULL)
+ *   workspace  ws_bytes >= fa_decode_workspace_size(B, Hq, dv, n) bytes, where n is n_splits or,
+ *              for n_splits = 0, fa_decode_default_splits(B, Hkv, Nk_max, <SMs of the device>).
+ *   Hkv >= 1 dividing Hq.  R = Hq / Hkv in {1, 2, 4, 8}; other group sizes return
+ *   FA_ERR_UNSUPPORTED.  Hkv = Hq is fa_decode_splitkv.
+ */
+fa_status fa_decode_splitkv_gqa(const void* q, const void* k_cache, const void* v_cache,
+                                const int* seqlens_k, void* o, float* lse, void* workspace,
+                                size_t ws_bytes, int B, int Hq, int Hkv, int Nk_max, int d, int dv,
+                                float scale, int n_splits, fa_dtype o_dtype, void* stream);
 
 /*
  * Bytes of device scratch that fa_decode_splitkv_noalloc owns (8 MiB): room for the split

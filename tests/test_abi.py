@@ -76,6 +76,19 @@ def test_decode_rejects_bad_arguments(lib):
     assert _dec(lib, ws_bytes=0) == fa.FA_ERR_WORKSPACE
 
 
+def test_gqa_decode_rejects_bad_arguments(lib):
+    f = lib.fa_decode_splitkv_gqa
+    def call(B=2, Hq=8, Hkv=2, Nk=1000, d=128, ws=P, ws_bytes=1 << 20, n=4):
+        return f(P, P, P, P, P, P, ws, ws_bytes, B, Hq, Hkv, Nk, d, d, 0.1, n, 0, NULL)
+    assert call(Hkv=0) == fa.FA_ERR_INVALID_ARG
+    assert call(Hq=6, Hkv=4) == fa.FA_ERR_INVALID_ARG   # Hkv must divide Hq
+    assert call(Hq=6, Hkv=2) == fa.FA_ERR_UNSUPPORTED   # group size 3
+    assert call(Hq=32, Hkv=2) == fa.FA_ERR_UNSUPPORTED  # group size 16
+    need = lib.fa_decode_workspace_size(2, 8, 128, 4)
+    assert call(ws_bytes=need - 1) == fa.FA_ERR_WORKSPACE
+    assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
 def test_merge_rejects_bad_arguments(lib):
     m = lib.fa_merge_states
     assert m(NULL, P, 2, 3, 4, P, P, 0, NULL) == fa.FA_ERR_INVALID_ARG

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from fa_inputs import decode_inputs, merge_inputs
+from fa_inputs import decode_inputs, gqa_decode_inputs, merge_inputs
 from tests.parity import assert_close, to_np
 
 pytestmark = pytest.mark.gpu
@@ -106,3 +106,74 @@ def test_merge_states_against_oracle(n_parts, rows, dv, empty):
     if fin.any():
         assert np.abs(a[fin] - b[fin]).max() <= 1e-5 * max(1.0, np.abs(b[fin]).max())
     assert np.abs(to_np(o) - o_ref).max() <= 1e-5
+
+
+def oracle_gqa_compact(q, k, v, lens, scale):
+    """Oracle for grouped heads: query head h attends with key/value head h // R over its
+    sequence's prefix; each group's cache rows are repeated for its R query heads (the pages'
+    packing of a group's query heads against one K, V)."""
+    B, Hq = q.shape[0], q.shape[1]
+    R = Hq // k.shape[1]
+    dv = v.shape[-1]
+    O = np.zeros((B, Hq, 1, dv))
+    L = np.zeros((B, Hq, 1))
+    for b in range(B):
+        n = int(lens[b])
+        if n == 0:
+            L[b] = -np.inf
+            continue
+        kb = k[b, :, :n].cpu().repeat_interleave(R, dim=0)
+        vb = v[b, :, :n].cpu().repeat_interleave(R, dim=0)
+        O[b], L[b] = oracle.attention(q[b].cpu(), kb, vb, causal=False, scale=scale)
+    return O, L
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("R", [1, 2, 4, 8])
+@pytest.mark.parametrize("n_splits", [1, 5, 0])
+def test_gqa_decode(d, R, n_splits):
+    B, Hkv, Nk_max = 3, 2, 700
+    lens = torch.tensor([1, 300, 700], dtype=torch.int32)
+    q, k, v, _ = gqa_decode_inputs(B, Hkv * R, Hkv, Nk_max, d, d, seed=R + d, device=DEV, seqlens=lens)
+    scale = 1.0 / math.sqrt(d)
+    o_ref, lse_ref = oracle_gqa_compact(q, k, v, lens, scale)
+    for dt in (torch.float32, torch.bfloat16):
+        o, lse = fa().decode_splitkv_gqa(q, k, v, lens.to(DEV), scale=scale, n_splits=n_splits, out_dtype=dt)
+        torch.cuda.synchronize()
+        assert fa().get_device_error() == 0
+        assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16), what=f"gqa d={d} R={R} n={n_splits}")
+
+
+def test_gqa_full_size_sampled():
+    """The benchmark's GQA workload (B=16, Hq=32, Hkv=8, d=128, lengths U[1024, 32768]) in its
+    launch configuration; 24 seeded query heads against the oracle."""
+    B, Hq, Hkv, Nk_max, d = 16, 32, 8, 32768, 128
+    q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=1024, hi=Nk_max, device=DEV)
+    o, lse = fa().decode_splitkv_gqa(q, k, v, lens.to(DEV), out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == 0
+    R = Hq // Hkv
+    for idx in sample_slices_gqa(B * Hq, 24):
+        b, h = divmod(idx, Hq)
+        n = int(lens[b])
+        o_ref, l_ref = oracle.attention(q[b, h].cpu(), k[b, h // R, :n].cpu(), v[b, h // R, :n].cpu(), scale=1 / math.sqrt(d))
+        assert_close(o[b, h], lse[b, h], o_ref, l_ref, what=f"gqa full b={b} h={h}")
+
+
+def sample_slices_gqa(total, k):
+    from fa_inputs import sample_slices
+    return sample_slices(total, k, seed=1)
+
+
+def test_gqa_rejects_bad_groups():
+    q = torch.zeros((1, 6, 1, 64), dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros((1, 4, 128, 64), dtype=torch.bfloat16, device=DEV)
+    lens = torch.full((1,), 128, dtype=torch.int32, device=DEV)
+    with pytest.raises(fa().FaError) as e:  # 6 query heads over 4 key/value heads
+        fa().decode_splitkv_gqa(q, k, k, lens)
+    assert e.value.status == fa().FA_ERR_INVALID_ARG
+    q3 = torch.zeros((1, 6, 1, 64), dtype=torch.bfloat16, device=DEV)
+    k3 = torch.zeros((1, 2, 128, 64), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(fa().FaError) as e:  # groups of 3 have no kernel
+        fa().decode_splitkv_gqa(q3, k3, k3, lens)
+    assert e.value.status == fa().FA_ERR_UNSUPPORTED
