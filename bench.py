@@ -212,9 +212,10 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     if args.decode_only:
         decode = run_decode(fa, dev, stream, args, world)
-        gqa = run_decode_gqa(fa, dev, stream, args, world)
+        gqa = [run_decode_gqa(fa, dev, stream, args, world, Hkv=h) for h in (8, 4)]
+        pre = run_splitkv_prefill(fa, dev, stream, args, world)
         if rank == 0:
-            print(json.dumps({"decode": decode, "decode_gqa": gqa}), flush=True)
+            print(json.dumps({"decode": decode, "decode_gqa": gqa, "splitkv_prefill": pre}), flush=True)
         return 0
     if args.bwd_only:
         backward = run_bwd(fa, dev, stream, args, world)
@@ -301,7 +302,8 @@ def run_ours(args, world, rank, local):
     }
     if decode is not None:
         line["decode"] = decode
-        line["decode_gqa"] = run_decode_gqa(fa, dev, stream, args, world)
+        line["decode_gqa"] = [run_decode_gqa(fa, dev, stream, args, world, Hkv=h) for h in (8, 4)]
+        line["splitkv_prefill"] = run_splitkv_prefill(fa, dev, stream, args, world)
     if not args.no_extra:
         line["other_fwd_configs"] = run_other_fwd(fa, dev, stream, args, world)
     if not args.no_bwd:
@@ -466,17 +468,20 @@ def run_decode(fa, dev, stream, args, world):
 GQA = dict(B=16, Hq=32, Hkv=8, Nk_max=32768, d=128, lo=1024, hi=32768)
 
 
-def run_decode_gqa(fa, dev, stream, args, world):
-    """Split-KV decode with 4 query heads per key/value head (Llama-style 32 / 8 grouping)."""
-    B, Hq, Hkv, Nk_max, d = GQA["B"], GQA["Hq"], GQA["Hkv"], GQA["Nk_max"], GQA["d"]
+def run_decode_gqa(fa, dev, stream, args, world, Hkv=None):
+    """Split-KV decode with grouped key/value heads (32 query heads over 8: Llama-style; over 4)."""
+    B, Hq, Nk_max, d = GQA["B"], GQA["Hq"], GQA["Nk_max"], GQA["d"]
+    Hkv = GQA["Hkv"] if Hkv is None else Hkv
     q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=GQA["lo"], hi=GQA["hi"], device=dev)
     lens_d = lens.to(dev)
-    n = fa.decode_default_splits(B, Hkv, Nk_max, fa.num_sms(dev))
-    ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n), dtype=torch.uint8, device=dev)
+    n = 0  # the library's automatic split count; the workspace covers either heuristic
+    sms = fa.num_sms(dev)
+    n_ws = max(fa.decode_default_splits(B, Hkv, Nk_max, sms), min(-(-6 * sms // (B * Hkv)), -(-Nk_max // 128)))
+    ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n_ws), dtype=torch.uint8, device=dev)
     o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
     for _ in range(max(args.warmup, 3)):
-        fa.decode_splitkv_gqa(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
+        _, _ = fa.decode_splitkv_gqa(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
     torch.cuda.synchronize(dev)
     steps = max(args.steps // 4, 5)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -494,8 +499,42 @@ def run_decode_gqa(fa, dev, stream, args, world):
     pk, src = peaks()
     gbs = world * (kv_bytes + other) / (ms / 1e3) / 1e9
     return {"workload": f"GQA split-KV decode B={B} Hq={Hq} Hkv={Hkv} d={d}, lengths U[1024,32768] (seed 0), bf16 O",
-            "n_splits": n, "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
+            "group": Hq // Hkv, "unit": "tensor core" if Hq // Hkv not in (1, 2, 4) else "CUDA cores", "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
             "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2}
+
+
+SPLIT_PREFILL = dict(B=1, H=8, N=512, Nk=32768, d=128)
+
+
+def run_splitkv_prefill(fa, dev, stream, args, world):
+    """Few query tiles over a long context (B=1 H=8 N=512 Nk=32K d=128, causal): fa_fwd keeps
+    B*H*N/128 = 32 query tiles (16 CTAs); fa_fwd_splitkv splits the keys and merges."""
+    B, H, N, Nk, d = (SPLIT_PREFILL[x] for x in ("B", "H", "N", "Nk", "d"))
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=0, device=dev)
+    o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    n = fa.fwd_splitkv_default_splits(B, H, N, Nk, fa.num_sms(dev))
+    ws = torch.empty(fa.fwd_splitkv_workspace_size(B, H, N, d, n), dtype=torch.uint8, device=dev)
+    # visible pairs: query i (position Nk - N + i) sees Nk - N + i + 1 keys
+    fl = 4.0 * B * H * d * sum(Nk - N + i + 1 for i in range(N))
+    out = {"workload": f"causal prefill B={B} H={H} N={N} Nk={Nk} d={d}, bf16 O", "flops_exact": fl, "n_splits": n}
+    for name, call in (("fa_fwd", lambda: fa.fwd(q, k, v, causal=True, out=o, lse=lse)),
+                       ("fa_fwd_splitkv", lambda: fa.fwd_splitkv(q, k, v, causal=True, n_splits=n, out=o, lse=lse,
+                                                                 workspace=ws))):
+        for _ in range(max(args.warmup, 3)):
+            call()
+        steps = max(5, args.steps // 10)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(steps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+        out[name] = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12}
+    assert fa.get_device_error(dev) == fa.FA_OK
+    return out
 
 
 def main():

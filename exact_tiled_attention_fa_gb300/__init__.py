@@ -7,6 +7,7 @@ missing or cannot be loaded, every entry point raises.
 
 Entry points (same names as the C ABI, without the ``fa_`` prefix):
   fwd              exact attention forward (tiled, online softmax)
+  fwd_splitkv      the forward with the keys split and merged (few query tiles)
   bwd              exact attention backward (dQ, dK, dV; P recomputed from LSE)
   decode_splitkv   split-KV single-query decode with log-sum-exp combine
   decode_splitkv_gqa  the same with grouped key/value heads (query heads of a group packed)
@@ -59,6 +60,12 @@ def _load():
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, i, vp]
     lib.fa_decode_splitkv.restype = i
+    lib.fa_fwd_splitkv_default_splits.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_splitkv_default_splits.restype = i
+    lib.fa_fwd_splitkv_workspace_size.argtypes = [i, i, i, i, i]
+    lib.fa_fwd_splitkv_workspace_size.restype = sz
+    lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, i, f, i, i, vp]
+    lib.fa_fwd_splitkv.restype = i
     lib.fa_decode_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i, i, vp]
     lib.fa_decode_splitkv_gqa.restype = i
     lib.fa_merge_states.argtypes = [vp, vp, i, i, i, vp, vp, i, vp]
@@ -195,6 +202,46 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, out_dtype=torch.bfloat16,
     return dq, dk, dv_
 
 
+def fwd_splitkv_default_splits(B, H, N, Nk, num_sms):
+    return int(_load().fa_fwd_splitkv_default_splits(B, H, N, Nk, num_sms))
+
+
+def fwd_splitkv_workspace_size(B, H, N, dv, n_splits):
+    return int(_load().fa_fwd_splitkv_workspace_size(B, H, N, dv, n_splits))
+
+
+def fwd_splitkv(q, k, v, causal=False, scale=None, n_splits=0, out_dtype=torch.bfloat16, out=None, lse=None,
+                workspace=None, return_lse=True):
+    """Forward with the keys split into chunks and merged; same inputs and result as ``fwd``."""
+    lib = _load()
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    _need(k, "k", torch.bfloat16, dev)
+    _need(v, "v", torch.bfloat16, dev)
+    B, H, N, d = q.shape
+    Nk, dv = v.shape[2], v.shape[3]
+    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape[:2]) != (B, H):
+        raise ValueError("shape mismatch between q, k, v")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    n = int(n_splits) if n_splits else fwd_splitkv_default_splits(B, H, N, Nk, num_sms(dev))
+    if workspace is None:
+        workspace = torch.empty(max(fwd_splitkv_workspace_size(B, H, N, dv, max(1, min(n, Nk))), 256),
+                                dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    if out is None:
+        out = torch.empty((B, H, N, dv), dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib.fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+                                B, H, N, Nk, d, dv, int(bool(causal)), scale, n, _odt(out.dtype), _stream(dev))
+    _check(st, "fa_fwd_splitkv")
+    return out, lse
+
+
 def decode_default_splits(B, H, Nk_max, num_sms):
     return int(_load().fa_decode_default_splits(B, H, Nk_max, num_sms))
 
@@ -268,7 +315,11 @@ def decode_splitkv_gqa(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out
             or seqlens.numel() != B):
         raise ValueError("shape mismatch between q, caches and seqlens")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    n = int(n_splits) if n_splits else decode_default_splits(B, Hkv, Nk_max, num_sms(dev))
+    if n_splits:
+        n = int(n_splits)
+    else:  # the larger of the two automatic counts (CUDA-core and tensor-core groups)
+        sms = num_sms(dev)
+        n = max(decode_default_splits(B, Hkv, Nk_max, sms), min(-(-6 * sms // (B * Hkv)), -(-Nk_max // 128)))
     if workspace is None:
         workspace = torch.empty(max(decode_workspace_size(B, Hq, dv, max(1, min(n, Nk_max))), 256),
                                 dtype=torch.uint8, device=dev)
@@ -282,8 +333,8 @@ def decode_splitkv_gqa(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out
         _need(lse, "lse", torch.float32, dev)
     with torch.cuda.device(dev):
         st = lib.fa_decode_splitkv_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(out), _ptr(lse),
-                                       _ptr(workspace), workspace.numel(), B, Hq, Hkv, Nk_max, d, dv, scale, n,
-                                       _odt(out.dtype), _stream(dev))
+                                       _ptr(workspace), workspace.numel(), B, Hq, Hkv, Nk_max, d, dv, scale,
+                                       int(n_splits), _odt(out.dtype), _stream(dev))
     _check(st, "fa_decode_splitkv_gqa")
     return out, lse
 

@@ -288,7 +288,6 @@ cudaError_t launch_decode_d(const DecodeParams& p, fa_dtype o_dtype, cudaStream_
     case 1: fa_decode_split_kernel<D, 1><<<grid, kDecWarps * 32, 0, st>>>(p); break;
     case 2: fa_decode_split_kernel<D, 2><<<grid, kDecWarps * 32, 0, st>>>(p); break;
     case 4: fa_decode_split_kernel<D, 4><<<grid, kDecWarps * 32, 0, st>>>(p); break;
-    case 8: fa_decode_split_kernel<D, 8><<<grid, kDecWarps * 32, 0, st>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaGetLastError();

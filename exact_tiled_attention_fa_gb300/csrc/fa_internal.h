@@ -74,6 +74,25 @@ cudaError_t launch_bwd(const BwdParams& p, int d, bool causal, fa_dtype grad_dty
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, fa_dtype o_dtype, cudaStream_t st);
 cudaError_t launch_bwd_dq(const BwdDqParams& p, fa_dtype grad_dtype, cudaStream_t st);
 
+// Split-KV on the tensor core: one CTA per (key split, 128-row query tile, group).  A group is
+// a head (prefill: its N query rows) or a key/value head with its R packed query heads (decode).
+struct SplitParams {
+    CUtensorMap tm_q;   // bf16 [n_groups][rows_per_group][d], box {min(d,64), 128, 1}
+    CUtensorMap tm_k;   // bf16 [n_groups][Nk][d]
+    CUtensorMap tm_v;   // bf16 [n_groups][Nk][d]
+    float* o_part;      // [n_groups * rows_per_group][n_splits][d] fp32
+    float* lse_part;    // [n_groups * rows_per_group][n_splits] fp32
+    const int* seqlens; // decode: keys per sequence (group / groups_per_batch); nullptr: Nk for all
+    int* status;
+    int n_groups, rows_per_group, n_qtiles, groups_per_batch;
+    int Nk, n_splits, chunk;  // chunk: keys per split, a multiple of 128
+    int causal_off;           // Nk - N: query row i sits at position causal_off + i
+    float scale_log2;
+    unsigned long long wait_limit_ns;
+};
+
+cudaError_t launch_splitkv(const SplitParams& p, int d, bool causal, bool varlen, cudaStream_t st);
+
 // Decode: keys per block of the split kernel's inner loop; a split is a whole
 // number of such blocks.
 constexpr int kDecodeKeyBlock = 64;

@@ -1,0 +1,9 @@
+// Split-KV tensor-core kernel instances for head size 128.
+#include "fa_splitkv_kernel.cuh"
+
+namespace fa {
+cudaError_t launch_splitkv_128(const SplitParams& p, bool causal, bool varlen, cudaStream_t st)
+{
+    return launch_splitkv_d<128>(p, causal, varlen, st);
+}
+}  // namespace fa

@@ -17,6 +17,8 @@
  *   fa_decode_splitkv_gqa  the same with the query heads of a key/value group packed
  *                       together ("flash_lab.py", section 4: GQA packs a group's query heads
  *                       as the rows of q; `decode_attention_time` method "fd").
+ *   fa_fwd_splitkv      the forward with the keys split and merged, for few query tiles
+ *                       ("flash_lab.py", section 4 applied to a query tile).
  *   fa_merge_states     the log-sum-exp combine of partial states on its own
  *                       ("flash_lab.py", section 4 `split_kv_decode` combine, the
  *                       lse form of section 1 `merge_states`).
@@ -177,14 +179,50 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
  *   o          o_dtype [B, Hq, 1, dv]      (device, written)
  *   lse        fp32 [B, Hq, 1]             (device, written; may be NULL)
  *   workspace  ws_bytes >= fa_decode_workspace_size(B, Hq, dv, n) bytes, where n is n_splits or,
- *              for n_splits = 0, fa_decode_default_splits(B, Hkv, Nk_max, <SMs of the device>).
- *   Hkv >= 1 dividing Hq.  R = Hq / Hkv in {1, 2, 4, 8}; other group sizes return
- *   FA_ERR_UNSUPPORTED.  Hkv = Hq is fa_decode_splitkv.
+ *              for n_splits = 0, fa_decode_default_splits(B, Hkv, Nk_max, <SMs of the device>) for
+ *              groups of 1, 2 or 4 heads and min(ceil(6 * SMs / (B * Hkv)), ceil(Nk_max / 128)) for
+ *              other group sizes (fa_decode_workspace_size of the larger of the two always suffices).
+ *   Hkv >= 1 dividing Hq, R = Hq / Hkv <= 128 (larger groups return FA_ERR_UNSUPPORTED).
+ *   Hkv = Hq is fa_decode_splitkv.  Groups of 1, 2 or 4 heads run on CUDA cores; other group
+ *   sizes on the tensor core, where the R query rows are the rows of a 128-row tile, splits are
+ *   whole 128-key tiles (the chunk is rounded up to a multiple of 128 instead of the key block),
+ *   and cache rows past a sequence's length are never used, whatever they hold.
  */
 fa_status fa_decode_splitkv_gqa(const void* q, const void* k_cache, const void* v_cache,
                                 const int* seqlens_k, void* o, float* lse, void* workspace,
                                 size_t ws_bytes, int B, int Hq, int Hkv, int Nk_max, int d, int dv,
                                 float scale, int n_splits, fa_dtype o_dtype, void* stream);
+
+/*
+ * Split count fa_fwd_splitkv uses for n_splits = 0 on a device with `num_sms` multiprocessors:
+ * enough (head, query tile, split) work items for two per multiprocessor, each split at least
+ * one 128-key tile.  Pure host function; 0 on invalid arguments.
+ */
+int fa_fwd_splitkv_default_splits(int B, int H, int N, int Nk, int num_sms);
+
+/*
+ * Bytes of workspace fa_fwd_splitkv needs for n_splits splits: fp32 partial outputs
+ * [B, H, N, n_splits, dv] then fp32 partial log-sum-exps [B, H, N, n_splits], each region
+ * 256-byte aligned.  0 on invalid arguments.
+ */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int dv, int n_splits);
+
+/*
+ * Exact attention forward with the keys split ("flash_lab.py" section 4 `split_kv_decode`
+ * applied to a query tile; SURVEY's split-KV prefill): for workloads with few 128-row query
+ * tiles (B*H*ceil(N/128) below the number of multiprocessors) the keys are cut into n_splits
+ * chunks of whole 128-key tiles; each (head, query tile, chunk) computes its normalised output
+ * and log-sum-exp, and a second kernel merges them.  Same arguments, masks, result and output
+ * conventions as fa_fwd, plus:
+ *   workspace  ws_bytes >= fa_fwd_splitkv_workspace_size(B, H, N, dv, n) bytes, 256-byte aligned,
+ *              where n is n_splits or, for 0, fa_fwd_splitkv_default_splits(B, H, N, Nk, <SMs>);
+ *   n_splits   >= 0; values above Nk are reduced to it.
+ * B*H and ceil(N/128) must each be at most 65535.  Returns FA_ERR_WORKSPACE if ws_bytes is too
+ * small (nothing launched).
+ */
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         void* workspace, size_t ws_bytes, int B, int H, int N, int Nk, int d, int dv,
+                         int causal, float scale, int n_splits, fa_dtype o_dtype, void* stream);
 
 /*
  * Bytes of device scratch that fa_decode_splitkv_noalloc owns (8 MiB): room for the split

@@ -82,11 +82,27 @@ def test_gqa_decode_rejects_bad_arguments(lib):
         return f(P, P, P, P, P, P, ws, ws_bytes, B, Hq, Hkv, Nk, d, d, 0.1, n, 0, NULL)
     assert call(Hkv=0) == fa.FA_ERR_INVALID_ARG
     assert call(Hq=6, Hkv=4) == fa.FA_ERR_INVALID_ARG   # Hkv must divide Hq
-    assert call(Hq=6, Hkv=2) == fa.FA_ERR_UNSUPPORTED   # group size 3
-    assert call(Hq=32, Hkv=2) == fa.FA_ERR_UNSUPPORTED  # group size 16
+    assert call(Hq=512, Hkv=2) == fa.FA_ERR_UNSUPPORTED  # group of 256 heads exceeds a 128-row tile
     need = lib.fa_decode_workspace_size(2, 8, 128, 4)
     assert call(ws_bytes=need - 1) == fa.FA_ERR_WORKSPACE
     assert call(d=96) == fa.FA_ERR_UNSUPPORTED
+
+
+def test_fwd_splitkv_rejects_bad_arguments(lib):
+    f = lib.fa_fwd_splitkv
+    def call(q=P, ws=P, ws_bytes=1 << 24, B=1, H=2, N=100, Nk=1000, d=64, causal=0, n=4, scale=0.125):
+        return f(q, P, P, P, P, ws, ws_bytes, B, H, N, Nk, d, d, causal, scale, n, 0, NULL)
+    assert call(q=NULL) == fa.FA_ERR_INVALID_ARG
+    assert call(ws=NULL) == fa.FA_ERR_INVALID_ARG
+    assert call(n=-1) == fa.FA_ERR_INVALID_ARG
+    assert call(causal=3) == fa.FA_ERR_INVALID_ARG
+    assert call(d=80) == fa.FA_ERR_UNSUPPORTED
+    need = lib.fa_fwd_splitkv_workspace_size(1, 2, 100, 64, 4)
+    assert need == (2 * 100 * 4 * 64 * 4 + 255) // 256 * 256 + (2 * 100 * 4 * 4 + 255) // 256 * 256
+    assert call(ws_bytes=need - 1) == fa.FA_ERR_WORKSPACE
+    ds = lib.fa_fwd_splitkv_default_splits
+    assert ds(1, 1, 1, 100000, 152) >= 2 and ds(64, 16, 1024, 1024, 152) == 1
+    assert 1 <= ds(8, 8, 77, 513, 152) <= 5
 
 
 def test_merge_rejects_bad_arguments(lib):

@@ -129,7 +129,7 @@ def oracle_gqa_compact(q, k, v, lens, scale):
 
 
 @pytest.mark.parametrize("d", [32, 64, 128])
-@pytest.mark.parametrize("R", [1, 2, 4, 8])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 8, 16])
 @pytest.mark.parametrize("n_splits", [1, 5, 0])
 def test_gqa_decode(d, R, n_splits):
     B, Hkv, Nk_max = 3, 2, 700
@@ -172,8 +172,8 @@ def test_gqa_rejects_bad_groups():
     with pytest.raises(fa().FaError) as e:  # 6 query heads over 4 key/value heads
         fa().decode_splitkv_gqa(q, k, k, lens)
     assert e.value.status == fa().FA_ERR_INVALID_ARG
-    q3 = torch.zeros((1, 6, 1, 64), dtype=torch.bfloat16, device=DEV)
-    k3 = torch.zeros((1, 2, 128, 64), dtype=torch.bfloat16, device=DEV)
-    with pytest.raises(fa().FaError) as e:  # groups of 3 have no kernel
+    q3 = torch.zeros((1, 256, 1, 64), dtype=torch.bfloat16, device=DEV)
+    k3 = torch.zeros((1, 1, 128, 64), dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(fa().FaError) as e:  # a group of 256 heads does not fit a 128-row tile
         fa().decode_splitkv_gqa(q3, k3, k3, lens)
     assert e.value.status == fa().FA_ERR_UNSUPPORTED

@@ -163,3 +163,42 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, scale=0.125)
     o, lse = run(q, k, v, True, 0.125, torch.float32)
     assert_close(o, lse, o_ref, lse_ref, what="after a timed-out launch")
+
+
+# Split-KV forward: few query tiles, keys cut into chunks of whole 128-key tiles and merged.
+SPLIT = [
+    (8, 8, 77, 513, 32, 2.0),     # the pages' ragged demo shape, causal offset 436
+    (1, 2, 300, 1000, 64, 1.0),
+    (2, 1, 700, 333, 128, 1.0),   # N > Nk: causal rows with no visible key
+    (1, 1, 1, 2000, 64, 1.0),
+    (1, 3, 256, 4097, 128, 2.0),
+]
+
+
+@pytest.mark.parametrize("B,H,N,Nk,d,mult", SPLIT)
+@pytest.mark.parametrize("n_splits", [1, 3, 0])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_splitkv_full_oracle(B, H, N, Nk, d, mult, n_splits, causal):
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=2, mult=mult, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=causal, scale=scale)
+    for dt in (torch.float32, torch.bfloat16):
+        o, lse = fa().fwd_splitkv(q, k, v, causal=causal, scale=scale, n_splits=n_splits, out_dtype=dt)
+        torch.cuda.synchronize()
+        assert fa().get_device_error() == 0
+        assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16),
+                     what=f"splitkv {B,H,N,Nk,d} n={n_splits} causal={causal} {dt}")
+
+
+def test_fwd_splitkv_long_context_sampled():
+    """Few query tiles over a long context (B=1, H=8, N=512, Nk=32768, d=128, causal): the
+    benchmark's split-KV prefill workload; two heads' last 256 rows against the oracle."""
+    B, H, N, Nk, d = 1, 8, 512, 32768, 128
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=0, device=DEV)
+    o, lse = fa().fwd_splitkv(q, k, v, causal=True, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == 0
+    for h in sample_slices(H, 2, seed=1):
+        o_ref, l_ref = oracle.attention(q[0, h].cpu(), k[0, h].cpu(), v[0, h].cpu(), causal=True,
+                                        scale=1 / math.sqrt(d), rows=(N - 256, N))
+        assert_close(o[0, h, N - 256:], lse[0, h, N - 256:], o_ref, l_ref, what=f"long ctx h={h}")
