@@ -460,9 +460,44 @@ def run_decode(fa, dev, stream, args, world):
     other = B * H * (d * 2 + d * 2 + 4)
     pk, src = peaks()
     gbs = world * (kv_bytes + other) / (ms / 1e3) / 1e9
+    # the same decode with the combine fused into the split kernel (one launch per call)
+    wsf = fa.decode_fused_workspace(B, H, Nk_max, d, n_splits=n, device=dev)
+    fused = lambda: fa.decode_splitkv_fused(q, k, v, lens_d, wsf, n_splits=n, out=o, lse=lse)  # noqa: E731
+    ms_f = time_calls(fused, dev, stream, max(args.warmup, 3), steps, world)
+    # a short-context decode, where the second launch is a visible share of the call
+    qs, ks, vs, ls = decode_inputs(1, 32, 2048, d, d, seed=1, lo=2048, hi=2048, device=dev)
+    ls_d = ls.to(dev)
+    os_ = torch.empty((1, 32, 1, d), dtype=torch.bfloat16, device=dev)
+    ns = fa.decode_default_splits(1, 32, 2048, fa.num_sms(dev))
+    ws2 = torch.empty(fa.decode_workspace_size(1, 32, d, ns), dtype=torch.uint8, device=dev)
+    wsf2 = fa.decode_fused_workspace(1, 32, 2048, d, n_splits=ns, device=dev)
+    short = {"workload": f"B=1 H=32 Nk=2048 d={d}", "n_splits": ns,
+             "two_launches_us": 1e3 * time_calls(lambda: fa.decode_splitkv(qs, ks, vs, ls_d, n_splits=ns, out=os_,
+                                                                           workspace=ws2, return_lse=False),
+                                                 dev, stream, 5, 50, world),
+             "fused_us": 1e3 * time_calls(lambda: fa.decode_splitkv_fused(qs, ks, vs, ls_d, wsf2, n_splits=ns, out=os_,
+                                                                          return_lse=False),
+                                          dev, stream, 5, 50, world)}
+    assert fa.get_device_error(dev) == fa.FA_OK
     return {"workload": "split-KV decode B=16 H=32 d=128, lengths U[1024,32768] (seed 0), bf16 O",
             "n_splits": n, "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
-            "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2}
+            "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2,
+            "fused_combine": {"ms": ms_f, "gbs": world * (kv_bytes + other) / (ms_f / 1e3) / 1e9, "launches_per_call": 1},
+            "short_context": short}
+
+
+def time_calls(call, dev, stream, warmup, steps, world):
+    """Average milliseconds per call over `steps` calls, CUDA events on `stream`, max over ranks."""
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    return max_over_ranks(e0.elapsed_time(e1), world) / steps
 
 
 GQA = dict(B=16, Hq=32, Hkv=8, Nk_max=32768, d=128, lo=1024, hi=32768)

@@ -11,6 +11,7 @@ Entry points (same names as the C ABI, without the ``fa_`` prefix):
   bwd              exact attention backward (dQ, dK, dV; P recomputed from LSE)
   decode_splitkv   split-KV single-query decode with log-sum-exp combine
   decode_splitkv_gqa  the same with grouped key/value heads (query heads of a group packed)
+  decode_splitkv_fused  the same with the combine done by each row's last split (one launch)
   merge_states     log-sum-exp combine of partial states
   decode_default_splits, decode_workspace_size, get_device_error,
   set_wait_timeout_ns, status_string
@@ -66,6 +67,10 @@ def _load():
     lib.fa_fwd_splitkv_workspace_size.restype = sz
     lib.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, i, f, i, i, vp]
     lib.fa_fwd_splitkv.restype = i
+    lib.fa_decode_fused_workspace_size.argtypes = [i, i, i, i]
+    lib.fa_decode_fused_workspace_size.restype = sz
+    lib.fa_decode_splitkv_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, i, vp]
+    lib.fa_decode_splitkv_fused.restype = i
     lib.fa_decode_splitkv_gqa.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, i, f, i, i, vp]
     lib.fa_decode_splitkv_gqa.restype = i
     lib.fa_merge_states.argtypes = [vp, vp, i, i, i, vp, vp, i, vp]
@@ -336,6 +341,50 @@ def decode_splitkv_gqa(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out
                                        _ptr(workspace), workspace.numel(), B, Hq, Hkv, Nk_max, d, dv, scale,
                                        int(n_splits), _odt(out.dtype), _stream(dev))
     _check(st, "fa_decode_splitkv_gqa")
+    return out, lse
+
+
+def decode_fused_workspace_size(B, H, dv, n_splits):
+    return int(_load().fa_decode_fused_workspace_size(B, H, dv, n_splits))
+
+
+def decode_fused_workspace(B, H, Nk_max, dv, n_splits=0, device=None):
+    """A workspace for ``decode_splitkv_fused`` with its counters zeroed (reuse it across calls)."""
+    n = int(n_splits) if n_splits else decode_default_splits(B, H, Nk_max, num_sms(device))
+    return torch.zeros(decode_fused_workspace_size(B, H, dv, max(1, min(n, Nk_max))), dtype=torch.uint8,
+                       device=device or "cuda")
+
+
+def decode_splitkv_fused(q, k_cache, v_cache, seqlens, workspace, scale=None, n_splits=0, out_dtype=torch.bfloat16,
+                         out=None, lse=None, return_lse=True):
+    """Split-KV decode with the combine fused into the split kernel.  ``workspace`` comes from
+    ``decode_fused_workspace`` (its counters must be zero; each completed call leaves them zero)."""
+    lib = _load()
+    _need(q, "q", torch.bfloat16)
+    dev = q.device
+    _need(k_cache, "k_cache", torch.bfloat16, dev)
+    _need(v_cache, "v_cache", torch.bfloat16, dev)
+    _need(seqlens, "seqlens", torch.int32, dev)
+    _need(workspace, "workspace", torch.uint8, dev)
+    B, H, one, d = q.shape
+    if one != 1:
+        raise ValueError("decode takes a single query per (b, h)")
+    Nk_max, dv = v_cache.shape[2], v_cache.shape[3]
+    if tuple(k_cache.shape) != (B, H, Nk_max, d) or tuple(v_cache.shape[:2]) != (B, H) or seqlens.numel() != B:
+        raise ValueError("shape mismatch between q, caches and seqlens")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    if out is None:
+        out = torch.empty((B, H, 1, dv), dtype=out_dtype, device=dev)
+    _need(out, "out", out.dtype, dev)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", torch.float32, dev)
+    with torch.cuda.device(dev):
+        st = lib.fa_decode_splitkv_fused(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(out), _ptr(lse),
+                                         _ptr(workspace), workspace.numel(), B, H, Nk_max, d, dv, scale,
+                                         int(n_splits), _odt(out.dtype), _stream(dev))
+    _check(st, "fa_decode_splitkv_fused")
     return out, lse
 
 

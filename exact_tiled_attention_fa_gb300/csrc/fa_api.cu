@@ -349,7 +349,7 @@ int gqa_tc_default_splits(int B, int Hkv, int Nk_max, int sms)
 // Split-KV decode for Hq query heads over Hkv key/value heads (Hkv = Hq: multi-head).
 fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,
                       float* lse, void* workspace, size_t ws_bytes, int B, int Hq, int Hkv, int Nk_max, int d, int dv,
-                      float scale, int n_splits, fa_dtype o_dtype, void* stream)
+                      float scale, int n_splits, fa_dtype o_dtype, void* stream, bool fused = false)
 {
     if (q == nullptr || k_cache == nullptr || v_cache == nullptr || seqlens_k == nullptr || o == nullptr ||
         workspace == nullptr)
@@ -374,7 +374,10 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
         n = tc ? gqa_tc_default_splits(B, Hkv, Nk_max, sms) : fa_decode_default_splits(B, Hkv, Nk_max, sms);
     }
     if (n > Nk_max) n = Nk_max;
-    if (ws_bytes < fa_decode_workspace_size(B, Hq, dv, n)) return FA_ERR_WORKSPACE;
+    const size_t part_bytes = fa_decode_workspace_size(B, Hq, dv, n);
+    const size_t counter_bytes = fused ? round_up(static_cast<size_t>(B) * Hkv * sizeof(unsigned int), kAlign) : 0;
+    if (ws_bytes < part_bytes + counter_bytes) return FA_ERR_WORKSPACE;
+    if (fused && tc) return FA_ERR_UNSUPPORTED;
     if (tc) {
         // packed groups on the tensor core: splits are whole 128-key tiles
         long long chunk = (static_cast<long long>(Nk_max) + n - 1) / n;
@@ -434,6 +437,8 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
     p.n_splits = n_eff;
     p.chunk = static_cast<int>(chunk);
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.counters = fused ? reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) + part_bytes) : nullptr;
+    p.o_dtype = o_dtype;
     cudaError_t e = fa::launch_decode(p, d, o_dtype, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? FA_OK : FA_ERR_CUDA;
 }
@@ -523,6 +528,20 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
                    cudaSuccess
                ? FA_OK
                : FA_ERR_CUDA;
+}
+
+size_t fa_decode_fused_workspace_size(int B, int H, int dv, int n_splits)
+{
+    const size_t parts = fa_decode_workspace_size(B, H, dv, n_splits);
+    return parts == 0 ? 0 : parts + round_up(static_cast<size_t>(B) * H * sizeof(unsigned int), kAlign);
+}
+
+fa_status fa_decode_splitkv_fused(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k,
+                                  void* o, float* lse, void* workspace, size_t ws_bytes, int B, int H, int Nk_max,
+                                  int d, int dv, float scale, int n_splits, fa_dtype o_dtype, void* stream)
+{
+    return decode_impl(q, k_cache, v_cache, seqlens_k, o, lse, workspace, ws_bytes, B, H, H, Nk_max, d, dv, scale,
+                       n_splits, o_dtype, stream, true);
 }
 
 fa_status fa_decode_splitkv_gqa(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k,

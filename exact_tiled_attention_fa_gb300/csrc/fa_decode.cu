@@ -61,7 +61,16 @@ struct DecCfg {
 // KV head ("flash_lab.py" section 4: the query heads of a GQA group are packed as the rows
 // of q), so each K/V element is read once and used R times.  R = 1 is plain multi-head
 // attention.  Writes o_part / lse_part of a non-empty split for each of the R heads.
-template <int D, int R>
+// o[i] = v in the output dtype.
+__device__ __forceinline__ void store_row_value(const DecodeParams& p, size_t i, float v)
+{
+    if (p.o_dtype == FA_F32)
+        reinterpret_cast<float*>(p.o)[i] = v;
+    else
+        reinterpret_cast<__nv_bfloat16*>(p.o)[i] = __float2bfloat16_rn(v);
+}
+
+template <int D, int R, bool FUSED>
 __global__ void __launch_bounds__(kDecWarps * 32) fa_decode_split_kernel(const DecodeParams p)
 {
     using C = DecCfg<D, R>;
@@ -71,10 +80,20 @@ __global__ void __launch_bounds__(kDecWarps * 32) fa_decode_split_kernel(const D
     const int b = blockIdx.z;
     const int n = clamp_len(p.seqlens[b], p.Nk_max, p.status);
     const int k0 = s * p.chunk;
-    if (k0 >= n) return;  // empty split: nothing to write, the combine skips it
-    const int k1 = min(n, k0 + p.chunk);
     const size_t bkv = static_cast<size_t>(b) * p.Hkv + g;
     const size_t bq0 = static_cast<size_t>(b) * p.H + static_cast<size_t>(g) * R;  // first query head
+    if (k0 >= n) {  // empty split: nothing to write, the combine skips it
+        if (FUSED && n == 0 && s == 0) {
+            // no split has a key: with the combine fused, split 0 writes O = 0, LSE = -inf
+            for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
+                const int r = idx / D;
+                store_row_value(p, (bq0 + r) * D + (idx - r * D), 0.f);
+                if (idx - r * D == 0 && p.lse != nullptr) p.lse[bq0 + r] = -INFINITY;
+            }
+        }
+        return;
+    }
+    const int k1 = min(n, k0 + p.chunk);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -205,6 +224,37 @@ __global__ void __launch_bounds__(kDecWarps * 32) fa_decode_split_kernel(const D
         p.o_part[slot * D + c] = o / L;
         if (c == 0) p.lse_part[slot] = (M + log2f(L)) * kLn2;
     }
+    if constexpr (!FUSED) return;
+    // ---- fused combine: the last split CTA of this (b, key/value head) to finish merges the
+    // R rows ("flash_lab.py" section 4: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s).
+    __threadfence();  // this CTA's partials are visible device-wide before it is counted
+    __syncthreads();
+    __shared__ int is_last;
+    const int n_valid = min(p.n_splits, (n + p.chunk - 1) / p.chunk);
+    if (threadIdx.x == 0) {
+        const unsigned int prev = atomicAdd(&p.counters[bkv], 1u);
+        is_last = prev == static_cast<unsigned int>(n_valid - 1);
+    }
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
+        const int r = idx / D;
+        const int c = idx - r * D;
+        const size_t row = bq0 + r;
+        const float* lse_row = p.lse_part + row * p.n_splits;
+        float M = -INFINITY;
+        for (int t = 0; t < n_valid; ++t) M = fmaxf(M, __ldcg(lse_row + t));
+        float sum = 0.f;
+        for (int t = 0; t < n_valid; ++t) sum += ex2((__ldcg(lse_row + t) - M) * kLog2e);
+        const float L = M + log2f(sum) * kLn2;
+        float o = 0.f;
+        for (int t = 0; t < n_valid; ++t)
+            o = fmaf(ex2((__ldcg(lse_row + t) - L) * kLog2e), __ldcg(p.o_part + (row * p.n_splits + t) * D + c), o);
+        store_row_value(p, row * D + c, o);
+        if (c == 0 && p.lse != nullptr) p.lse[row] = L;
+    }
+    if (threadIdx.x == 0) p.counters[bkv] = 0u;  // ready for the next call
 }
 
 template <typename OutT>
@@ -285,13 +335,18 @@ cudaError_t launch_decode_d(const DecodeParams& p, fa_dtype o_dtype, cudaStream_
     dim3 grid(p.n_splits, p.Hkv, p.B);
     const int R = p.H / p.Hkv;
     switch (R) {
-    case 1: fa_decode_split_kernel<D, 1><<<grid, kDecWarps * 32, 0, st>>>(p); break;
-    case 2: fa_decode_split_kernel<D, 2><<<grid, kDecWarps * 32, 0, st>>>(p); break;
-    case 4: fa_decode_split_kernel<D, 4><<<grid, kDecWarps * 32, 0, st>>>(p); break;
+    case 1:
+        if (p.counters != nullptr)
+            fa_decode_split_kernel<D, 1, true><<<grid, kDecWarps * 32, 0, st>>>(p);
+        else
+            fa_decode_split_kernel<D, 1, false><<<grid, kDecWarps * 32, 0, st>>>(p);
+        break;
+    case 2: fa_decode_split_kernel<D, 2, false><<<grid, kDecWarps * 32, 0, st>>>(p); break;
+    case 4: fa_decode_split_kernel<D, 4, false><<<grid, kDecWarps * 32, 0, st>>>(p); break;
     default: return cudaErrorInvalidValue;
     }
     cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || p.counters != nullptr) return e;  // fused: no second launch
     MergeParams m{};
     m.o_parts = p.o_part;
     m.lse_parts = p.lse_part;

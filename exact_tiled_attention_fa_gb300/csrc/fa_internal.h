@@ -110,6 +110,10 @@ struct DecodeParams {
     int B, H, Nk_max, n_splits, chunk;
     int Hkv;              // key/value heads; query head h reads key/value head h / (H / Hkv)
     float scale_log2;
+    // Fused combine: non-null = per-(b, key/value head) arrival counters (zero on entry, left
+    // zero); the last split CTA of a (b, key/value head) merges its rows into o / lse.
+    unsigned int* counters;
+    fa_dtype o_dtype;
 };
 
 cudaError_t launch_decode(const DecodeParams& p, int d, fa_dtype o_dtype, cudaStream_t st);

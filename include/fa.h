@@ -19,6 +19,8 @@
  *                       as the rows of q; `decode_attention_time` method "fd").
  *   fa_fwd_splitkv      the forward with the keys split and merged, for few query tiles
  *                       ("flash_lab.py", section 4 applied to a query tile).
+ *   fa_decode_splitkv_fused  the decode with the combine done by the last split of each
+ *                       (b, h) instead of a second kernel.
  *   fa_merge_states     the log-sum-exp combine of partial states on its own
  *                       ("flash_lab.py", section 4 `split_kv_decode` combine, the
  *                       lse form of section 1 `merge_states`).
@@ -192,6 +194,29 @@ fa_status fa_decode_splitkv_gqa(const void* q, const void* k_cache, const void* 
                                 const int* seqlens_k, void* o, float* lse, void* workspace,
                                 size_t ws_bytes, int B, int Hq, int Hkv, int Nk_max, int d, int dv,
                                 float scale, int n_splits, fa_dtype o_dtype, void* stream);
+
+/*
+ * Bytes of workspace fa_decode_splitkv_fused needs: fa_decode_workspace_size(B, H, dv, n_splits)
+ * followed by B*H 32-bit arrival counters (256-byte aligned).  0 on invalid arguments.
+ */
+size_t fa_decode_fused_workspace_size(int B, int H, int dv, int n_splits);
+
+/*
+ * fa_decode_splitkv with the combine fused into the split kernel: every non-empty split of a
+ * (b, h) writes its o_s, lse_s and then counts itself on a per-(b, h) counter; the split that
+ * arrives last merges the row ("flash_lab.py" section 4 combine), so one kernel is launched
+ * instead of two (the launch gap is a decode cost the pages single out, section 5).  Same
+ * arguments, checks and result as fa_decode_splitkv, except:
+ *   workspace  ws_bytes >= fa_decode_fused_workspace_size(B, H, dv, n) bytes.  Its counter region
+ *              (the last B*H*4 bytes of that size) must be zero before the first call that uses
+ *              this workspace; every call that completes leaves it zero again.  After a call that
+ *              failed on the device (fa_get_device_error != FA_OK) zero it again.  Calls sharing a
+ *              workspace must not overlap on the GPU.
+ */
+fa_status fa_decode_splitkv_fused(const void* q, const void* k_cache, const void* v_cache,
+                                  const int* seqlens_k, void* o, float* lse, void* workspace,
+                                  size_t ws_bytes, int B, int H, int Nk_max, int d, int dv, float scale,
+                                  int n_splits, fa_dtype o_dtype, void* stream);
 
 /*
  * Split count fa_fwd_splitkv uses for n_splits = 0 on a device with `num_sms` multiprocessors:

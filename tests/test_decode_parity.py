@@ -177,3 +177,42 @@ def test_gqa_rejects_bad_groups():
     with pytest.raises(fa().FaError) as e:  # a group of 256 heads does not fit a 128-row tile
         fa().decode_splitkv_gqa(q3, k3, k3, lens)
     assert e.value.status == fa().FA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("n_splits", [1, 3, 16, 0])
+def test_fused_combine(d, n_splits):
+    """The combine done by each row's last split: oracle parity, counters left zero, and bit-equal
+    to itself on a second call with the same workspace."""
+    B, H, Nk_max = 5, 3, 1000
+    lens = torch.tensor([0, 1, 64, 65, 1000], dtype=torch.int32)
+    q, k, v, _ = decode_inputs(B, H, Nk_max, d, d, seed=d + 1, device=DEV, seqlens=lens)
+    scale = 1.0 / math.sqrt(d)
+    o_ref, lse_ref = oracle_decode_compact(q, k, v, lens, scale)
+    ws = fa().decode_fused_workspace(B, H, Nk_max, d, n_splits=n_splits, device=DEV)
+    parts = fa().decode_workspace_size(B, H, d, max(1, n_splits or fa().decode_default_splits(B, H, Nk_max, fa().num_sms())))
+    first = None
+    for dt in (torch.float32, torch.bfloat16, torch.float32):
+        o, lse = fa().decode_splitkv_fused(q, k, v, lens.to(DEV), ws, scale=scale, n_splits=n_splits, out_dtype=dt)
+        torch.cuda.synchronize()
+        assert fa().get_device_error() == 0
+        assert int(ws[parts:].count_nonzero()) == 0, "arrival counters not reset"
+        assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16), what=f"fused d={d} n={n_splits}")
+        if dt == torch.float32:
+            if first is None:
+                first = (o.clone(), lse.clone())
+            else:
+                assert torch.equal(o, first[0]) and torch.equal(lse, first[1])
+
+
+def test_fused_combine_full_size_matches_two_kernel_path():
+    B, H, Nk_max, d = 16, 32, 32768, 128
+    q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=0, lo=1024, hi=Nk_max, device=DEV)
+    ld = lens.to(DEV)
+    o2, l2 = fa().decode_splitkv(q, k, v, ld, out_dtype=torch.float32)
+    ws = fa().decode_fused_workspace(B, H, Nk_max, d, device=DEV)
+    o1, l1 = fa().decode_splitkv_fused(q, k, v, ld, ws, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == 0
+    # same splits, same partials, the same merge arithmetic in a different kernel
+    assert float((o1 - o2).abs().max()) <= 1e-6 and float((l1 - l2).abs().max()) <= 1e-6
