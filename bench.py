@@ -47,8 +47,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture, keyed by
 # the SHA-256 of the kernel source it was taken on; reported only while the source is unchanged.
 KERNEL_TRAFFIC = {
-    # profiles/fa_fwd_kernel_d64_gpt2medium_prefill.md: non-causal launch, 402.87 MB read + 108.18 MB written
-    "5edcc810dbab2d56202fac3f0222a8491a770d00cc9650288296e487cd453b08": 511.05e6,
+    # profiles/fa_fwd_kernel_d64_gpt2medium_prefill.md: non-causal launch, 402.84 MB read + 104.95 MB written
+    "59bcf3d43c35ed9ac6f20b48377ef2aa393edca9079ff2511d333577f406782b": 507.79e6,
 }
 
 
@@ -69,7 +69,7 @@ def peaks():
 def kernel_source_hash():
     import hashlib
     h = hashlib.sha256()
-    for name in ("fa_fwd_kernel.cuh", "ptx.cuh"):
+    for name in ("fa_fwd_kernel.cuh", "fa_kernel_common.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "exact_tiled_attention_fa_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -216,6 +216,11 @@ def run_ours(args, world, rank, local):
         pre = run_splitkv_prefill(fa, dev, stream, args, world)
         if rank == 0:
             print(json.dumps({"decode": decode, "decode_gqa": gqa, "splitkv_prefill": pre}), flush=True)
+        return 0
+    if args.splitkv_only:
+        pre = run_splitkv_prefill(fa, dev, stream, args, world)
+        if rank == 0:
+            print(json.dumps({"splitkv_prefill": pre}), flush=True)
         return 0
     if args.bwd_only:
         backward = run_bwd(fa, dev, stream, args, world)
@@ -587,6 +592,7 @@ def main():
     ap.add_argument("--cpu-slices", type=int, default=1024)
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
     ap.add_argument("--bwd-only", action="store_true", help="only the backward (profiling)")
+    ap.add_argument("--splitkv-only", action="store_true", help="only the split-KV prefill workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
