@@ -268,6 +268,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     p.Nk = Nk;
     p.Tr = static_cast<int>(Tr);
     p.Tc = static_cast<int>(Tc);
+    int sms = 0;
+    if (sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
+    p.num_ctas = sms;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.scale = scale;
     p.wait_limit_ns = g_wait_ns.load();

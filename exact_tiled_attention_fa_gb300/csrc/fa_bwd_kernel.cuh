@@ -12,7 +12,10 @@
 // The skipped tiles are those whose last query position lies before the key tile's
 // first key (query i sits at position Nk - N + i).
 //
-// GB300 mapping.  One CTA per (head, 128-key tile j).  It computes the transposed
+// GB300 mapping.  A persistent grid (one CTA per SM) walks work items (head, 128-key tile
+// j); an item's K_j, V_j load while the previous item runs (double-buffered for d <= 64)
+// and its dK_j, dV_j are written while the next item's first products run.  Per item, the CTA
+// computes the transposed
 // products S^T = K_j Q_i^T and dP^T = V_j dO_i^T, so that a TMEM lane is a key:
 // the rows of P^T and dS^T that a thread produces are exactly the A operand rows
 // the tensor core needs for dV_j += P^T dO_i and dK_j += dS^T Q_i, both issued with
@@ -75,14 +78,16 @@ constexpr int kBwdWarpDq = 12;  // warps 12-15
 // Register split after launch (setmaxnreg): the two compute warpgroups grow, the
 // control and dQ warpgroups shrink.  The launcher checks kBwdThreads * (registers at
 // launch) >= 256 * kBwdComputeRegs + 128 * (kBwdControlRegs + kBwdDqRegs).
-constexpr int kBwdComputeRegs = 192;
-constexpr int kBwdControlRegs = 56;
+constexpr int kBwdComputeRegs = 184;
+constexpr int kBwdControlRegs = 72;
 constexpr int kBwdDqRegs = 64;
 
 constexpr int kBwdMaxQStages = 3;
+constexpr int kBwdMaxKVBufs = 2;
 enum : int {
-    kBbKV = 0,        // K_j and V_j landed
-    kBbQFull = 1,     // +stage: Q_i, dO_i, L_i, D_i landed
+    kBbKVFull = 0,    // +buffer: K_j and V_j landed
+    kBbKVEmpty = kBbKVFull + kBwdMaxKVBufs,  // +buffer: both issuers are done with the item's K_j, V_j
+    kBbQFull = kBbKVEmpty + kBwdMaxKVBufs,   // +stage: Q_i, dO_i, L_i, D_i landed
     kBbQEmpty = kBbQFull + kBwdMaxQStages,   // +stage: both issuers' tensor-core work on it is done
     kBbSFull = kBbQEmpty + kBwdMaxQStages,   // S^T(t) in TMEM
     kBbDPFull,        // dP^T(t) in TMEM
@@ -90,7 +95,7 @@ enum : int {
     kBbDSReady,       // dS^T(t) written to TMEM and shared memory (256 arrivals)
     kBbDQFull,        // dQ(t) in TMEM
     kBbDQFree,        // dQ(t) read out of TMEM (128 arrivals)
-    kBbDone,          // every product of the walk has completed (one commit per issuer)
+    kBbDone,          // dV and dK of an item are complete (committed by their issuer alone)
     kBbDrain,         // +issuer (2)
     kBbDPFree = kBbDrain + 2,  // dP^T(t) loaded into registers (256 arrivals)
     kBbDVDone,        // dV(t) has read P^T(t)
@@ -114,9 +119,12 @@ struct BwdCfg {
     // two stages leave the S^T(t+2) issue waiting for the load; d = 128 has room for two only.
     static constexpr int kQStages = D == 128 ? 2 : 3;
     static_assert(kQStages <= kBwdMaxQStages, "barrier slots");
-    static constexpr int kOffK = 0;
-    static constexpr int kOffV = kTileBytes;
-    static constexpr int kOffQ = 2 * kTileBytes;                          // + stage * kTileBytes
+    // K_j / V_j buffers: two for d <= 64, so the next item's K and V load while this item runs
+    static constexpr int kKVBufs = D == 128 ? 1 : 2;
+    static_assert(kKVBufs <= kBwdMaxKVBufs, "barrier slots");
+    static constexpr int kOffK = 0;                                       // + buffer * kTileBytes
+    static constexpr int kOffV = kKVBufs * kTileBytes;                    // + buffer * kTileBytes
+    static constexpr int kOffQ = 2 * kKVBufs * kTileBytes;                // + stage * kTileBytes
     static constexpr int kOffDO = kOffQ + kQStages * kTileBytes;          // + stage * kTileBytes
     static constexpr int kOffDS = kOffDO + kQStages * kTileBytes;         // two query halves of kDSBlk
     static constexpr int kOffL = kOffDS + 2 * kDSBlk;                     // + stage * 512
@@ -165,21 +173,38 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     const int lane = threadIdx.x & 31;
     const unsigned long long limit = p.wait_limit_ns;
 
-    // work item: head bh, key tile j; query tiles [i_first, Tr)
-    const int bh = blockIdx.x / p.Tc;
-    const int j = blockIdx.x - bh * p.Tc;
+    // ---- work items: (head bh, key tile j), walked persistently.  CTA c takes items c, c + G,
+    // c + 2G, ... of the head-major order (the CTAs running at one time share a few heads, so
+    // those heads' Q and dO come from HBM once).  Under a causal mask the key tiles of a head
+    // are rotated by the head index, so that a CTA's items mix heavy and light walks.
+    const int n_items = p.BH * p.Tc;
     const int off = p.Nk - p.N;
-    const int j0 = j * kBlockN;
-    int i_first = 0;
-    if (CAUSAL) {
-        const int a = j0 - off - (kBlockM - 1);  // first tile whose last row position reaches j0
-        i_first = a <= 0 ? 0 : (a + kBlockM - 1) / kBlockM;
-    }
-    const int n = p.Tr > i_first ? p.Tr - i_first : 0;
+    struct Item {
+        int bh, j0, i_first, n;
+    };
+    auto item_at = [&](int x) -> Item {
+        Item it;
+        it.bh = x / p.Tc;
+        const int jr = x - it.bh * p.Tc;
+        const int j = CAUSAL ? (jr + it.bh) % p.Tc : jr;
+        it.j0 = j * kBlockN;
+        it.i_first = 0;
+        if (CAUSAL) {
+            const int a = it.j0 - off - (kBlockM - 1);  // first tile whose last row position reaches j0
+            it.i_first = a <= 0 ? 0 : (a + kBlockM - 1) / kBlockM;
+        }
+        it.n = p.Tr > it.i_first ? p.Tr - it.i_first : 0;
+        return it;
+    };
+    constexpr int QS = C::kQStages;
+    constexpr int KVB = C::kKVBufs;
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(kBbKV), 1);
-        for (int s = 0; s < C::kQStages; ++s) {
+        for (int i = 0; i < KVB; ++i) {
+            mbar_init(bar(kBbKVFull + i), 1);
+            mbar_init(bar(kBbKVEmpty + i), 2);  // one commit from each issuer
+        }
+        for (int s = 0; s < QS; ++s) {
             mbar_init(bar(kBbQFull + s), 1);
             mbar_init(bar(kBbQEmpty + s), 2);
         }
@@ -192,7 +217,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         mbar_init(bar(kBbDQFull), 1);
         mbar_init(bar(kBbDQFree), 128);
         mbar_init(bar(kBbDPFree), 256);
-        mbar_init(bar(kBbDone), 2);
+        // Only warp 10 (dV, dK) commits Done: with two K/V buffers warp 9 may finish the next
+        // item before warp 10 finishes this one, and a second arrival of its own would complete
+        // the phase early.
+        mbar_init(bar(kBbDone), 1);
         mbar_init(bar(kBbDVDone), 1);
         mbar_init(bar(kBbSFree), 256);
         mbar_init(bar(kBbDKDone), 1);
@@ -217,41 +245,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             prefetch_tensormap(&p.tm_v);
             prefetch_tensormap(&p.tm_do);
             const uint64_t pol_keep = policy_evict_last();  // Q_i, dO_i: read by every key tile of the head
-            const uint64_t pol_once = policy_evict_first(); // K_j, V_j: read by this CTA only
-            mbar_arrive_expect_tx(bar(kBbKV), 2 * C::kTileBytes);
-#pragma unroll
-            for (int cb = 0; cb < C::kNumCB; ++cb) {
-                tma_load_3d(sbase + C::kOffK + cb * C::kBlkBytes, &p.tm_k, bar(kBbKV), cb * C::kCB, j0, bh, pol_once);
-                tma_load_3d(sbase + C::kOffV + cb * C::kBlkBytes, &p.tm_v, bar(kBbKV), cb * C::kCB, j0, bh, pol_once);
-            }
-            int issued = 0;
+            const uint64_t pol_once = policy_evict_first(); // K_j, V_j: read by one CTA only
+            int g = 0;        // query tiles loaded (Q ring position)
+            int kv = 0;       // items whose K/V were loaded
             bool ok = true;
-            constexpr int QS = C::kQStages;
-            for (int t = 0; t < n; ++t) {
-                const int s = t % QS;
-                if (t >= QS && !mbar_wait(bar(kBbQEmpty + s), ((t / QS) - 1) & 1, limit, abort_flag)) {
+            for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+                const Item it = item_at(x);
+                if (it.n == 0) continue;  // no query tile sees this key tile (every role skips it)
+                const int kb = kv % KVB;
+                if (kv >= KVB && !mbar_wait(bar(kBbKVEmpty + kb), static_cast<uint32_t>(kv / KVB - 1) & 1, limit, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const int i0 = (i_first + t) * kBlockM;
-                mbar_arrive_expect_tx(bar(kBbQFull + s), 2 * C::kTileBytes + 2 * 512);
+                mbar_arrive_expect_tx(bar(kBbKVFull + kb), 2 * C::kTileBytes);
 #pragma unroll
                 for (int cb = 0; cb < C::kNumCB; ++cb) {
-                    tma_load_3d(sbase + C::kOffQ + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_q, bar(kBbQFull + s),
-                                cb * C::kCB, i0, bh, pol_keep);
-                    tma_load_3d(sbase + C::kOffDO + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_do,
-                                bar(kBbQFull + s), cb * C::kCB, i0, bh, pol_keep);
+                    tma_load_3d(sbase + C::kOffK + kb * C::kTileBytes + cb * C::kBlkBytes, &p.tm_k, bar(kBbKVFull + kb),
+                                cb * C::kCB, it.j0, it.bh, pol_once);
+                    tma_load_3d(sbase + C::kOffV + kb * C::kTileBytes + cb * C::kBlkBytes, &p.tm_v, bar(kBbKVFull + kb),
+                                cb * C::kCB, it.j0, it.bh, pol_once);
                 }
-                const size_t row = static_cast<size_t>(bh) * p.Tr * kBlockM + i0;
-                bulk_load(sbase + C::kOffL + s * 512, p.lse2 + row, 512, bar(kBbQFull + s));
-                bulk_load(sbase + C::kOffDsc + s * 512, p.dsc + row, 512, bar(kBbQFull + s));
-                ++issued;
+                ++kv;
+                for (int t = 0; t < it.n; ++t, ++g) {
+                    const int s = g % QS;
+                    if (g >= QS && !mbar_wait(bar(kBbQEmpty + s), static_cast<uint32_t>(g / QS - 1) & 1, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const int i0 = (it.i_first + t) * kBlockM;
+                    mbar_arrive_expect_tx(bar(kBbQFull + s), 2 * C::kTileBytes + 2 * 512);
+#pragma unroll
+                    for (int cb = 0; cb < C::kNumCB; ++cb) {
+                        tma_load_3d(sbase + C::kOffQ + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_q, bar(kBbQFull + s),
+                                    cb * C::kCB, i0, it.bh, pol_keep);
+                        tma_load_3d(sbase + C::kOffDO + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_do,
+                                    bar(kBbQFull + s), cb * C::kCB, i0, it.bh, pol_keep);
+                    }
+                    const size_t row = static_cast<size_t>(it.bh) * p.Tr * kBlockM + i0;
+                    bulk_load(sbase + C::kOffL + s * 512, p.lse2 + row, 512, bar(kBbQFull + s));
+                    bulk_load(sbase + C::kOffDsc + s * 512, p.dsc + row, 512, bar(kBbQFull + s));
+                }
             }
             if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
             // every issued copy lands before the CTA may exit
-            mbar_wait(bar(kBbKV), 0, kDrainLimitNs, nullptr);
-            for (int t = issued - QS < 0 ? 0 : issued - QS; t < issued; ++t)
-                mbar_wait(bar(kBbQFull + t % QS), (t / QS) & 1, kDrainLimitNs, nullptr);
+            for (int t = kv - KVB < 0 ? 0 : kv - KVB; t < kv; ++t)
+                mbar_wait(bar(kBbKVFull + t % KVB), static_cast<uint32_t>(t / KVB) & 1, kDrainLimitNs, nullptr);
+            for (int t = g - QS < 0 ? 0 : g - QS; t < g; ++t)
+                mbar_wait(bar(kBbQFull + t % QS), static_cast<uint32_t>(t / QS) & 1, kDrainLimitNs, nullptr);
         } else if ((warp == kBwdWarpMma || warp == kBwdWarpMma + 1) && lane == 0) {
             // ============================================================ MMA issuers
             // Barrier operations stall the issuing thread for a few hundred cycles, and the
@@ -264,7 +304,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                 ok = ok && mbar_wait(bar(b), static_cast<uint32_t>(parity) & 1, limit, abort_flag);
                 return ok;
             };
-            // S^T(t) = K_j Q_i^T or dP^T(t) = V_j dO_i^T: both operands K-major in shared memory.
+            // S^T = K_j Q_i^T or dP^T = V_j dO_i^T: both operands K-major in shared memory.
             auto issue_t = [&](uint32_t d_col, int a_off, int b_off) {
                 const uint64_t a0 = smem_desc(sbase + a_off, 16, C::kAtomBytes, C::kLayout);
                 const uint64_t b0 = smem_desc(sbase + b_off, 16, C::kAtomBytes, C::kLayout);
@@ -284,62 +324,66 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                     umma_ts(tmem + d_col, tmem + a_col + half_stride * (kk >> 2) + 8u * (kk & 3),
                             b0 + ((kk * 16 * C::kRowBytes) >> 4), C::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
             };
-            // dQ(t) = dS K_j: A = dS (MN-major, two 64-query blocks), B = K_j (MN-major).
-            auto issue_dq = [&]() {
+            // dQ = dS K_j: A = dS (MN-major, two 64-query blocks), B = K_j (MN-major).
+            auto issue_dq = [&](int k_off) {
                 const uint64_t a0 = smem_desc(sbase + C::kOffDS, C::kDSBlk, 1024, kSwizzle128B);
-                const uint64_t b0 = smem_desc(sbase + C::kOffK, C::kBlkBytes, C::kAtomBytes, C::kLayout);
+                const uint64_t b0 = smem_desc(sbase + k_off, C::kBlkBytes, C::kAtomBytes, C::kLayout);
 #pragma unroll
                 for (int kk = 0; kk < kBlockN / 16; ++kk)
                     umma_ss(tmem + C::kColDQ, a0 + ((kk * 16 * 128) >> 4), b0 + ((kk * 16 * C::kRowBytes) >> 4),
                             C::kIdescDQ, kk > 0 ? 1u : 0u);
             };
-            if (issuer_t) {
-                // S^T(t), dP^T(t) for every t; the stage of tile t is released (one of two
-                // arrivals) once dP^T(t) has been issued, its last read by this issuer.
-                if (n > 0 && wait(kBbKV, 0) && wait(kBbQFull, 0)) {
-                    tc_fence_after_sync();
-                    issue_t(C::kColS, C::kOffK, C::kOffQ);
-                    umma_commit(bar(kBbSFull));
-                    issue_t(C::kColDP, C::kOffV, C::kOffDO);
-                    umma_commit(bar(kBbDPFull));
-                    umma_commit(bar(kBbQEmpty));
+            int g = 0;  // query tiles processed (all items)
+            int k = 0;  // items processed
+            for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+                const Item it = item_at(x);
+                if (it.n == 0) continue;
+                const int kb = k % KVB;
+                const int k_off = C::kOffK + kb * C::kTileBytes;
+                const int v_off = C::kOffV + kb * C::kTileBytes;
+                if (!wait(kBbKVFull + kb, k / KVB)) break;
+                if (issuer_t) {
+                    // S^T and dP^T of every query tile; a Q stage is released (one of two arrivals)
+                    // once dP^T has been issued, this issuer's last read of it.
+                    for (int t = 0; t < it.n; ++t, ++g) {
+                        const int s = g % QS;
+                        // S^T(g) overwrites S^T(g-1), loaded by the compute warps (d <= 64), or
+                        // P^T(g-1) (d = 128), which dV(g-1) must have read
+                        if ((g > 0 && !wait(C::kDSOwn ? kBbSFree : kBbDVDone, g - 1)) || !wait(kBbQFull + s, g / QS)) break;
+                        tc_fence_after_sync();
+                        issue_t(C::kColS, k_off, C::kOffQ + s * C::kTileBytes);
+                        umma_commit(bar(kBbSFull));
+                        // dP^T(g) overwrites dP^T(g-1): loaded by the compute warps (d <= 64), or, with
+                        // dS^T and dQ in those columns (d = 128), dK and dQ done and dQ read out
+                        if (g > 0 && !wait(C::kDSOwn ? kBbDPFree : kBbDQFree, g - 1)) break;
+                        tc_fence_after_sync();
+                        issue_t(C::kColDP, v_off, C::kOffDO + s * C::kTileBytes);
+                        umma_commit(bar(kBbDPFull));
+                        umma_commit(bar(kBbQEmpty + s));
+                    }
+                } else {
+                    for (int t = 0; t < it.n; ++t, ++g) {
+                        const int s = g % QS;
+                        if (!wait(kBbPReady, g)) break;
+                        tc_fence_after_sync();
+                        issue_acc(C::kColDV, C::kColP, C::kPHalf, C::kOffDO + s * C::kTileBytes, t > 0);
+                        umma_commit(bar(kBbDVDone));
+                        if (!wait(kBbDSReady, g)) break;
+                        tc_fence_after_sync();
+                        issue_acc(C::kColDK, C::kColDS, C::kPHalf, C::kOffQ + s * C::kTileBytes, t > 0);
+                        umma_commit(bar(kBbQEmpty + s));
+                        if (C::kDSOwn) umma_commit(bar(kBbDKDone));
+                        if (!C::kDQAlias && g > 0 && !wait(kBbDQFree, g - 1)) break;
+                        tc_fence_after_sync();
+                        issue_dq(k_off);
+                        umma_commit(bar(kBbDQFull));
+                    }
                 }
-                for (int t = 0; ok && t + 1 < n; ++t) {
-                    const int s1 = (t + 1) % C::kQStages;
-                    // S^T(t+1) overwrites S^T(t), loaded by the compute warps (d <= 64), or P^T(t)
-                    // (d = 128), which dV(t) must have read
-                    if (!wait(C::kDSOwn ? kBbSFree : kBbDVDone, t) || !wait(kBbQFull + s1, (t + 1) / C::kQStages)) break;
-                    tc_fence_after_sync();
-                    issue_t(C::kColS, C::kOffK, C::kOffQ + s1 * C::kTileBytes);
-                    umma_commit(bar(kBbSFull));
-                    // dP^T(t+1) overwrites dP^T(t): loaded by the compute warps (d <= 64), or, with
-                    // dS^T and dQ in those columns (d = 128), dK(t) and dQ(t) done and dQ(t) read out
-                    if (!wait(C::kDSOwn ? kBbDPFree : kBbDQFree, t)) break;
-                    tc_fence_after_sync();
-                    issue_t(C::kColDP, C::kOffV, C::kOffDO + s1 * C::kTileBytes);
-                    umma_commit(bar(kBbDPFull));
-                    umma_commit(bar(kBbQEmpty + s1));
-                }
-            } else {
-                if (n > 0) wait(kBbKV, 0);
-                for (int t = 0; ok && t < n; ++t) {
-                    const int s = t % C::kQStages;
-                    if (!wait(kBbPReady, t)) break;
-                    tc_fence_after_sync();
-                    issue_acc(C::kColDV, C::kColP, C::kPHalf, C::kOffDO + s * C::kTileBytes, t > 0);
-                    umma_commit(bar(kBbDVDone));
-                    if (!wait(kBbDSReady, t)) break;
-                    tc_fence_after_sync();
-                    issue_acc(C::kColDK, C::kColDS, C::kPHalf, C::kOffQ + s * C::kTileBytes, t > 0);
-                    umma_commit(bar(kBbQEmpty + s));
-                    if (C::kDSOwn) umma_commit(bar(kBbDKDone));
-                    if (!C::kDQAlias && t > 0 && !wait(kBbDQFree, t - 1)) break;
-                    tc_fence_after_sync();
-                    issue_dq();
-                    umma_commit(bar(kBbDQFull));
-                }
+                if (!ok) break;
+                umma_commit(bar(kBbKVEmpty + kb));  // this issuer's reads of K_j, V_j are done
+                if (!issuer_t) umma_commit(bar(kBbDone));
+                ++k;
             }
-            umma_commit(bar(kBbDone));
             if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
             const int me = issuer_t ? 0 : 1;
             umma_commit(bar(kBbDrain + me));
@@ -351,24 +395,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         const int r = threadIdx.x & 127;  // query row of the tile == TMEM lane
         const uint32_t t_dq = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kColDQ;
         bool ok = true;
-        for (int t = 0; t < n; ++t) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDQFull), t & 1, limit, abort_flag));
-            if (!ok) break;
-            tc_fence_after_sync();
-            float* acc = p.dq_acc + (static_cast<size_t>(bh) * p.Tr + (i_first + t)) * (D / 4) * (kBlockM * 4) + r * 4;
+        int g = 0;
+        for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+            const Item it = item_at(x);
+            for (int t = 0; t < it.n; ++t, ++g) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDQFull), g & 1, limit, abort_flag));
+                if (!ok) break;
+                tc_fence_after_sync();
+                float* acc = p.dq_acc + (static_cast<size_t>(it.bh) * p.Tr + (it.i_first + t)) * (D / 4) * (kBlockM * 4) +
+                             r * 4;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(t_dq + 32u * c, v);
-                tmem_ld_wait();
-                if (c == D / 32 - 1) {  // the whole dQ(t) row is in registers: release the columns
-                    tc_fence_before_sync();
-                    mbar_arrive(bar(kBbDQFree));
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_ld32(t_dq + 32u * c, v);
+                    tmem_ld_wait();
+                    if (c == D / 32 - 1) {  // the whole dQ row is in registers: release the columns
+                        tc_fence_before_sync();
+                        mbar_arrive(bar(kBbDQFree));
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4)
+                        red_add_v4(acc + static_cast<size_t>(c * 8 + e / 4) * (kBlockM * 4), __uint_as_float(v[e]),
+                                   __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
                 }
-#pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    red_add_v4(acc + static_cast<size_t>(c * 8 + e / 4) * (kBlockM * 4), __uint_as_float(v[e]),
-                               __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
             }
         }
         if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
@@ -376,134 +425,152 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         regs_increase<kBwdComputeRegs>();
         // ============================================================ compute
         const int h = warp >> 2;                 // query half of the tile
-        const int k = threadIdx.x & 127;         // key row of the tile == TMEM lane
+        const int kr = threadIdx.x & 127;        // key row of the tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t t_s = tmem + lane_base + C::kColS + 64u * h;
         const uint32_t t_dp = tmem + lane_base + C::kColDP + 64u * h;
         const uint32_t t_ds = tmem + lane_base + C::kColDS + C::kPHalf * h;
         const uint32_t t_p = tmem + lane_base + C::kColP + C::kPHalf * h;
-        const uint32_t ds_row = sbase + C::kOffDS + h * C::kDSBlk + k * 128;  // this thread's dS^T row
+        const uint32_t ds_row = sbase + C::kOffDS + h * C::kDSBlk + kr * 128;  // this thread's dS^T row
         const float2 sl2 = make_float2(p.scale_log2, p.scale_log2);
         const float2 sc2 = make_float2(p.scale, p.scale);
         bool ok = true;
-        for (int t = 0; t < n; ++t) {
-            const int s = t % C::kQStages;
-            const int i0 = (i_first + t) * kBlockM;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbSFull), t & 1, limit, abort_flag));
-            if (!ok) break;
-            tc_fence_after_sync();
-            uint32_t u[64];
-            tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-            tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-            tmem_ld_wait();
-            if constexpr (C::kDSOwn) {  // the S^T columns may now be overwritten by S^T(t+1)
-                tc_fence_before_sync();
-                mbar_arrive(bar(kBbSFree));
-            }
-            // P = exp2(S scale log2(e) - L log2(e)); L = +inf gives 0 (row past N or with no key)
-            const uint32_t l_addr = sbase + C::kOffL + s * 512 + h * 256;
-            float pf[64];
-            uint32_t pk[32];
+        int g = 0;
+        int k = 0;
+        for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
+            const Item it = item_at(x);
+            const int key = it.j0 + kr;
+            const bool valid = key < p.Nk;
+            const size_t row = (static_cast<size_t>(it.bh) * p.Nk + (valid ? key : 0)) * D + h * (D / 2);
+            GradT* dk = reinterpret_cast<GradT*>(p.dk) + row;
+            GradT* dv = reinterpret_cast<GradT*>(p.dv) + row;
+            if (it.n == 0) {  // no query sees these keys: zero gradients, no tensor-core work
+                float z[16];
 #pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                const float4 l4 = ld_shared_f4(l_addr + c * 4);
-                const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2,
-                                              make_float2(-l4.x, -l4.y));
-                const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sl2,
-                                              make_float2(-l4.z, -l4.w));
-                pf[c] = ex2(x01.x);
-                pf[c + 1] = ex2(x01.y);
-                pf[c + 2] = ex2(x23.x);
-                pf[c + 3] = ex2(x23.y);
+                for (int e = 0; e < 16; ++e) z[e] = 0.f;
+                if (valid)
+                    for (int c = 0; c < D / 2; c += 16) {
+                        store_row16<GradT>(dv + c, z);
+                        store_row16<GradT>(dk + c, z);
+                    }
+                continue;
             }
-            if (CAUSAL && off + i0 < j0 + kBlockN - 1) {
-                // key j0 + k is hidden from query i0 + q when j0 + k > off + i0 + q
-                const int thr = j0 + k - off - i0 - 64 * h;  // my columns c < thr are masked
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                    if (c < thr) pf[c] = 0.f;
-            }
-#pragma unroll
-            for (int c = 0; c < 64; c += 2) pk[c / 2] = pack_bf16x2(pf[c], pf[c + 1]);
-            if (C::kDSOwn && t > 0) {  // dK(t-1) must have read dS^T(t-1) from the shared columns
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDKDone), (t - 1) & 1, limit, abort_flag));
+            for (int t = 0; t < it.n; ++t, ++g) {
+                const int s = g % QS;
+                const int i0 = (it.i_first + t) * kBlockM;
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbSFull), g & 1, limit, abort_flag));
                 if (!ok) break;
                 tc_fence_after_sync();
-            }
-            tmem_st32(t_p, pk);
-            tmem_st_wait();
-            tc_fence_before_sync();
-            mbar_arrive(bar(kBbPReady));
+                uint32_t u[64];
+                tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+                tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+                tmem_ld_wait();
+                if constexpr (C::kDSOwn) {  // the S^T columns may now be overwritten by the next S^T
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(kBbSFree));
+                }
+                // P = exp2(S scale log2(e) - L log2(e)); L = +inf gives 0 (row past N or with no key)
+                const uint32_t l_addr = sbase + C::kOffL + s * 512 + h * 256;
+                float pf[64];
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 l4 = ld_shared_f4(l_addr + c * 4);
+                    const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2,
+                                                  make_float2(-l4.x, -l4.y));
+                    const float2 x23 = __ffma2_rn(make_float2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sl2,
+                                                  make_float2(-l4.z, -l4.w));
+                    pf[c] = ex2(x01.x);
+                    pf[c + 1] = ex2(x01.y);
+                    pf[c + 2] = ex2(x23.x);
+                    pf[c + 3] = ex2(x23.y);
+                }
+                if (CAUSAL && off + i0 < it.j0 + kBlockN - 1) {
+                    // key j0 + kr is hidden from query i0 + q when j0 + kr > off + i0 + q
+                    const int thr = it.j0 + kr - off - i0 - 64 * h;  // my columns c < thr are masked
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        if (c < thr) pf[c] = 0.f;
+                }
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) pk[c / 2] = pack_bf16x2(pf[c], pf[c + 1]);
+                if (C::kDSOwn && g > 0) {  // dK must have read the previous dS^T from the shared columns
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDKDone), (g - 1) & 1, limit, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                }
+                tmem_st32(t_p, pk);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(bar(kBbPReady));
 
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDPFull), t & 1, limit, abort_flag));
-            if (!ok) break;
-            tc_fence_after_sync();
-            tmem_ld32(t_dp, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
-            tmem_ld32(t_dp + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
-            tmem_ld_wait();
-            if constexpr (C::kDSOwn) {  // the dP^T columns may now be overwritten by dP(t+1)
-                tc_fence_before_sync();
-                mbar_arrive(bar(kBbDPFree));
-            }
-            // dS' = scale dS = P o (dP scale - scale D)
-            const uint32_t d_addr = sbase + C::kOffDsc + s * 512 + h * 256;
-#pragma unroll
-            for (int c = 0; c < 64; c += 4) {
-                const float4 d4 = ld_shared_f4(d_addr + c * 4);
-                const float2 y01 = __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sc2,
-                                              make_float2(-d4.x, -d4.y));
-                const float2 y23 = __ffma2_rn(make_float2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sc2,
-                                              make_float2(-d4.z, -d4.w));
-                const float2 g01 = __fmul2_rn(y01, make_float2(pf[c], pf[c + 1]));
-                const float2 g23 = __fmul2_rn(y23, make_float2(pf[c + 2], pf[c + 3]));
-                pk[c / 2] = pack_bf16x2(g01.x, g01.y);
-                pk[c / 2 + 1] = pack_bf16x2(g23.x, g23.y);
-            }
-            if constexpr (C::kDSOwn) {
-                // dV(t) must have read P^T(t) from the shared columns, and dQ(t-1) dS(t-1) from
-                // shared memory
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDVDone), t & 1, limit, abort_flag) &&
-                                                 (t == 0 || mbar_wait(bar(kBbDQFull), (t - 1) & 1, limit, abort_flag)));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDPFull), g & 1, limit, abort_flag));
                 if (!ok) break;
                 tc_fence_after_sync();
+                tmem_ld32(t_dp, *reinterpret_cast<uint32_t(*)[32]>(&u[0]));
+                tmem_ld32(t_dp + 32, *reinterpret_cast<uint32_t(*)[32]>(&u[32]));
+                tmem_ld_wait();
+                if constexpr (C::kDSOwn) {  // the dP^T columns may now be overwritten by the next dP^T
+                    tc_fence_before_sync();
+                    mbar_arrive(bar(kBbDPFree));
+                }
+                // dS' = scale dS = P o (dP scale - scale D)
+                const uint32_t d_addr = sbase + C::kOffDsc + s * 512 + h * 256;
+#pragma unroll
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 d4 = ld_shared_f4(d_addr + c * 4);
+                    const float2 y01 = __ffma2_rn(make_float2(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sc2,
+                                                  make_float2(-d4.x, -d4.y));
+                    const float2 y23 = __ffma2_rn(make_float2(__uint_as_float(u[c + 2]), __uint_as_float(u[c + 3])), sc2,
+                                                  make_float2(-d4.z, -d4.w));
+                    const float2 g01 = __fmul2_rn(y01, make_float2(pf[c], pf[c + 1]));
+                    const float2 g23 = __fmul2_rn(y23, make_float2(pf[c + 2], pf[c + 3]));
+                    pk[c / 2] = pack_bf16x2(g01.x, g01.y);
+                    pk[c / 2 + 1] = pack_bf16x2(g23.x, g23.y);
+                }
+                if constexpr (C::kDSOwn) {
+                    // dV must have read P^T from the shared columns, and the previous dQ the previous
+                    // dS from shared memory
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDVDone), g & 1, limit, abort_flag) &&
+                                                     (g == 0 || mbar_wait(bar(kBbDQFull), (g - 1) & 1, limit, abort_flag)));
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                }
+                tmem_st32(t_ds, pk);
+                // dS^T row kr into the MN-major dS operand: 16-byte chunk q8 of the 128-byte row goes
+                // to chunk q8 ^ (kr mod 8) (128-byte swizzle).
+#pragma unroll
+                for (int q8 = 0; q8 < 8; ++q8)
+                    st_shared_v4(ds_row + ((q8 ^ (kr & 7)) << 4), pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2],
+                                 pk[4 * q8 + 3]);
+                fence_proxy_async_shared();
+                tmem_st_wait();
+                tc_fence_before_sync();
+                mbar_arrive(bar(kBbDSReady));
             }
-            tmem_st32(t_ds, pk);
-            // dS^T row k into the MN-major dS operand: 16-byte chunk q8 of the 128-byte row goes
-            // to chunk q8 ^ (k mod 8) (128-byte swizzle).
+            if (!ok) break;
+            // dK_j and dV_j of this item: this thread writes key row j0 + kr, columns of its half.
+            // The next item's first dV and dK (which overwrite these columns) are issued only after
+            // this warpgroup's next P^T arrival, i.e. after these loads.
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDone), k & 1, limit, abort_flag));
+            if (!ok) break;
+            ++k;
+            tc_fence_after_sync();
 #pragma unroll
-            for (int q8 = 0; q8 < 8; ++q8)
-                st_shared_v4(ds_row + ((q8 ^ (k & 7)) << 4), pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2], pk[4 * q8 + 3]);
-            fence_proxy_async_shared();
-            tmem_st_wait();
-            tc_fence_before_sync();
-            mbar_arrive(bar(kBbDSReady));
-        }
-        // dK_j and dV_j: this thread writes key row j0 + k, columns of its half
-        if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDone), 0, limit, abort_flag));
-            if (ok) {
-                tc_fence_after_sync();
-                const int key = j0 + k;
-                const bool valid = key < p.Nk;
-                const size_t row = (static_cast<size_t>(bh) * p.Nk + (valid ? key : 0)) * D + h * (D / 2);
-                GradT* dk = reinterpret_cast<GradT*>(p.dk) + row;
-                GradT* dv = reinterpret_cast<GradT*>(p.dv) + row;
+            for (int c = 0; c < D / 2; c += 16) {
+                uint32_t a[16], b[16];
+                tmem_ld16(tmem + lane_base + C::kColDV + h * (D / 2) + c, a);
+                tmem_ld16(tmem + lane_base + C::kColDK + h * (D / 2) + c, b);
+                tmem_ld_wait();
+                float fa[16], fb[16];
 #pragma unroll
-                for (int c = 0; c < D / 2; c += 16) {
-                    uint32_t a[16], b[16];
-                    tmem_ld16(tmem + lane_base + C::kColDV + h * (D / 2) + c, a);
-                    tmem_ld16(tmem + lane_base + C::kColDK + h * (D / 2) + c, b);
-                    tmem_ld_wait();
-                    float fa[16], fb[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        fa[e] = n > 0 ? __uint_as_float(a[e]) : 0.f;
-                        fb[e] = n > 0 ? __uint_as_float(b[e]) : 0.f;
-                    }
-                    if (valid) {
-                        store_row16<GradT>(dv + c, fa);
-                        store_row16<GradT>(dk + c, fb);
-                    }
+                for (int e = 0; e < 16; ++e) {
+                    fa[e] = __uint_as_float(a[e]);
+                    fb[e] = __uint_as_float(b[e]);
+                }
+                if (valid) {
+                    store_row16<GradT>(dv + c, fa);
+                    store_row16<GradT>(dk + c, fb);
                 }
             }
         }
@@ -541,8 +608,9 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st)
     }
     if (regs[dev] * kBwdThreads < 256 * kBwdComputeRegs + 128 * (kBwdControlRegs + kBwdDqRegs))
         return cudaErrorLaunchOutOfResources;  // the register split would not fit
-    const long long grid = static_cast<long long>(p.BH) * p.Tc;
-    if (grid <= 0) return cudaSuccess;
+    const long long items = static_cast<long long>(p.BH) * p.Tc;
+    if (items <= 0) return cudaSuccess;
+    const long long grid = items < p.num_ctas ? items : p.num_ctas;  // persistent: one CTA per SM
     kern<<<static_cast<unsigned>(grid), kBwdThreads, C::kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }

@@ -48,6 +48,7 @@ struct BwdParams {
     void* dv;           // [B*H][Nk][d]
     int* status;
     int BH, N, Nk, Tr, Tc;
+    int num_ctas;       // persistent CTAs (one per SM)
     float scale_log2;   // scale * log2(e)
     float scale;
     unsigned long long wait_limit_ns;

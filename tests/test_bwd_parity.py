@@ -138,6 +138,23 @@ def test_full_size_sampled_heads(causal):
     check(sel[4:], ref, mags, bf16_out=True, what=f"C2 causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_persistent_items_per_cta(d, causal):
+    """More (head, key tile) items than SMs, so each CTA walks several, short causal walks right
+    after long ones; every head against the oracle."""
+    B, H, N = 2, 16, 1024
+    q, k, v = attention_inputs(B, H, N, N, d, d, seed=8, device=DEV)
+    do = grad_output(B, H, N, d, seed=8, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    got = gpu_grads(q, k, v, do, causal, scale)
+    heads = range(0, B * H, 3)
+    flat = [t.reshape(B * H, *t.shape[2:]) for t in (q, k, v, do) + tuple(got)]
+    sel = [t[list(heads)].cpu() for t in flat]
+    ref = oracle.attention_bwd(sel[0], sel[1], sel[2], sel[3], causal=causal, scale=scale)
+    check(sel[4:], ref, magnitudes(sel[0], sel[1], sel[2], sel[3], causal, scale), what=f"items d={d} causal={causal}")
+
+
 def test_rejects_small_workspace_and_bad_args():
     B, H, N, d = 1, 1, 128, 64
     q, k, v = attention_inputs(B, H, N, N, d, d, seed=0, device=DEV)
