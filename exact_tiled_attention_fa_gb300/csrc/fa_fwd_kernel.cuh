@@ -64,8 +64,12 @@ constexpr int kWarpMma = 9;       // warps 9 and 10 issue the MMAs of Q0 and Q1;
 // two softmax warpgroups.  The split needs kFwdThreads * (registers at launch) >=
 // 256 * kSoftmaxRegs + 128 * kControlRegs; the launcher checks this before every launch,
 // because an increase that the pool cannot satisfy would wait forever.
-constexpr int kSoftmaxRegs = 224;
-constexpr int kControlRegs = 56;
+// d = 128 keeps the softmax at 224 (its long causal prefill measured 1.6 % faster than with 216);
+// for d <= 64 the control warps get 72 (the d = 64 prefill measured 1.6 % faster than with 56).
+template <int D>
+constexpr int kSoftmaxRegs = D == 128 ? 224 : 216;
+template <int D>
+constexpr int kControlRegs = D == 128 ? 56 : 72;
 
 // barrier slots
 constexpr int kMaxStages = 8;
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
 
     if (warp >= kWarpProducer) {
-      regs_decrease<kControlRegs>();
+      regs_decrease<kControlRegs<D>>();
       if (warp == kWarpProducer) {
         // ============================================================ producer
         if (lane == 0) {
@@ -401,7 +405,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         }
       }
     } else {
-        regs_increase<kSoftmaxRegs>();
+        regs_increase<kSoftmaxRegs<D>>();
         // ============================================================ softmax + epilogue
         const int wg = warp >> 2;               // query tile of this warpgroup
         const int r = threadIdx.x & 127;        // row within the tile == TMEM lane
@@ -583,7 +587,7 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
         regs[dev] = attr.numRegs;
     }
     const int launch_regs = (dev >= 0 && dev < 64) ? regs[dev] : 0;
-    if (launch_regs * kFwdThreads < 256 * kSoftmaxRegs + 128 * kControlRegs)
+    if (launch_regs * kFwdThreads < 256 * kSoftmaxRegs<D> + 128 * kControlRegs<D>)
         return cudaErrorLaunchOutOfResources;  // the register split would not fit
     const int pairs = (p.n_items + 1) / 2;
     const int grid = pairs < p.num_ctas ? pairs : p.num_ctas;
