@@ -168,3 +168,26 @@ def test_rejects_small_workspace_and_bad_args():
     with pytest.raises(fa().FaError) as e:
         fa().bwd(q48, q48, q48, q48.float(), torch.zeros((1, 1, 8), device=DEV), q48)
     assert e.value.status == fa().FA_ERR_UNSUPPORTED
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """A 1 ns wait limit makes the backward's first barrier waits run out: the kernel records
+    FA_ERR_TIMEOUT, drains its copies and MMAs and returns; the next call is correct."""
+    B, H, N, d = 2, 8, 1024, 64
+    q, k, v = attention_inputs(B, H, N, N, d, d, seed=9, device=DEV)
+    do = grad_output(B, H, N, d, seed=9, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = fa().fwd(q, k, v, causal=True, scale=scale, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    fa().set_wait_timeout_ns(1)
+    try:
+        fa().bwd(q, k, v, o, lse, do, causal=True, scale=scale, out_dtype=torch.float32)
+        status = fa().get_device_error()
+    finally:
+        fa().set_wait_timeout_ns(0)
+    assert status == fa().FA_ERR_TIMEOUT
+    q2, k2, v2, do2 = (t[:, :2].contiguous() for t in (q, k, v, do))
+    got = gpu_grads(q2, k2, v2, do2, True, scale)
+    sel = [t.reshape(B * 2, N, d).cpu() for t in (q2, k2, v2, do2)]
+    ref = oracle.attention_bwd(*sel, causal=True, scale=scale)
+    check([g.reshape(B * 2, N, d) for g in got], ref, magnitudes(*sel, True, scale), what="after a timed-out launch")

@@ -202,3 +202,25 @@ def test_fwd_splitkv_long_context_sampled():
         o_ref, l_ref = oracle.attention(q[0, h].cpu(), k[0, h].cpu(), v[0, h].cpu(), causal=True,
                                         scale=1 / math.sqrt(d), rows=(N - 256, N))
         assert_close(o[0, h, N - 256:], lse[0, h, N - 256:], o_ref, l_ref, what=f"long ctx h={h}")
+
+
+def test_splitkv_bounded_wait_reports_timeout_and_context_survives():
+    """The split-KV kernel under a 1 ns wait limit (prefill and packed-group decode) records
+    FA_ERR_TIMEOUT and returns; the next calls are correct."""
+    from fa_inputs import gqa_decode_inputs
+    q, k, v = attention_inputs(1, 4, 256, 4096, 128, 128, seed=10, device=DEV)
+    qd, kc, vc, lens = gqa_decode_inputs(2, 16, 2, 2048, 128, 128, seed=10, lo=100, hi=2048, device=DEV)
+    fa().set_wait_timeout_ns(1)
+    try:
+        fa().fwd_splitkv(q, k, v, causal=True, n_splits=4, out_dtype=torch.float32)
+        s1 = fa().get_device_error()
+        fa().decode_splitkv_gqa(qd, kc, vc, lens.to(DEV), n_splits=4, out_dtype=torch.float32)
+        s2 = fa().get_device_error()
+    finally:
+        fa().set_wait_timeout_ns(0)
+    assert s1 == fa().FA_ERR_TIMEOUT and s2 == fa().FA_ERR_TIMEOUT
+    o, lse = fa().fwd_splitkv(q, k, v, causal=True, n_splits=4, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == 0
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, scale=1 / math.sqrt(128))
+    assert_close(o, lse, o_ref, lse_ref, what="splitkv after a timed-out launch")
