@@ -3,8 +3,8 @@
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  It shares no code with the CUDA path: the C
 library ``fa_oracle.c`` (built here with gcc into ``liboracle.so``) is the
-plain definition of standard attention in float64, and ``numpy_oracle`` is
-an independent numpy restatement of the same pages.
+plain definition of standard attention and of its backward in float64, and
+``numpy_oracle`` is an independent numpy restatement of the same pages.
 
 Inputs are torch tensors or numpy arrays.  bf16 tensors are handed to the C
 library as raw bit patterns and widened exactly there; everything else is

@@ -15,7 +15,8 @@ It restates, in float64 and in the pages' own notation, the algorithms of
   order (outer loop over query tiles, inner loop over key/value tiles, the
   running max m and sum l rescaled by exp(m_old - m_new), one division by l
   at the end, L = m + log l, and the causal "stop at the first fully masked
-  tile" rule);
+  tile" rule), and ``flash_bwd_tiled`` -- the FlashAttention-2 form of the
+  backward (outer loop over key/value tiles, P recomputed as exp(S - L));
 * section 4 (flash-decoding): ``split_kv_decode`` -- split the keys into
   segments, normalise each segment's output, keep its log-sum-exp, merge.
 
