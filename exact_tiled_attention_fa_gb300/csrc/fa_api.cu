@@ -137,6 +137,26 @@ bool make_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d)
     return r == CUDA_SUCCESS;
 }
 
+// Output tensor [BH][rows][d] of bf16 or fp32 as a 3-D tiled map for bulk stores: the box is
+// 128 rows of one column block (128 bytes of a row, or the whole 64-byte row of bf16 d = 32),
+// swizzled to match the staging tile the forward kernel writes.
+bool make_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t)
+{
+    auto enc = encode_fn();
+    if (enc == nullptr) return false;
+    const int es = t == FA_F32 ? 4 : 2;
+    const int blk = d * es < 128 ? d : 128 / es;  // elements per box row
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(rows) * d * es};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(blk), static_cast<cuuint32_t>(fa::kBlockM), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, t == FA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     blk * es == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 bool head_ok(int d) { return d == 32 || d == 64 || d == 128; }
 bool dtype_ok(fa_dtype t) { return t == FA_BF16 || t == FA_F32; }
@@ -179,7 +199,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 
     fa::FwdParams p;
     if (!make_map(&p.tm_q, q, static_cast<int>(BH), N, d) || !make_map(&p.tm_k, k, static_cast<int>(BH), Nk, d) ||
-        !make_map(&p.tm_v, v, static_cast<int>(BH), Nk, dv))
+        !make_map(&p.tm_v, v, static_cast<int>(BH), Nk, dv) ||
+        !make_out_map(&p.tm_o, o, static_cast<int>(BH), N, dv, o_dtype))
         return FA_ERR_CUDA;
     int* status = nullptr;
     if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;

@@ -84,7 +84,9 @@ enum : int {
     kBarSFree = 18,                         // +tile (2): the softmax has read S_i out of TMEM
     kBarKVFull = 20,                        // +stage: K_j and V_j landed
     kBarKVEmpty = kBarKVFull + kMaxStages,  // +stage: both issuers are done with the stage
-    kBarCount = kBarKVEmpty + kMaxStages
+    kBarOStaged = kBarKVEmpty + kMaxStages,  // +tile (2): the warpgroup wrote its O rows to the staging tile
+    kBarOFree = kBarOStaged + 2,             // +tile (2): the previous bulk store has read the staging tile
+    kBarCount = kBarOFree + 2
 };
 
 template <int D>
@@ -104,10 +106,19 @@ struct FwdCfg {
     static constexpr int kOffQ = 0;  // Q buffer (b, i) at kOffQ + (2 * b + i) * kTileBytes
     static constexpr int kOffK = 2 * kQBuf * kTileBytes;
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
-    static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+    // For d <= 64 the epilogue writes O / l through shared memory and one bulk tensor store per
+    // query tile (a thread owns a row, so direct global stores would be 16-byte pieces 2*d bytes
+    // apart); one staging tile per query tile, sized for fp32 output.  d = 128 has no room left
+    // and stores rows directly (its items are long, so the epilogue weighs little).
+    static constexpr bool kStoreO = D <= 64;
+    static constexpr bool kAlternate = D <= 64;  // causal items alternate their query tiles (decode_item)
+    static constexpr int kOffStage = kOffV + kStages * kTileBytes;
+    static constexpr int kStageTileBytes = kStoreO ? kBlockM * D * 4 : 0;
+    static constexpr int kOffBar = kOffStage + 2 * kStageTileBytes;
     static constexpr int kNumBars = 48;
     static_assert(kStages <= kMaxStages && kBarCount <= kNumBars, "barrier slots");
     static constexpr int kUsedBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
+    static_assert(kUsedBytes <= 227 * 1024, "shared memory per CTA");
     // At least 120 KB so that a second CTA (which would wait for the 512 TMEM columns
     // this persistent CTA holds) never shares the SM.
     static constexpr int kSmemBytes = kUsedBytes > 120 * 1024 ? kUsedBytes : 120 * 1024;
@@ -131,10 +142,50 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     return r;
 }
 
-// Shape of one work item (head bh, query rows [i0, i0 + 256)).
+// Layout of a staged output tile: column blocks of 128-byte rows (64-byte rows for bf16 with
+// d = 32), 128 rows each, swizzled like the tensor map that stores them (the 16-byte chunk
+// index of row r XOR r mod 8 for 128-byte rows, XOR (r / 2) mod 4 for 64-byte rows), so that
+// the 32 rows a warp writes at once fall on distinct banks.
+template <typename OutT, int D>
+struct OStage {
+    static constexpr int kRowBytes = D * static_cast<int>(sizeof(OutT)) < 128 ? D * static_cast<int>(sizeof(OutT)) : 128;
+    static constexpr int kElems = kRowBytes / static_cast<int>(sizeof(OutT));  // elements per block row
+    static constexpr int kNumCB = D / kElems;
+    static constexpr int kBlkBytes = kBlockM * kRowBytes;
+    static constexpr int kChunks = kRowBytes / 16;
+};
+
+// Writes row r of a staged output tile: the raw fp32 O words times inv, converted to OutT.
+template <typename OutT, int D>
+__device__ __forceinline__ void stage_row(uint32_t stg, int r, const uint32_t (&o)[D], float inv)
+{
+    using OS = OStage<OutT, D>;
+    constexpr int kEpc = 16 / static_cast<int>(sizeof(OutT));  // elements per 16-byte chunk
+    const uint32_t row_addr = stg + static_cast<uint32_t>(r) * OS::kRowBytes;
+    const uint32_t sw = OS::kRowBytes == 128 ? static_cast<uint32_t>(r & 7) : static_cast<uint32_t>((r >> 1) & 3);
+#pragma unroll
+    for (int g = 0; g < D / kEpc; ++g) {
+        const uint32_t addr = row_addr + static_cast<uint32_t>((g / OS::kChunks) * OS::kBlkBytes) +
+                              ((static_cast<uint32_t>(g % OS::kChunks) ^ sw) << 4);
+        const int e = g * kEpc;
+        if constexpr (sizeof(OutT) == 2) {
+            st_shared_v4(addr, pack_bf16x2(__uint_as_float(o[e]) * inv, __uint_as_float(o[e + 1]) * inv),
+                         pack_bf16x2(__uint_as_float(o[e + 2]) * inv, __uint_as_float(o[e + 3]) * inv),
+                         pack_bf16x2(__uint_as_float(o[e + 4]) * inv, __uint_as_float(o[e + 5]) * inv),
+                         pack_bf16x2(__uint_as_float(o[e + 6]) * inv, __uint_as_float(o[e + 7]) * inv));
+        } else {
+            st_shared_v4(addr, __float_as_uint(__uint_as_float(o[e]) * inv), __float_as_uint(__uint_as_float(o[e + 1]) * inv),
+                         __float_as_uint(__uint_as_float(o[e + 2]) * inv), __float_as_uint(__uint_as_float(o[e + 3]) * inv));
+        }
+    }
+}
+
+// Shape of one work item (head bh, query rows [i0, i0 + 256)).  Query tile slot i (warpgroup i,
+// issuer i) takes rows [r0[i], r0[i] + 128).
 struct Item {
     int bh, i0;
-    int rows[2];  // valid query rows of Q0 / Q1 (0 when the tile lies past N)
+    int r0[2];    // first query row of slot 0 / 1
+    int rows[2];  // valid query rows of slot 0 / 1 (0 when the tile lies past N)
     int n[2];     // key/value tiles each query tile visits
     int n_kv;     // max(n[0], n[1])
 };
@@ -151,7 +202,7 @@ __device__ __forceinline__ int cta_item(const FwdParams& p, int k)
     return item < p.n_items ? static_cast<int>(item) : -1;
 }
 
-__device__ __forceinline__ Item decode_item(const FwdParams& p, int item, bool causal)
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int item, bool causal, bool alternate)
 {
     Item it;
     it.bh = item / p.n_qp;
@@ -160,9 +211,16 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int item, bool c
     it.i0 = qp * 2 * kBlockM;
     const int n_all = (p.Nk + kBlockN - 1) / kBlockN;
     const int off = p.Nk - p.N;
+    // Under a causal mask the upper query tile of a pair sees one key tile more than the lower
+    // one, and the slot with fewer tiles can only run ahead as far as the shared K/V ring lets
+    // it.  With `alternate`, odd items (every second item of a CTA) swap the halves, so over two
+    // items both slots carry the same number of tiles (d <= 64: causal prefill 670 -> 699
+    // TFLOP/s; the long d = 128 items measured 10 % slower with it, so they keep the order).
+    const int swap = (causal && alternate) ? (item & 1) : 0;
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-        const int r0 = it.i0 + i * kBlockM;
+        const int r0 = it.i0 + (i ^ swap) * kBlockM;
+        it.r0[i] = r0;
         it.rows[i] = r0 < p.N ? min(kBlockM, p.N - r0) : 0;
         int n = it.rows[i] > 0 ? n_all : 0;
         if (causal && n > 0) {
@@ -210,6 +268,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             mbar_init(bar(kBarKVFull + s), 1);
             mbar_init(bar(kBarKVEmpty + s), 2);  // one arrival from each MMA issuer
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(kBarOStaged + i), kBlockM);
+            mbar_init(bar(kBarOFree + i), 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -230,6 +292,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             prefetch_tensormap(&p.tm_q);
             prefetch_tensormap(&p.tm_k);
             prefetch_tensormap(&p.tm_v);
+            if (C::kStoreO) prefetch_tensormap(&p.tm_o);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
             int q_loads[2] = {0, 0};  // loads issued into each Q buffer
@@ -238,7 +301,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             for (int k = 0; ok; ++k) {
                 const int item = cta_item(p, k);
                 if (item < 0) break;
-                const Item it = decode_item(p, item, CAUSAL);
+                const Item it = decode_item(p, item, CAUSAL, C::kAlternate);
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (it.n[i] == 0) continue;
                     const int b = q_loads[i] % C::kQBuf;  // buffer of this load
@@ -252,7 +315,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
 #pragma unroll
                     for (int cb = 0; cb < C::kNumCB; ++cb)
                         tma_load_3d(sbase + C::kOffQ + q_bar * C::kTileBytes + cb * C::kBlkBytes, &p.tm_q,
-                                    bar(kBarQFull + q_bar), cb * C::kCB, it.i0 + i * kBlockM, it.bh, pol_q);
+                                    bar(kBarQFull + q_bar), cb * C::kCB, it.r0[i], it.bh, pol_q);
                     ++q_loads[i];
                 }
                 for (int j = 0; ok && j < it.n_kv; ++j, ++g) {
@@ -338,7 +401,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             for (int k = 0; ok; ++k) {
                 const int item = cta_item(p, k);
                 if (item < 0) break;
-                const Item it = decode_item(p, item, CAUSAL);
+                const Item it = decode_item(p, item, CAUSAL, C::kAlternate);
                 const int n = i ? it.n[1] : it.n[0];
                 const int q_bar = 2 * (q_uses % C::kQBuf) + i;
                 if (n > 0 && !mbar_wait(bar(kBarQFull + q_bar), (q_uses / C::kQBuf) & 1, limit, abort_flag)) {
@@ -417,15 +480,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         const int off = p.Nk - p.N;
         int tiles = 0;   // (query tile, key tile) pairs processed by this warpgroup
         int items = 0;   // items in which this warpgroup had key tiles
+        int staged = 0;  // output tiles this warpgroup wrote through the staging tile
         bool ok = true;
 
         for (int k = 0; ok; ++k) {
             const int item = cta_item(p, k);
             if (item < 0) break;
-            const Item it = decode_item(p, item, CAUSAL);
+            const Item it = decode_item(p, item, CAUSAL, C::kAlternate);
             const int n = wg ? it.n[1] : it.n[0];
             const int rows = wg ? it.rows[1] : it.rows[0];
-            const int row0 = it.i0 + wg * kBlockM;  // first query row of this tile
+            const int row0 = wg ? it.r0[1] : it.r0[0];  // first query row of this tile
             const int qpos = off + row0 + r;
             float m_run = -INFINITY;  // running max of scale*log2(e)*S over visible keys
             float l = 0.f;
@@ -534,25 +598,64 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const size_t row = static_cast<size_t>(it.bh) * p.N + static_cast<size_t>(row0 + r);
             const bool valid = r < rows;
-            OutT* orow = reinterpret_cast<OutT*>(p.o) + row * D;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                float v[32];
+            if constexpr (C::kStoreO) {
+                using OS = OStage<OutT, D>;
+                const uint32_t stg = sbase + C::kOffStage + static_cast<uint32_t>(wg) * C::kStageTileBytes;
+                if (staged > 0) {  // the previous tile's bulk store must have read the staging tile
+                    if (r == 0) {
+                        bulk_wait_read_all();
+                        mbar_arrive(bar(kBarOFree + wg));
+                    }
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOFree + wg), (staged - 1) & 1, limit, abort_flag));
+                    if (!ok) break;
+                }
+                uint32_t o[D];
                 if (n > 0) {
-                    uint32_t o[32];
-                    tmem_ld32(t_o + 32u * c, o);
-                    tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
+                    for (int c = 0; c < D / 32; ++c) tmem_ld32(t_o + 32u * c, *reinterpret_cast<uint32_t(*)[32]>(&o[32 * c]));
+                    tmem_ld_wait();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0.f;
+                    for (int e = 0; e < D; ++e) o[e] = 0u;
                 }
-                if (valid) store_row32<OutT>(orow + 32 * c, v);
+                stage_row<OutT, D>(stg, r, o, inv);
+                fence_proxy_async_shared();
+                mbar_arrive(bar(kBarOStaged + wg));
+                if (r == 0) {  // one thread stores the tile; rows past N lie outside the map and are skipped
+                    ok = mbar_wait(bar(kBarOStaged + wg), staged & 1, limit, abort_flag);
+                    if (ok) {
+#pragma unroll
+                        for (int cb = 0; cb < OS::kNumCB; ++cb)
+                            tma_store_3d(&p.tm_o, stg + cb * OS::kBlkBytes, cb * OS::kElems, row0, it.bh);
+                        bulk_commit_group();
+                    }
+                }
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ++staged;
+            } else {
+                OutT* orow = reinterpret_cast<OutT*>(p.o) + row * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    float v[32];
+                    if (n > 0) {
+                        uint32_t o[32];
+                        tmem_ld32(t_o + 32u * c, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = 0.f;
+                    }
+                    if (valid) store_row32<OutT>(orow + 32 * c, v);
+                }
             }
             if (p.lse != nullptr && valid)
                 p.lse[row] = l > 0.f ? (m_run + log2f(l)) * 0.69314718055994531f : -INFINITY;
         }
+        // Bulk stores must finish before the CTA's shared memory goes away.
+        if (C::kStoreO && r == 0 && staged > 0) bulk_wait_all();
         if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
     }
 

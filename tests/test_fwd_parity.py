@@ -70,8 +70,11 @@ def test_rows_without_visible_keys():
     assert torch.all(o[:, :, :200] == 0) and torch.all(torch.isneginf(lse[:, :, :200]))
 
 
-def test_deterministic_and_no_writes_past_output():
-    B, H, N, Nk, d = 2, 2, 333, 257, 128
+@pytest.mark.parametrize("d", [128, 64, 32])
+def test_deterministic_and_no_writes_past_output(d):
+    # d <= 64 writes O through a staging tile and bulk tensor stores, d = 128 row by row; both
+    # must leave the memory after the last row untouched (the last query tile is ragged).
+    B, H, N, Nk = 2, 2, 333, 257
     q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=6, device=DEV)
     guard = 4096
     for causal in (False, True):
