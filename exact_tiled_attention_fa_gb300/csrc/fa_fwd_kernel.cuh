@@ -564,19 +564,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                     tc_fence_after_sync();
                 }
                 if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                    // O row times alpha in chunks of kRescale columns: all of them at once for
+                    // d <= 64 (one TMEM round trip), 32 at a time for d = 128 (registers).
+                    constexpr int kRescale = D <= 64 ? D : 32;
+                    const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t oc[32];
-                        tmem_ld32(t_o + 32u * c, oc);
+                    for (int c0 = 0; c0 < D; c0 += kRescale) {
+                        uint32_t oc[kRescale];
+#pragma unroll
+                        for (int c = 0; c < kRescale; c += 32)
+                            tmem_ld32(t_o + static_cast<uint32_t>(c0 + c), *reinterpret_cast<uint32_t(*)[32]>(&oc[c]));
                         tmem_ld_wait();
-                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
+                        for (int e = 0; e < kRescale; e += 2) {
                             const float2 v = __fmul2_rn(make_float2(__uint_as_float(oc[e]), __uint_as_float(oc[e + 1])), a2);
                             oc[e] = __float_as_uint(v.x);
                             oc[e + 1] = __float_as_uint(v.y);
                         }
-                        tmem_st32(t_o + 32u * c, oc);
+#pragma unroll
+                        for (int c = 0; c < kRescale; c += 32)
+                            tmem_st32(t_o + static_cast<uint32_t>(c0 + c), *reinterpret_cast<uint32_t(*)[32]>(&oc[c]));
                     }
                 }
                 tmem_st32(t_p + 0, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
