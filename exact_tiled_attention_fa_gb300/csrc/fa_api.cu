@@ -276,7 +276,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     fa::BwdParams p;
     if (!make_map(&p.tm_q, q, static_cast<int>(BH), N, d) || !make_map(&p.tm_k, k, static_cast<int>(BH), Nk, d) ||
         !make_map(&p.tm_v, v, static_cast<int>(BH), Nk, dv) ||
-        !make_map(&p.tm_do, grad_o, static_cast<int>(BH), N, dv))
+        !make_map(&p.tm_do, grad_o, static_cast<int>(BH), N, dv) ||
+        !make_out_map(&p.tm_dk, grad_k, static_cast<int>(BH), Nk, d, grad_dtype) ||
+        !make_out_map(&p.tm_dv, grad_v, static_cast<int>(BH), Nk, dv, grad_dtype))
         return FA_ERR_CUDA;
     p.lse2 = lse2;
     p.dsc = dsc;

@@ -101,6 +101,8 @@ enum : int {
     kBbDVDone,        // dV(t) has read P^T(t)
     kBbSFree,         // S^T(t) loaded into registers (256 arrivals; d <= 64)
     kBbDKDone,        // dK(t) has read dS^T(t) (d <= 64)
+    kBbStageFull,     // the item's dK, dV rows written to the staging tiles (256 arrivals)
+    kBbStageFree,     // the bulk stores of the staging tiles have read them
     kBbCount
 };
 
@@ -130,7 +132,7 @@ struct BwdCfg {
     static constexpr int kOffL = kOffDS + 2 * kDSBlk;                     // + stage * 512
     static constexpr int kOffDsc = kOffL + kQStages * 512;                // + stage * 512
     static constexpr int kOffBar = kOffDsc + kQStages * 512;
-    static constexpr int kNumBars = 24;
+    static constexpr int kNumBars = 26;
     static_assert(kBbCount <= kNumBars, "barrier slots");
     static constexpr int kUsedBytes = kOffBar + kNumBars * 8 + 16;
     static constexpr int kMaxSmem = 232448;                // 227 KB per CTA
@@ -198,6 +200,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     };
     constexpr int QS = C::kQStages;
     constexpr int KVB = C::kKVBufs;
+    // dK_j and dV_j leave through shared memory and bulk tensor stores when both tiles fit in
+    // the dS buffer, which no tensor-core operation reads once the item's last dQ is done
+    // (bf16 gradients with d <= 64, fp32 with d = 32); otherwise each thread stores its row.
+    constexpr int kGRow = D * static_cast<int>(sizeof(GradT));  // bytes of a gradient row
+    constexpr bool kStageGrad = C::kDSOwn && kGRow <= 128;
+    constexpr int kGTile = kBlockN * kGRow;                      // one staged 128-row tile
+    static_assert(!kStageGrad || 2 * kGTile <= 2 * C::kDSBlk, "staging tiles exceed the dS buffer");
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < KVB; ++i) {
@@ -224,6 +233,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         mbar_init(bar(kBbDVDone), 1);
         mbar_init(bar(kBbSFree), 256);
         mbar_init(bar(kBbDKDone), 1);
+        mbar_init(bar(kBbStageFull), 256);
+        mbar_init(bar(kBbStageFree), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -244,6 +255,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             prefetch_tensormap(&p.tm_k);
             prefetch_tensormap(&p.tm_v);
             prefetch_tensormap(&p.tm_do);
+            if (kStageGrad) {
+                prefetch_tensormap(&p.tm_dk);
+                prefetch_tensormap(&p.tm_dv);
+            }
             const uint64_t pol_keep = policy_evict_last();  // Q_i, dO_i: read by every key tile of the head
             const uint64_t pol_once = policy_evict_first(); // K_j, V_j: read by one CTA only
             int g = 0;        // query tiles loaded (Q ring position)
@@ -437,6 +452,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         bool ok = true;
         int g = 0;
         int k = 0;
+        int staged = 0;            // items whose dK, dV went out through the staging tiles
+        bool stage_busy = false;   // the last of those stores may still be reading the dS buffer
         for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
             const Item it = item_at(x);
             const int key = it.j0 + kr;
@@ -536,6 +553,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                     if (!ok) break;
                     tc_fence_after_sync();
                 }
+                if (kStageGrad && stage_busy) {  // the previous item's bulk stores read the dS buffer
+                    if (threadIdx.x == 0) {
+                        bulk_wait_read_all();
+                        mbar_arrive(bar(kBbStageFree));
+                    }
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbStageFree), (staged - 1) & 1, limit, abort_flag));
+                    if (!ok) break;
+                    stage_busy = false;
+                }
                 tmem_st32(t_ds, pk);
                 // dS^T row kr into the MN-major dS operand: 16-byte chunk q8 of the 128-byte row goes
                 // to chunk q8 ^ (kr mod 8) (128-byte swizzle).
@@ -556,24 +582,76 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             if (!ok) break;
             ++k;
             tc_fence_after_sync();
+            if constexpr (kStageGrad) {
+                // Row kr of each tile, this thread's half of the columns, into the staging tiles
+                // (dV at the start of the dS buffer, dK after it), 16-byte chunks swizzled like
+                // the tensor maps (chunk index XOR kr mod 8 for 128-byte rows, XOR (kr / 2) mod 4
+                // for 64-byte rows); one thread then stores both tiles, rows past Nk clipped.
+                constexpr int kEpc = 16 / static_cast<int>(sizeof(GradT));  // elements per chunk
+                constexpr int kHalfChunks = kGRow / 32;                     // chunks of a half row
+                const uint32_t sw = kGRow == 128 ? static_cast<uint32_t>(kr & 7) : static_cast<uint32_t>((kr >> 1) & 3);
+                const uint32_t stg = sbase + C::kOffDS + static_cast<uint32_t>(kr) * kGRow;
+                uint32_t a[D / 2], b[D / 2];
 #pragma unroll
-            for (int c = 0; c < D / 2; c += 16) {
-                uint32_t a[16], b[16];
-                tmem_ld16(tmem + lane_base + C::kColDV + h * (D / 2) + c, a);
-                tmem_ld16(tmem + lane_base + C::kColDK + h * (D / 2) + c, b);
-                tmem_ld_wait();
-                float fa[16], fb[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    fa[e] = __uint_as_float(a[e]);
-                    fb[e] = __uint_as_float(b[e]);
+                for (int c = 0; c < D / 2; c += 16) {
+                    tmem_ld16(tmem + lane_base + C::kColDV + h * (D / 2) + c, *reinterpret_cast<uint32_t(*)[16]>(&a[c]));
+                    tmem_ld16(tmem + lane_base + C::kColDK + h * (D / 2) + c, *reinterpret_cast<uint32_t(*)[16]>(&b[c]));
                 }
-                if (valid) {
-                    store_row16<GradT>(dv + c, fa);
-                    store_row16<GradT>(dk + c, fb);
+                tmem_ld_wait();
+#pragma unroll
+                for (int q = 0; q < kHalfChunks; ++q) {
+                    const uint32_t off = ((static_cast<uint32_t>(h * kHalfChunks + q) ^ sw) << 4);
+                    const int e = q * kEpc;
+                    if constexpr (sizeof(GradT) == 2) {
+                        st_shared_v4(stg + off, pack_bf16x2(__uint_as_float(a[e]), __uint_as_float(a[e + 1])),
+                                     pack_bf16x2(__uint_as_float(a[e + 2]), __uint_as_float(a[e + 3])),
+                                     pack_bf16x2(__uint_as_float(a[e + 4]), __uint_as_float(a[e + 5])),
+                                     pack_bf16x2(__uint_as_float(a[e + 6]), __uint_as_float(a[e + 7])));
+                        st_shared_v4(stg + kGTile + off, pack_bf16x2(__uint_as_float(b[e]), __uint_as_float(b[e + 1])),
+                                     pack_bf16x2(__uint_as_float(b[e + 2]), __uint_as_float(b[e + 3])),
+                                     pack_bf16x2(__uint_as_float(b[e + 4]), __uint_as_float(b[e + 5])),
+                                     pack_bf16x2(__uint_as_float(b[e + 6]), __uint_as_float(b[e + 7])));
+                    } else {
+                        st_shared_v4(stg + off, a[e], a[e + 1], a[e + 2], a[e + 3]);
+                        st_shared_v4(stg + kGTile + off, b[e], b[e + 1], b[e + 2], b[e + 3]);
+                    }
+                }
+                fence_proxy_async_shared();
+                mbar_arrive(bar(kBbStageFull));
+                bool stored = true;
+                if (threadIdx.x == 0) {
+                    stored = mbar_wait(bar(kBbStageFull), staged & 1, limit, abort_flag);
+                    if (stored) {
+                        tma_store_3d(&p.tm_dv, sbase + C::kOffDS, 0, it.j0, it.bh);
+                        tma_store_3d(&p.tm_dk, sbase + C::kOffDS + kGTile, 0, it.j0, it.bh);
+                        bulk_commit_group();
+                    }
+                }
+                ok = __all_sync(0xffffffffu, stored);
+                if (!ok) break;
+                ++staged;
+                stage_busy = true;
+            } else {
+#pragma unroll
+                for (int c = 0; c < D / 2; c += 16) {
+                    uint32_t a[16], b[16];
+                    tmem_ld16(tmem + lane_base + C::kColDV + h * (D / 2) + c, a);
+                    tmem_ld16(tmem + lane_base + C::kColDK + h * (D / 2) + c, b);
+                    tmem_ld_wait();
+                    float fa[16], fb[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        fa[e] = __uint_as_float(a[e]);
+                        fb[e] = __uint_as_float(b[e]);
+                    }
+                    if (valid) {
+                        store_row16<GradT>(dv + c, fa);
+                        store_row16<GradT>(dk + c, fb);
+                    }
                 }
             }
         }
+        if (kStageGrad && threadIdx.x == 0 && staged > 0) bulk_wait_all();  // stores done before exit
         if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
     }
 

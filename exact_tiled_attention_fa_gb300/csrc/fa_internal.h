@@ -42,6 +42,8 @@ struct BwdParams {
     CUtensorMap tm_k;   // bf16 [B*H][Nk][d]
     CUtensorMap tm_v;   // bf16 [B*H][Nk][d]
     CUtensorMap tm_do;  // bf16 [B*H][N][d]
+    CUtensorMap tm_dk;  // dK [B*H][Nk][d] (gradient dtype), box {128 bytes of a row (64 for bf16 d = 32), 128, 1}
+    CUtensorMap tm_dv;  // dV, the same
     const float* lse2;  // [B*H][Tr*128]: LSE * log2(e); +inf past N and where no key is visible
     const float* dsc;   // [B*H][Tr*128]: scale * sum_c dO[c] O[c]; 0 past N
     float* dq_acc;      // [B*H][Tr][d/4][128][4] fp32, zeroed before the kernel

@@ -140,19 +140,42 @@ def test_full_size_sampled_heads(causal):
 
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-def test_persistent_items_per_cta(d, causal):
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
+def test_persistent_items_per_cta(d, causal, grad_dtype):
     """More (head, key tile) items than SMs, so each CTA walks several, short causal walks right
-    after long ones; every head against the oracle."""
+    after long ones; every third head against the oracle.  bf16 gradients with d = 64 leave
+    through the staging tiles (reused item after item), the others row by row."""
     B, H, N = 2, 16, 1024
     q, k, v = attention_inputs(B, H, N, N, d, d, seed=8, device=DEV)
     do = grad_output(B, H, N, d, seed=8, device=DEV)
     scale = 1.0 / math.sqrt(d)
-    got = gpu_grads(q, k, v, do, causal, scale)
+    got = gpu_grads(q, k, v, do, causal, scale, out_dtype=grad_dtype)
     heads = range(0, B * H, 3)
     flat = [t.reshape(B * H, *t.shape[2:]) for t in (q, k, v, do) + tuple(got)]
     sel = [t[list(heads)].cpu() for t in flat]
     ref = oracle.attention_bwd(sel[0], sel[1], sel[2], sel[3], causal=causal, scale=scale)
-    check(sel[4:], ref, magnitudes(sel[0], sel[1], sel[2], sel[3], causal, scale), what=f"items d={d} causal={causal}")
+    check(sel[4:], ref, magnitudes(sel[0], sel[1], sel[2], sel[3], causal, scale),
+          bf16_out=(grad_dtype == torch.bfloat16), what=f"items d={d} causal={causal} {grad_dtype}")
+
+
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("grad_dtype", [torch.float32, torch.bfloat16])
+def test_no_writes_past_gradients(d, grad_dtype):
+    """Ragged Nk (the last key tile has 44 keys): the memory right after dQ, dK and dV stays
+    untouched, whether the tiles leave through bulk tensor stores or row by row."""
+    B, H, N, Nk = 2, 2, 300, 300
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=11, device=DEV)
+    do = grad_output(B, H, N, d, seed=11, device=DEV)
+    o, lse = fa().fwd(q, k, v, causal=True, out_dtype=torch.float32)
+    guard = 4096
+    bufs = [torch.full((B * H * n * d + guard,), float("nan"), dtype=grad_dtype, device=DEV) for n in (N, Nk, Nk)]
+    grads = tuple(b[: B * H * n * d].view(B, H, n, d) for b, n in zip(bufs, (N, Nk, Nk)))
+    fa().bwd(q, k, v, o, lse, do, causal=True, grads=grads)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == 0
+    for b, g, n in zip(bufs, grads, (N, Nk, Nk)):
+        assert not torch.isnan(g).any()
+        assert torch.isnan(b[B * H * n * d:]).all()
 
 
 def test_rejects_small_workspace_and_bad_args():
