@@ -18,11 +18,11 @@
 // computes the transposed
 // products S^T = K_j Q_i^T and dP^T = V_j dO_i^T, so that a TMEM lane is a key:
 // the rows of P^T and dS^T that a thread produces are exactly the A operand rows
-// the tensor core needs for dV_j += P^T dO_i and dK_j += dS^T Q_i, both issued with
-// A read from tensor memory.  dV_j and dK_j stay in tensor memory for the whole
-// walk.  dQ_i = dS K_j needs dS with the queries as rows: the threads write their
-// dS^T rows to shared memory, which is dS in the MN-major (M-contiguous) operand
-// layout, and the tensor core reads it from there.  dQ_i (fp32, TMEM) is added
+// the tensor core needs for dV_j += P^T dO_i (A read from tensor memory) and
+// dK_j += dS^T Q_i.  dV_j and dK_j stay in tensor memory for the whole walk.  The
+// threads write their dS^T rows to shared memory: read there as K-major rows they are
+// the A operand of dK (d <= 64; d = 128 keeps dS^T in tensor memory too), and read as
+// MN-major (M-contiguous) they are dS, the A operand of dQ_i = dS K_j.  dQ_i (fp32, TMEM) is added
 // into a zeroed fp32 accumulator in global memory with vector atomics; a final
 // kernel converts it.  The scale is folded into dS (both dQ and dK carry it).
 //
@@ -31,8 +31,8 @@
 //                    and half of the query columns (warpgroup 0: queries 0-63,
 //                    warpgroup 1: queries 64-127 of the tile).  Per query tile it
 //                    reads S^T and writes P^T (bf16), then reads dP^T and writes dS^T
-//                    (bf16) to tensor memory and to shared memory.  At the end it writes
-//                    dK_j and dV_j.
+//                    (bf16) to shared memory (and for d = 128 to tensor memory).  At the
+//                    end it writes dK_j and dV_j.
 //   warp 8           TMA producer: K_j and V_j once; Q_i, dO_i, L_i and D_i into a
 //                    ring of three stages (two for d = 128).
 //   warps 9, 10      tcgen05 issuers.  Every barrier wait or commit stalls the issuing
@@ -45,9 +45,9 @@
 //                    while the compute warps exponentiate t+1.
 //   warps 12-15      dQ reduction: thread t owns query row t of the dQ tile.
 // Tensor memory (512 columns): S^T [0,128), dP^T [128,256), dV [256,256+d),
-// dK [256+d,256+2d), dQ [384,384+d) and P^T / dS^T [448,512) for d <= 64: P^T(t) is
-// stored once dK(t-1) has read dS^T(t-1), dS^T(t) once dV(t) has read P^T(t).  For
-// d = 128 there is no room for them: P^T(t) overwrites the S^T columns it came from,
+// dK [256+d,256+2d), dQ [384,384+d) and P^T [448,512) for d <= 64: P^T(t) is stored
+// once dV(t-1) has read P^T(t-1), dS(t) into shared memory once dK(t-1) and dQ(t-1) have
+// read dS(t-1).  For d = 128 there is no room: P^T(t) overwrites the S^T columns it came from,
 // dS^T(t) the dP^T columns, dQ(t) overwrites those again once dK(t) has read dS^T,
 // and dP(t+1) waits until the dQ reduction warps have read dQ(t) out.
 //
@@ -79,7 +79,7 @@ constexpr int kBwdWarpDq = 12;  // warps 12-15
 // control and dQ warpgroups shrink.  The launcher checks kBwdThreads * (registers at
 // launch) >= 256 * kBwdComputeRegs + 128 * (kBwdControlRegs + kBwdDqRegs).
 constexpr int kBwdComputeRegs = 184;
-constexpr int kBwdControlRegs = 72;
+constexpr int kBwdControlRegs = 80;
 constexpr int kBwdDqRegs = 64;
 
 constexpr int kBwdMaxQStages = 3;
@@ -100,7 +100,6 @@ enum : int {
     kBbDPFree = kBbDrain + 2,  // dP^T(t) loaded into registers (256 arrivals)
     kBbDVDone,        // dV(t) has read P^T(t)
     kBbSFree,         // S^T(t) loaded into registers (256 arrivals; d <= 64)
-    kBbDKDone,        // dK(t) has read dS^T(t) (d <= 64)
     kBbStageFull,     // the item's dK, dV rows written to the staging tiles (256 arrivals)
     kBbStageFree,     // the bulk stores of the staging tiles have read them
     kBbCount
@@ -143,12 +142,12 @@ struct BwdCfg {
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
     static constexpr uint32_t kColDQ = D == 128 ? 128 : 384;
     static constexpr bool kDQAlias = D == 128;
-    // d <= 64: P^T and dS^T share the last 64 columns (dV(t) reads P^T(t) before dS^T(t) is
-    // written), so S^T(t+1) and dP^T(t+1) may start as soon as S^T(t), dP^T(t) are loaded.
+    // d <= 64: P^T has the last 64 columns to itself and dS^T stays in shared memory, so
+    // S^T(t+1) and dP^T(t+1) may start as soon as S^T(t), dP^T(t) are loaded.
     static constexpr bool kDSOwn = D <= 64;
-    static constexpr uint32_t kColDS = kDSOwn ? 448 : kColDP;
+    static constexpr uint32_t kColDS = kColDP;  // d = 128: dS^T over the dP^T columns
     static constexpr uint32_t kColP = kDSOwn ? 448 : kColS;
-    static constexpr uint32_t kPHalf = kDSOwn ? 32 : 64;  // columns between the query halves of P^T, dS^T
+    static constexpr uint32_t kPHalf = kDSOwn ? 32 : 64;  // columns between the query halves of P^T (and dS^T)
     static constexpr uint32_t kIdescT = idesc_bf16(kBlockN, kBlockM, false);  // S^T, dP^T
     static constexpr uint32_t kIdescAcc = idesc_bf16(kBlockN, D, true);     // dV, dK
     static constexpr uint32_t kIdescDQ = idesc_bf16(kBlockM, D, true) | (1u << 15);  // A MN-major
@@ -232,7 +231,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         mbar_init(bar(kBbDone), 1);
         mbar_init(bar(kBbDVDone), 1);
         mbar_init(bar(kBbSFree), 256);
-        mbar_init(bar(kBbDKDone), 1);
         mbar_init(bar(kBbStageFull), 256);
         mbar_init(bar(kBbStageFree), 1);
         *abort_flag = 0;
@@ -339,6 +337,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                     umma_ts(tmem + d_col, tmem + a_col + half_stride * (kk >> 2) + 8u * (kk & 3),
                             b0 + ((kk * 16 * C::kRowBytes) >> 4), C::kIdescAcc, (accumulate || kk > 0) ? 1u : 0u);
             };
+            // d <= 64: dK += dS^T Q_i with A = dS^T read from the shared-memory dS buffer, whose key
+            // rows hold their 128 queries as two swizzled 64-query blocks (K-major for this product).
+            auto issue_dk_smem = [&](int q_off, bool accumulate) {
+                const uint64_t a0 = smem_desc(sbase + C::kOffDS, 16, 1024, kSwizzle128B);
+                const uint64_t b0 = smem_desc(sbase + q_off, C::kBlkBytes, C::kAtomBytes, C::kLayout);
+#pragma unroll
+                for (int kk = 0; kk < kBlockM / 16; ++kk) {
+                    const uint32_t ao = ((kk * 16) / 64 * C::kDSBlk + ((kk * 16) % 64) * 2) >> 4;
+                    umma_ss(tmem + C::kColDK, a0 + ao, b0 + ((kk * 16 * C::kRowBytes) >> 4), C::kIdescAcc,
+                            (accumulate || kk > 0) ? 1u : 0u);
+                }
+            };
             // dQ = dS K_j: A = dS (MN-major, two 64-query blocks), B = K_j (MN-major).
             auto issue_dq = [&](int k_off) {
                 const uint64_t a0 = smem_desc(sbase + C::kOffDS, C::kDSBlk, 1024, kSwizzle128B);
@@ -385,9 +395,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                         umma_commit(bar(kBbDVDone));
                         if (!wait(kBbDSReady, g)) break;
                         tc_fence_after_sync();
-                        issue_acc(C::kColDK, C::kColDS, C::kPHalf, C::kOffQ + s * C::kTileBytes, t > 0);
+                        if constexpr (C::kDSOwn)
+                            issue_dk_smem(C::kOffQ + s * C::kTileBytes, t > 0);
+                        else
+                            issue_acc(C::kColDK, C::kColDS, C::kPHalf, C::kOffQ + s * C::kTileBytes, t > 0);
                         umma_commit(bar(kBbQEmpty + s));
-                        if (C::kDSOwn) umma_commit(bar(kBbDKDone));
                         if (!C::kDQAlias && g > 0 && !wait(kBbDQFree, g - 1)) break;
                         tc_fence_after_sync();
                         issue_dq(k_off);
@@ -511,8 +523,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                 }
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) pk[c / 2] = pack_bf16x2(pf[c], pf[c + 1]);
-                if (C::kDSOwn && g > 0) {  // dK must have read the previous dS^T from the shared columns
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDKDone), (g - 1) & 1, limit, abort_flag));
+                if (C::kDSOwn && g > 0) {  // dV must have read the previous P^T from these columns
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDVDone), (g - 1) & 1, limit, abort_flag));
                     if (!ok) break;
                     tc_fence_after_sync();
                 }
@@ -546,10 +558,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                     pk[c / 2 + 1] = pack_bf16x2(g23.x, g23.y);
                 }
                 if constexpr (C::kDSOwn) {
-                    // dV must have read P^T from the shared columns, and the previous dQ the previous
-                    // dS from shared memory
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDVDone), g & 1, limit, abort_flag) &&
-                                                     (g == 0 || mbar_wait(bar(kBbDQFull), (g - 1) & 1, limit, abort_flag)));
+                    // the previous dK and dQ must have read the previous dS from shared memory (dQ is
+                    // issued after dK by the same thread, so its completion covers both)
+                    ok = __all_sync(0xffffffffu, g == 0 || mbar_wait(bar(kBbDQFull), (g - 1) & 1, limit, abort_flag));
                     if (!ok) break;
                     tc_fence_after_sync();
                 }
@@ -562,7 +573,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                     if (!ok) break;
                     stage_busy = false;
                 }
-                tmem_st32(t_ds, pk);
+                if constexpr (!C::kDSOwn) tmem_st32(t_ds, pk);  // d = 128: dK reads dS^T from tensor memory
                 // dS^T row kr into the MN-major dS operand: 16-byte chunk q8 of the 128-byte row goes
                 // to chunk q8 ^ (kr mod 8) (128-byte swizzle).
 #pragma unroll
@@ -570,7 +581,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
                     st_shared_v4(ds_row + ((q8 ^ (kr & 7)) << 4), pk[4 * q8], pk[4 * q8 + 1], pk[4 * q8 + 2],
                                  pk[4 * q8 + 3]);
                 fence_proxy_async_shared();
-                tmem_st_wait();
+                if constexpr (!C::kDSOwn) tmem_st_wait();
                 tc_fence_before_sync();
                 mbar_arrive(bar(kBbDSReady));
             }
