@@ -47,8 +47,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch of the dominant kernel from one ncu capture, keyed by
 # the SHA-256 of the kernel source it was taken on; reported only while the source is unchanged.
 KERNEL_TRAFFIC = {
-    # profiles/fa_fwd_kernel_d64_gpt2medium_prefill.md: non-causal launch, 402.78 MB read + 107.30 MB written
-    "34379067489fbaf84ac4d05ce03a006ebb18c7ed1a1ef1438f1546ef44e079a5": 510.08e6,
+    # profiles/fa_fwd_kernel_d64_gpt2medium_prefill.md: non-causal launch, 402.73 MB read + 107.41 MB written
+    "b800e7b8da5af2eef0c5cbcce61c0916032c7c4e929bd6cd3b16a1baeb837617": 510.13e6,
 }
 
 
