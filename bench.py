@@ -546,7 +546,7 @@ def run_decode_gqa(fa, dev, stream, args, world, Hkv=None):
     lens_d = lens.to(dev)
     n = 0  # the library's automatic split count; the workspace covers either heuristic
     sms = fa.num_sms(dev)
-    n_ws = max(fa.decode_default_splits(B, Hkv, Nk_max, sms), min(-(-6 * sms // (B * Hkv)), -(-Nk_max // 128)))
+    n_ws = max(fa.decode_default_splits(B, Hq, Nk_max, sms), min(-(-6 * sms // (B * Hkv)), -(-Nk_max // 128)))
     ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n_ws), dtype=torch.uint8, device=dev)
     o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)

@@ -324,7 +324,7 @@ def decode_splitkv_gqa(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out
         n = int(n_splits)
     else:  # the larger of the two automatic counts (CUDA-core and tensor-core groups)
         sms = num_sms(dev)
-        n = max(decode_default_splits(B, Hkv, Nk_max, sms), min(-(-6 * sms // (B * Hkv)), -(-Nk_max // 128)))
+        n = max(decode_default_splits(B, Hq, Nk_max, sms), min(-(-6 * sms // (B * Hkv)), -(-Nk_max // 128)))
     if workspace is None:
         workspace = torch.empty(max(decode_workspace_size(B, Hq, dv, max(1, min(n, Nk_max))), 256),
                                 dtype=torch.uint8, device=dev)

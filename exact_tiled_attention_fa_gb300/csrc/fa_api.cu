@@ -395,9 +395,11 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
     if (n == 0) {
         int sms = 0;
         if (sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
-        // one CTA per (b, key/value head, split); a tensor-core CTA holds a whole SM, so its
-        // splits are longer (about six per SM in total, each at least one 128-key tile)
-        n = tc ? gqa_tc_default_splits(B, Hkv, Nk_max, sms) : fa_decode_default_splits(B, Hkv, Nk_max, sms);
+        // one CTA per (b, key/value head, split).  On CUDA cores a CTA's arithmetic grows with
+        // the R heads it carries, so the count follows the B * Hq query heads (R = 4: 4.3 -> 4.8
+        // TB/s against counting B * Hkv items); a tensor-core CTA holds a whole SM, so its splits
+        // are longer (about six per SM in total, each at least one 128-key tile)
+        n = tc ? gqa_tc_default_splits(B, Hkv, Nk_max, sms) : fa_decode_default_splits(B, Hq, Nk_max, sms);
     }
     if (n > Nk_max) n = Nk_max;
     const size_t part_bytes = fa_decode_workspace_size(B, Hq, dv, n);

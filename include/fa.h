@@ -181,7 +181,7 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
  *   o          o_dtype [B, Hq, 1, dv]      (device, written)
  *   lse        fp32 [B, Hq, 1]             (device, written; may be NULL)
  *   workspace  ws_bytes >= fa_decode_workspace_size(B, Hq, dv, n) bytes, where n is n_splits or,
- *              for n_splits = 0, fa_decode_default_splits(B, Hkv, Nk_max, <SMs of the device>) for
+ *              for n_splits = 0, fa_decode_default_splits(B, Hq, Nk_max, <SMs of the device>) for
  *              groups of 1, 2 or 4 heads and min(ceil(6 * SMs / (B * Hkv)), ceil(Nk_max / 128)) for
  *              other group sizes (fa_decode_workspace_size of the larger of the two always suffices).
  *   Hkv >= 1 dividing Hq, R = Hq / Hkv <= 128 (larger groups return FA_ERR_UNSUPPORTED).
