@@ -13,12 +13,15 @@
 // one head and a pair of 128-row query tiles Q0, Q1 that share every K/V tile.
 // Items are ordered head-major (the query pairs of one head run on neighbouring
 // CTAs, so that head's K and V are read from HBM once and then hit in L2) and are
-// handed out two at a time, a heavy and a light one (see cta_item).  Ten warps:
+// handed out two at a time, a heavy and a light one (see cta_item); under a causal
+// mask odd items swap which slot takes the upper query tile (d <= 64, decode_item).
+// Twelve warps (three warpgroups, as `setmaxnreg` acts on whole warpgroups):
 //   warps 0-3 / 4-7  softmax warpgroups for Q0 / Q1: thread t owns query row t
 //                    (= TMEM lane t): it reads its score row from TMEM, masks,
 //                    updates m and l in base 2 with a log2(e)-prescaled scale,
 //                    writes P (bf16) back to TMEM, rescales its O row when the max
-//                    grew, and at the end of the item writes O / l and LSE.
+//                    grew, and at the end of the item writes LSE and O / l (d <= 64:
+//                    through a shared-memory staging tile and one bulk tensor store).
 //   warp 8           TMA producer: Q0, Q1 per item (double-buffered for d <= 64),
 //                    K_j / V_j into a ring of stages.
 //   warps 9, 10      tcgen05 issuers for Q0 and Q1: S_i = Q_i K_j^T (both operands in
@@ -28,6 +31,7 @@
 //                    Every barrier wait or commit stalls the issuing thread for a few
 //                    hundred cycles, so each issuer handles only its own query tile,
 //                    and K_j / V_j share one barrier.
+//   warp 11          idle (completes the control warpgroup).
 // Tensor memory (512 columns): S0, S1 (128 fp32 columns each), O0, O1 (d each) and
 // P0, P1 (64 columns of packed bf16 each).  For d = 128 there is no room left, so
 // P_i overwrites the first half of S_i (already read into registers); S_i(j+1) is
