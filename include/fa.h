@@ -115,8 +115,9 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   B, H, N, Nk >= 1; d = dv in {32, 64, 128}; causal 0 or 1; scale > 0 and finite, the
  *   value the forward used.
  * Three kernels are enqueued on `stream`: a preparation pass (D, lse in base 2, zeroing the
- * dQ accumulator), the tensor-core pass (one CTA per (b, h, 128-key tile), dK and dV
- * written directly, dQ added into the accumulator) and the dQ conversion.
+ * dQ accumulator), the tensor-core pass (a persistent grid, one CTA per SM, walking the
+ * (b, h, 128-key tile) items; each item's dK and dV written when its walk ends, dQ added into
+ * the accumulator) and the dQ conversion.
  * Returns FA_ERR_WORKSPACE if ws_bytes is too small (nothing launched).
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
