@@ -93,7 +93,7 @@ enum : int {
     kBarCount = kBarOFree + 2
 };
 
-template <int D>
+template <int D, int OutBytes>
 struct FwdCfg {
     static_assert(D == 32 || D == 64 || D == 128, "head size");
     static constexpr int kCB = D < 64 ? D : 64;            // elements per column block (swizzle span)
@@ -103,7 +103,8 @@ struct FwdCfg {
     static constexpr int kAtomBytes = 8 * kRowBytes;       // 8-row swizzle atom
     static constexpr int kBlkBytes = kBlockM * kRowBytes;  // one 128-row column block
     static constexpr int kTileBytes = kNumCB * kBlkBytes;  // 128 x D bf16
-    static constexpr int kStages = D == 128 ? 2 : (D == 64 ? 3 : 4);  // K/V ring depth
+    // K/V ring depth: d = 64 with bf16 output has room for a fourth stage beside its staging tiles
+    static constexpr int kStages = D == 128 ? 2 : (D == 64 ? (OutBytes == 2 ? 4 : 3) : 4);
     // Q buffers per query tile: two for d <= 64, so the next item's Q loads while the
     // current item runs (an item there spans few key tiles); one for d = 128 (no room).
     static constexpr int kQBuf = D == 128 ? 1 : 2;
@@ -112,12 +113,12 @@ struct FwdCfg {
     static constexpr int kOffV = kOffK + kStages * kTileBytes;
     // For d <= 64 the epilogue writes O / l through shared memory and one bulk tensor store per
     // query tile (a thread owns a row, so direct global stores would be 16-byte pieces 2*d bytes
-    // apart); one staging tile per query tile, sized for fp32 output.  d = 128 has no room left
+    // apart); one staging tile per query tile, sized for the output type.  d = 128 has no room left
     // and stores rows directly (its items are long, so the epilogue weighs little).
     static constexpr bool kStoreO = D <= 64;
     static constexpr bool kAlternate = D <= 64;  // causal items alternate their query tiles (decode_item)
     static constexpr int kOffStage = kOffV + kStages * kTileBytes;
-    static constexpr int kStageTileBytes = kStoreO ? kBlockM * D * 4 : 0;
+    static constexpr int kStageTileBytes = kStoreO ? kBlockM * D * OutBytes : 0;
     static constexpr int kOffBar = kOffStage + 2 * kStageTileBytes;
     static constexpr int kNumBars = 48;
     static_assert(kStages <= kMaxStages && kBarCount <= kNumBars, "barrier slots");
@@ -240,7 +241,7 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int item, bool c
 template <int D, bool CAUSAL, typename OutT>
 __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p)
 {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, static_cast<int>(sizeof(OutT))>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -682,7 +683,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
 template <int D, bool CAUSAL, typename OutT>
 cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
 {
-    using C = FwdCfg<D>;
+    using C = FwdCfg<D, static_cast<int>(sizeof(OutT))>;
     auto kern = fa_fwd_kernel<D, CAUSAL, OutT>;
     static bool configured[64] = {};  // the shared-memory attribute is set once per device
     int dev = 0;
