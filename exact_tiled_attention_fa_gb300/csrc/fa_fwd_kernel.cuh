@@ -547,18 +547,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 // non-exponential instructions of this loop.
                 const float2 sl2x2 = make_float2(sl2, sl2);
                 const float2 negm = make_float2(-m_use, -m_use);
-                float2 rs01 = make_float2(0.f, 0.f), rs23 = make_float2(0.f, 0.f);
+                // Four running pairs for the row sum keep its dependency chains short.
+                float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                make_float2(0.f, 0.f)};
                 uint32_t pk[kBlockN / 2];
 #pragma unroll
-                for (int c = 0; c < kBlockN; c += 4) {
-                    const float2 x01 = __ffma2_rn(make_float2(s[c + 0], s[c + 1]), sl2x2, negm);
-                    const float2 x23 = __ffma2_rn(make_float2(s[c + 2], s[c + 3]), sl2x2, negm);
-                    const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
-                    const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
-                    rs01 = __fadd2_rn(rs01, p01);
-                    rs23 = __fadd2_rn(rs23, p23);
-                    pk[c / 2] = pack_bf16x2(p01.x, p01.y);
-                    pk[c / 2 + 1] = pack_bf16x2(p23.x, p23.y);
+                for (int c = 0; c < kBlockN; c += 8) {
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        const float2 x = __ffma2_rn(make_float2(s[c + 2 * h], s[c + 2 * h + 1]), sl2x2, negm);
+                        const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                        rs[h] = __fadd2_rn(rs[h], e);
+                        pk[c / 2 + h] = pack_bf16x2(e.x, e.y);
+                    }
                 }
                 // O_i and the P_i columns are free once P_i(j-1) V_{j-1} has completed.  With P
                 // aliased into S_i this is implied by the arrival of S_i(j); otherwise wait for it.
@@ -596,7 +597,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 tmem_st_wait();
                 tc_fence_before_sync();
                 mbar_arrive(bar(kBarPFull + wg));
-                l = l * alpha + ((rs01.x + rs01.y) + (rs23.x + rs23.y));
+                l = l * alpha + (((rs[0].x + rs[0].y) + (rs[1].x + rs[1].y)) + ((rs[2].x + rs[2].y) + (rs[3].x + rs[3].y)));
                 ++tiles;
             }
             if (!ok) break;
