@@ -275,15 +275,22 @@ __global__ void __launch_bounds__(kSkThreads, 1) fa_splitkv_kernel(const __grid_
                 m_run = mt;
             }
             const float m_use = m_run == -INFINITY ? 0.f : m_run;
-            float rs = 0.f;
+            // packed two-wide scale-and-subtract and four running pairs for the row sum
+            const float2 sl2x2 = make_float2(sl2, sl2), negm = make_float2(-m_use, -m_use);
+            float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                             make_float2(0.f, 0.f)};
             uint32_t pk[kBlockN / 2];
 #pragma unroll
-            for (int c = 0; c < kBlockN; c += 2) {
-                const float p0 = ex2(fmaf(sv[c], sl2, -m_use));
-                const float p1 = ex2(fmaf(sv[c + 1], sl2, -m_use));
-                rs += p0 + p1;
-                pk[c / 2] = pack_bf16x2(p0, p1);
+            for (int c = 0; c < kBlockN; c += 8) {
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float2 x = __ffma2_rn(make_float2(sv[c + 2 * h], sv[c + 2 * h + 1]), sl2x2, negm);
+                    const float2 e = make_float2(ex2(x.x), ex2(x.y));
+                    rs2[h] = __fadd2_rn(rs2[h], e);
+                    pk[c / 2 + h] = pack_bf16x2(e.x, e.y);
+                }
             }
+            const float rs = ((rs2[0].x + rs2[0].y) + (rs2[1].x + rs2[1].y)) + ((rs2[2].x + rs2[2].y) + (rs2[3].x + rs2[3].y));
             // O and the P columns are free once P(t-1) V_{t-1} has completed
             if (t > 0) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(kSbPVDone), (t - 1) & 1, limit, abort_flag));
@@ -295,8 +302,13 @@ __global__ void __launch_bounds__(kSkThreads, 1) fa_splitkv_kernel(const __grid_
                         uint32_t oc[32];
                         tmem_ld32(t_o + 32u * c, oc);
                         tmem_ld_wait();
+                        const float2 a2 = make_float2(alpha, alpha);
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) oc[e] = __float_as_uint(__uint_as_float(oc[e]) * alpha);
+                        for (int e = 0; e < 32; e += 2) {
+                            const float2 v = __fmul2_rn(make_float2(__uint_as_float(oc[e]), __uint_as_float(oc[e + 1])), a2);
+                            oc[e] = __float_as_uint(v.x);
+                            oc[e + 1] = __float_as_uint(v.y);
+                        }
                         tmem_st32(t_o + 32u * c, oc);
                     }
                 }
