@@ -235,7 +235,7 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int dv, int n_splits);
 
 /*
  * Exact attention forward with the keys split ("flash_lab.py" section 4 `split_kv_decode`
- * applied to a query tile; SURVEY's split-KV prefill): for workloads with few 128-row query
+ * applied to a query tile): for workloads with few 128-row query
  * tiles (B*H*ceil(N/128) below the number of multiprocessors) the keys are cut into n_splits
  * chunks of whole 128-key tiles; each (head, query tile, chunk) computes its normalised output
  * and log-sum-exp, and a second kernel merges them.  Same arguments, masks, result and output
