@@ -195,15 +195,22 @@ struct Item {
     int n_kv;     // max(n[0], n[1])
 };
 
-// k-th work item of this CTA, or -1 past the end.  A CTA takes pairs of consecutive
-// items (pair blockIdx.x + t * gridDim.x).  Within a head the query pairs run heaviest,
-// lightest, second heaviest, second lightest, ... (see decode_item), so under a causal
-// mask the two items of a pair together carry about the same work as any other pair
-// and the static assignment stays balanced without a global work counter.
-__device__ __forceinline__ int cta_item(const FwdParams& p, int k)
+// k-th work item of this CTA, or -1 past the end.  Under a causal mask a CTA takes pairs
+// of consecutive items (pair blockIdx.x + t * gridDim.x): within a head the query pairs run
+// heaviest, lightest, second heaviest, second lightest, ... (see decode_item), so the two
+// items of a pair together carry about the same work as any other pair and the static
+// assignment stays balanced without a global work counter.  Without a mask every item
+// carries the same work and CTA c takes items c, c + G, c + 2G, ...: the last round is then
+// one item, not one pair, short (B=64 H=16 N=1024: 27 items on the busiest CTA instead of 28).
+__device__ __forceinline__ int cta_item(const FwdParams& p, int k, bool causal)
 {
-    const long long pair = blockIdx.x + static_cast<long long>(k >> 1) * gridDim.x;
-    const long long item = 2 * pair + (k & 1);
+    long long item;
+    if (causal) {
+        const long long pair = blockIdx.x + static_cast<long long>(k >> 1) * gridDim.x;
+        item = 2 * pair + (k & 1);
+    } else {
+        item = blockIdx.x + static_cast<long long>(k) * gridDim.x;
+    }
     return item < p.n_items ? static_cast<int>(item) : -1;
 }
 
@@ -304,7 +311,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             long long g = 0;          // K/V tiles issued so far (ring position)
             bool ok = true;
             for (int k = 0; ok; ++k) {
-                const int item = cta_item(p, k);
+                const int item = cta_item(p, k, CAUSAL);
                 if (item < 0) break;
                 const Item it = decode_item(p, item, CAUSAL, C::kAlternate);
                 for (int i = 0; i < 2 && ok; ++i) {
@@ -404,7 +411,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             };
 
             for (int k = 0; ok; ++k) {
-                const int item = cta_item(p, k);
+                const int item = cta_item(p, k, CAUSAL);
                 if (item < 0) break;
                 const Item it = decode_item(p, item, CAUSAL, C::kAlternate);
                 const int n = i ? it.n[1] : it.n[0];
@@ -489,7 +496,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         bool ok = true;
 
         for (int k = 0; ok; ++k) {
-            const int item = cta_item(p, k);
+            const int item = cta_item(p, k, CAUSAL);
             if (item < 0) break;
             const Item it = decode_item(p, item, CAUSAL, C::kAlternate);
             const int n = wg ? it.n[1] : it.n[0];
@@ -705,8 +712,8 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
     const int launch_regs = (dev >= 0 && dev < 64) ? regs[dev] : 0;
     if (launch_regs * kFwdThreads < 256 * kSoftmaxRegs<D> + 128 * kControlRegs<D>)
         return cudaErrorLaunchOutOfResources;  // the register split would not fit
-    const int pairs = (p.n_items + 1) / 2;
-    const int grid = pairs < p.num_ctas ? pairs : p.num_ctas;
+    const int units = CAUSAL ? (p.n_items + 1) / 2 : p.n_items;  // pairs of items, or items (cta_item)
+    const int grid = units < p.num_ctas ? units : p.num_ctas;
     kern<<<grid, kFwdThreads, C::kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
