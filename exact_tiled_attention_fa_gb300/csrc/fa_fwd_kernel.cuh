@@ -13,7 +13,7 @@
 // one head and a pair of 128-row query tiles Q0, Q1 that share every K/V tile.
 // Items are ordered head-major (the query pairs of one head run on neighbouring
 // CTAs, so that head's K and V are read from HBM once and then hit in L2) and are
-// handed out two at a time, a heavy and a light one (see cta_item); under a causal
+// handed out two at a time, a heavy and a light one (see first_item); under a causal
 // mask odd items swap which slot takes the upper query tile (d <= 64, decode_item).
 // Twelve warps (three warpgroups, as `setmaxnreg` acts on whole warpgroups):
 //   warps 0-3 / 4-7  softmax warpgroups for Q0 / Q1: thread t owns query row t
@@ -195,30 +195,54 @@ struct Item {
     int n_kv;     // max(n[0], n[1])
 };
 
-// k-th work item of this CTA, or -1 past the end.  Under a causal mask a CTA takes pairs
+// The work items of a CTA.  Under a causal mask a CTA takes pairs
 // of consecutive items (pair blockIdx.x + t * gridDim.x): within a head the query pairs run
 // heaviest, lightest, second heaviest, second lightest, ... (see decode_item), so the two
 // items of a pair together carry about the same work as any other pair and the static
 // assignment stays balanced without a global work counter.  Without a mask every item
 // carries the same work and CTA c takes items c, c + G, c + 2G, ...: the last round is then
 // one item, not one pair, short (B=64 H=16 N=1024: 27 items on the busiest CTA instead of 28).
-__device__ __forceinline__ int cta_item(const FwdParams& p, int k, bool causal)
+// This CTA's items in that order, with each item's head and position in the head
+// advanced by additions: the per-item bookkeeping runs on warps that share their issue slots
+// with exponentiating warps, where a 32-bit division and 64-bit index arithmetic cost hundreds
+// of cycles at every item boundary.
+struct ItemCursor {
+    int item, bh, t, k;
+};
+
+__device__ __forceinline__ ItemCursor first_item(const FwdParams& p, bool causal)
 {
-    long long item;
-    if (causal) {
-        const long long pair = blockIdx.x + static_cast<long long>(k >> 1) * gridDim.x;
-        item = 2 * pair + (k & 1);
-    } else {
-        item = blockIdx.x + static_cast<long long>(k) * gridDim.x;
-    }
-    return item < p.n_items ? static_cast<int>(item) : -1;
+    ItemCursor c;
+    c.item = causal ? 2 * static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+    c.bh = c.item / p.n_qp;
+    c.t = c.item - c.bh * p.n_qp;
+    c.k = 0;
+    return c;
 }
 
-__device__ __forceinline__ Item decode_item(const FwdParams& p, int item, bool causal, bool alternate)
+__device__ __forceinline__ void next_item(const FwdParams& p, ItemCursor& c, bool causal)
 {
+    if (causal && (c.k & 1) == 0) {  // second item of the pair
+        c.item += 1;
+        c.t += 1;
+    } else {                         // first item of the next round
+        c.item += causal ? 2 * static_cast<int>(gridDim.x) - 1 : static_cast<int>(gridDim.x);
+        c.bh += p.step_heads;
+        c.t += p.step_rem;
+    }
+    if (c.t >= p.n_qp) {
+        c.t -= p.n_qp;
+        c.bh += 1;
+    }
+    c.k += 1;
+}
+
+__device__ __forceinline__ Item decode_item(const FwdParams& p, const ItemCursor& c, bool causal, bool alternate)
+{
+    const int item = c.item;
     Item it;
-    it.bh = item / p.n_qp;
-    const int t = item - it.bh * p.n_qp;
+    it.bh = c.bh;
+    const int t = c.t;
     const int qp = (t & 1) ? (t >> 1) : p.n_qp - 1 - (t >> 1);  // heavy, light, heavy, light, ...
     it.i0 = qp * 2 * kBlockM;
     const int n_all = (p.Nk + kBlockN - 1) / kBlockN;
@@ -310,10 +334,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             int q_loads[2] = {0, 0};  // loads issued into each Q buffer
             long long g = 0;          // K/V tiles issued so far (ring position)
             bool ok = true;
-            for (int k = 0; ok; ++k) {
-                const int item = cta_item(p, k, CAUSAL);
-                if (item < 0) break;
-                const Item it = decode_item(p, item, CAUSAL, C::kAlternate);
+            for (ItemCursor cur = first_item(p, CAUSAL); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL)) {
+                const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (it.n[i] == 0) continue;
                     const int b = q_loads[i] % C::kQBuf;  // buffer of this load
@@ -410,10 +432,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 return true;
             };
 
-            for (int k = 0; ok; ++k) {
-                const int item = cta_item(p, k, CAUSAL);
-                if (item < 0) break;
-                const Item it = decode_item(p, item, CAUSAL, C::kAlternate);
+            for (ItemCursor cur = first_item(p, CAUSAL); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL)) {
+                const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
                 const int n = i ? it.n[1] : it.n[0];
                 const int q_bar = 2 * (q_uses % C::kQBuf) + i;
                 if (n > 0 && !mbar_wait(bar(kBarQFull + q_bar), (q_uses / C::kQBuf) & 1, limit, abort_flag)) {
@@ -495,10 +515,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         int staged = 0;  // output tiles this warpgroup wrote through the staging tile
         bool ok = true;
 
-        for (int k = 0; ok; ++k) {
-            const int item = cta_item(p, k, CAUSAL);
-            if (item < 0) break;
-            const Item it = decode_item(p, item, CAUSAL, C::kAlternate);
+        for (ItemCursor cur = first_item(p, CAUSAL); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL)) {
+            const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
             const int n = wg ? it.n[1] : it.n[0];
             const int rows = wg ? it.rows[1] : it.rows[0];
             const int row0 = wg ? it.r0[1] : it.r0[0];  // first query row of this tile
@@ -672,7 +690,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 }
             }
             if (p.lse != nullptr && valid)
-                p.lse[row] = l > 0.f ? (m_run + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                p.lse[row] = l > 0.f ? (m_run + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
         }
         // Bulk stores must finish before the CTA's shared memory goes away.
         if (C::kStoreO && r == 0 && staged > 0) bulk_wait_all();
@@ -712,9 +730,13 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
     const int launch_regs = (dev >= 0 && dev < 64) ? regs[dev] : 0;
     if (launch_regs * kFwdThreads < 256 * kSoftmaxRegs<D> + 128 * kControlRegs<D>)
         return cudaErrorLaunchOutOfResources;  // the register split would not fit
-    const int units = CAUSAL ? (p.n_items + 1) / 2 : p.n_items;  // pairs of items, or items (cta_item)
+    const int units = CAUSAL ? (p.n_items + 1) / 2 : p.n_items;  // pairs of items, or items
     const int grid = units < p.num_ctas ? units : p.num_ctas;
-    kern<<<grid, kFwdThreads, C::kSmemBytes, st>>>(p);
+    FwdParams q = p;
+    const long long step = CAUSAL ? 2LL * grid - 1 : grid;  // see next_item
+    q.step_heads = static_cast<int>(step / p.n_qp);
+    q.step_rem = static_cast<int>(step % p.n_qp);
+    kern<<<grid, kFwdThreads, C::kSmemBytes, st>>>(q);
     return cudaGetLastError();
 }
 

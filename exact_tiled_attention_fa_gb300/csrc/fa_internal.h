@@ -29,6 +29,10 @@ struct FwdParams {
     int num_ctas;       // persistent CTAs (one per SM)
     float scale_log2;   // scale * log2(e)
     unsigned long long wait_limit_ns;
+    // set by the launcher from its grid size G: the step between a CTA's item rounds (G items
+    // without a causal mask, 2G - 1 from the second item of a pair under one) as whole heads
+    // and a remainder, so that the kernel advances (head, position) without a division
+    int step_heads, step_rem;
 };
 
 // Launch the forward kernel for head size d (= dv), causal flag and output type.

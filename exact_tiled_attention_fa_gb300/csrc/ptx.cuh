@@ -364,6 +364,15 @@ __device__ __forceinline__ void regs_decrease()
 // math
 // ---------------------------------------------------------------------------
 // Hardware base-2 exponential (MUFU); exp2(-inf) = +0.
+// Base-2 logarithm, hardware approximation (MUFU), for x >= 1 where its absolute error is
+// far below what a log-sum-exp needs.
+__device__ __forceinline__ float lg2_approx(float x)
+{
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float ex2(float x)
 {
     float y;
