@@ -183,11 +183,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
     struct Item {
         int bh, j0, i_first, n;
     };
-    auto item_at = [&](int x) -> Item {
+    // CTA c walks items c, c + G, c + 2G, ...; the cursor keeps each item's head, its key tile
+    // before the rotation and the rotation (head mod Tc) up to date by additions, as the per-item
+    // bookkeeping otherwise costs divisions on warps that share issue slots with busy ones.
+    struct Cursor {
+        int x, bh, jr, rot;
+    };
+    auto first_item = [&]() -> Cursor {
+        Cursor c;
+        c.x = blockIdx.x;
+        c.bh = c.x / p.Tc;
+        c.jr = c.x - c.bh * p.Tc;
+        c.rot = c.bh % p.Tc;
+        return c;
+    };
+    auto next_item = [&](Cursor& c) {
+        c.x += gridDim.x;
+        c.bh += p.step_heads;
+        c.jr += p.step_jr;
+        c.rot += p.step_rot;
+        if (c.jr >= p.Tc) {
+            c.jr -= p.Tc;
+            c.bh += 1;
+            c.rot += 1;
+        }
+        if (c.rot >= p.Tc) c.rot -= p.Tc;
+    };
+    auto item_at = [&](const Cursor& c) -> Item {
         Item it;
-        it.bh = x / p.Tc;
-        const int jr = x - it.bh * p.Tc;
-        const int j = CAUSAL ? (jr + it.bh) % p.Tc : jr;
+        it.bh = c.bh;
+        int j = c.jr;
+        if (CAUSAL) {
+            j += c.rot;  // (jr + bh) mod Tc
+            if (j >= p.Tc) j -= p.Tc;
+        }
         it.j0 = j * kBlockN;
         it.i_first = 0;
         if (CAUSAL) {
@@ -262,8 +291,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             int g = 0;        // query tiles loaded (Q ring position)
             int kv = 0;       // items whose K/V were loaded
             bool ok = true;
-            for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
-                const Item it = item_at(x);
+            for (Cursor cur = first_item(); ok && cur.x < n_items; next_item(cur)) {
+                const Item it = item_at(cur);
                 if (it.n == 0) continue;  // no query tile sees this key tile (every role skips it)
                 const int kb = kv % KVB;
                 if (kv >= KVB && !mbar_wait(bar(kBbKVEmpty + kb), static_cast<uint32_t>(kv / KVB - 1) & 1, limit, abort_flag)) {
@@ -360,8 +389,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
             };
             int g = 0;  // query tiles processed (all items)
             int k = 0;  // items processed
-            for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
-                const Item it = item_at(x);
+            for (Cursor cur = first_item(); ok && cur.x < n_items; next_item(cur)) {
+                const Item it = item_at(cur);
                 if (it.n == 0) continue;
                 const int kb = k % KVB;
                 const int k_off = C::kOffK + kb * C::kTileBytes;
@@ -423,8 +452,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         const uint32_t t_dq = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kColDQ;
         bool ok = true;
         int g = 0;
-        for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
-            const Item it = item_at(x);
+        for (Cursor cur = first_item(); ok && cur.x < n_items; next_item(cur)) {
+            const Item it = item_at(cur);
             for (int t = 0; t < it.n; ++t, ++g) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDQFull), g & 1, limit, abort_flag));
                 if (!ok) break;
@@ -466,8 +495,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         int k = 0;
         int staged = 0;            // items whose dK, dV went out through the staging tiles
         bool stage_busy = false;   // the last of those stores may still be reading the dS buffer
-        for (int x = blockIdx.x; ok && x < n_items; x += gridDim.x) {
-            const Item it = item_at(x);
+        for (Cursor cur = first_item(); ok && cur.x < n_items; next_item(cur)) {
+            const Item it = item_at(cur);
             const int key = it.j0 + kr;
             const bool valid = key < p.Nk;
             const size_t row = (static_cast<size_t>(it.bh) * p.Nk + (valid ? key : 0)) * D + h * (D / 2);
@@ -700,7 +729,11 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t st)
     const long long items = static_cast<long long>(p.BH) * p.Tc;
     if (items <= 0) return cudaSuccess;
     const long long grid = items < p.num_ctas ? items : p.num_ctas;  // persistent: one CTA per SM
-    kern<<<static_cast<unsigned>(grid), kBwdThreads, C::kSmemBytes, st>>>(p);
+    BwdParams q = p;  // the cursor's steps (see first_item / next_item)
+    q.step_heads = static_cast<int>(grid / p.Tc);
+    q.step_jr = static_cast<int>(grid % p.Tc);
+    q.step_rot = q.step_heads % p.Tc;
+    kern<<<static_cast<unsigned>(grid), kBwdThreads, C::kSmemBytes, st>>>(q);
     return cudaGetLastError();
 }
 

@@ -59,6 +59,9 @@ struct BwdParams {
     float scale_log2;   // scale * log2(e)
     float scale;
     unsigned long long wait_limit_ns;
+    // set by the launcher from its grid size G: G = step_heads * Tc + step_jr, and step_heads mod Tc
+    // (the causal rotation), so that the kernel advances its items without a division
+    int step_heads, step_jr, step_rot;
 };
 
 struct BwdPrepParams {
