@@ -194,7 +194,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
         return FA_ERR_INVALID_ARG;
     const long long BH = static_cast<long long>(B) * H;
     const long long n_qp = (static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
-    if (BH * n_qp > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    // the kernels index items with 32-bit ints and step past the last one by up to 2 * SMs
+    if (BH * n_qp > 0x3fffffffLL) return FA_ERR_INVALID_ARG;
     if (!head_ok(d) || dv != d) return FA_ERR_UNSUPPORTED;
 
     fa::FwdParams p;
@@ -246,7 +247,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     const long long BH = static_cast<long long>(B) * H;
     const long long Tr = (static_cast<long long>(N) + fa::kBlockM - 1) / fa::kBlockM;
     const long long Tc = (static_cast<long long>(Nk) + fa::kBlockN - 1) / fa::kBlockN;
-    if (BH * Tc > 0x7fffffffLL || BH > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    if (BH * Tc > 0x3fffffffLL) return FA_ERR_INVALID_ARG;  // 32-bit item indices with headroom for the cursor's step
     if (!head_ok(d) || dv != d) return FA_ERR_UNSUPPORTED;
     if (ws_bytes < fa_bwd_workspace_size(B, H, N, d)) return FA_ERR_WORKSPACE;
 

@@ -82,7 +82,7 @@ typedef enum { FA_BF16 = 0, FA_F32 = 1 } fa_dtype;
  *   o    o_dtype [B, H, N, dv]     (device, written)
  *   lse  fp32 [B, H, N]            (device, written; may be NULL to skip it)
  *   B, H, N, Nk >= 1; d = dv in {32, 64, 128}; causal 0 or 1; scale > 0 and finite
- *   (1/sqrt(d) is the usual value).
+ *   (1/sqrt(d) is the usual value); B*H*ceil(N/256) < 2^30 (else FA_ERR_INVALID_ARG).
  * Returns FA_OK after enqueueing the kernel on `stream`.
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -113,7 +113,7 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   workspace    device scratch of ws_bytes >= fa_bwd_workspace_size(B, H, N, d) bytes,
  *                256-byte aligned; its contents on entry do not matter.
  *   B, H, N, Nk >= 1; d = dv in {32, 64, 128}; causal 0 or 1; scale > 0 and finite, the
- *   value the forward used.
+ *   value the forward used; B*H*ceil(Nk/128) < 2^30 (else FA_ERR_INVALID_ARG).
  * Three kernels are enqueued on `stream`: a preparation pass (D, lse in base 2, zeroing the
  * dQ accumulator), the tensor-core pass (a persistent grid, one CTA per SM, walking the
  * (b, h, 128-key tile) items; each item's dK and dV written when its walk ends, dQ added into
