@@ -138,9 +138,10 @@ bool make_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d)
 }
 
 // Output tensor [BH][rows][d] of bf16 or fp32 as a 3-D tiled map for bulk stores: the box is
-// 128 rows of one column block (128 bytes of a row, or the whole 64-byte row of bf16 d = 32),
-// swizzled to match the staging tile the forward kernel writes.
-bool make_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t)
+// box_rows rows of one column block (128 bytes of a row, or the whole 64-byte row of bf16 d = 32),
+// swizzled to match the staging tiles the kernels write (the forward stores 32-row quarters, one
+// per warp; the backward whole 128-row tiles).
+bool make_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t, int box_rows)
 {
     auto enc = encode_fn();
     if (enc == nullptr) return false;
@@ -148,7 +149,7 @@ bool make_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t
     const int blk = d * es < 128 ? d : 128 / es;  // elements per box row
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * es, static_cast<cuuint64_t>(rows) * d * es};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(blk), static_cast<cuuint32_t>(fa::kBlockM), 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(blk), static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, t == FA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims,
                      strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -201,7 +202,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     fa::FwdParams p;
     if (!make_map(&p.tm_q, q, static_cast<int>(BH), N, d) || !make_map(&p.tm_k, k, static_cast<int>(BH), Nk, d) ||
         !make_map(&p.tm_v, v, static_cast<int>(BH), Nk, dv) ||
-        !make_out_map(&p.tm_o, o, static_cast<int>(BH), N, dv, o_dtype))
+        !make_out_map(&p.tm_o, o, static_cast<int>(BH), N, dv, o_dtype, 32))
         return FA_ERR_CUDA;
     int* status = nullptr;
     if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
@@ -278,8 +279,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     if (!make_map(&p.tm_q, q, static_cast<int>(BH), N, d) || !make_map(&p.tm_k, k, static_cast<int>(BH), Nk, d) ||
         !make_map(&p.tm_v, v, static_cast<int>(BH), Nk, dv) ||
         !make_map(&p.tm_do, grad_o, static_cast<int>(BH), N, dv) ||
-        !make_out_map(&p.tm_dk, grad_k, static_cast<int>(BH), Nk, d, grad_dtype) ||
-        !make_out_map(&p.tm_dv, grad_v, static_cast<int>(BH), Nk, dv, grad_dtype))
+        !make_out_map(&p.tm_dk, grad_k, static_cast<int>(BH), Nk, d, grad_dtype, fa::kBlockM) ||
+        !make_out_map(&p.tm_dv, grad_v, static_cast<int>(BH), Nk, dv, grad_dtype, fa::kBlockM))
         return FA_ERR_CUDA;
     p.lse2 = lse2;
     p.dsc = dsc;

@@ -88,9 +88,7 @@ enum : int {
     kBarSFree = 18,                         // +tile (2): the softmax has read S_i out of TMEM
     kBarKVFull = 20,                        // +stage: K_j and V_j landed
     kBarKVEmpty = kBarKVFull + kMaxStages,  // +stage: both issuers are done with the stage
-    kBarOStaged = kBarKVEmpty + kMaxStages,  // +tile (2): the warpgroup wrote its O rows to the staging tile
-    kBarOFree = kBarOStaged + 2,             // +tile (2): the previous bulk store has read the staging tile
-    kBarCount = kBarOFree + 2
+    kBarCount = kBarKVEmpty + kMaxStages
 };
 
 template <int D, int OutBytes>
@@ -303,10 +301,6 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(kBarKVFull + s), 1);
             mbar_init(bar(kBarKVEmpty + s), 2);  // one arrival from each MMA issuer
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(kBarOStaged + i), kBlockM);
-            mbar_init(bar(kBarOFree + i), 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
@@ -639,14 +633,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             if constexpr (C::kStoreO) {
                 using OS = OStage<OutT, D>;
                 const uint32_t stg = sbase + C::kOffStage + static_cast<uint32_t>(wg) * C::kStageTileBytes;
-                if (staged > 0) {  // the previous tile's bulk store must have read the staging tile
-                    if (r == 0) {
-                        bulk_wait_read_all();
-                        mbar_arrive(bar(kBarOFree + wg));
-                    }
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOFree + wg), (staged - 1) & 1, limit, abort_flag));
-                    if (!ok) break;
-                }
+                // Each warp stages its 32 rows and stores them itself (a 32-row box), so the epilogue
+                // needs no barrier across the warpgroup: lane 0 first waits until the warp's previous
+                // store has read its rows (issued one item ago, long done).
+                const int wq = warp & 3;
+                if (lane == 0 && staged > 0) bulk_wait_read_all();
+                __syncwarp();
                 uint32_t o[D];
                 if (n > 0) {
 #pragma unroll
@@ -658,18 +650,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 }
                 stage_row<OutT, D>(stg, r, o, inv);
                 fence_proxy_async_shared();
-                mbar_arrive(bar(kBarOStaged + wg));
-                if (r == 0) {  // one thread stores the tile; rows past N lie outside the map and are skipped
-                    ok = mbar_wait(bar(kBarOStaged + wg), staged & 1, limit, abort_flag);
-                    if (ok) {
+                __syncwarp();
+                if (lane == 0 && row0 + 32 * wq < p.N) {  // rows past N lie outside the map and are skipped
 #pragma unroll
-                        for (int cb = 0; cb < OS::kNumCB; ++cb)
-                            tma_store_3d(&p.tm_o, stg + cb * OS::kBlkBytes, cb * OS::kElems, row0, it.bh);
-                        bulk_commit_group();
-                    }
+                    for (int cb = 0; cb < OS::kNumCB; ++cb)
+                        tma_store_3d(&p.tm_o, stg + cb * OS::kBlkBytes + wq * 32 * OS::kRowBytes, cb * OS::kElems,
+                                     row0 + 32 * wq, it.bh);
+                    bulk_commit_group();
                 }
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
                 ++staged;
             } else {
                 OutT* orow = reinterpret_cast<OutT*>(p.o) + row * D;
@@ -693,7 +681,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 p.lse[row] = l > 0.f ? (m_run + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
         }
         // Bulk stores must finish before the CTA's shared memory goes away.
-        if (C::kStoreO && r == 0 && staged > 0) bulk_wait_all();
+        if (C::kStoreO && lane == 0 && staged > 0) bulk_wait_all();
         if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
     }
 

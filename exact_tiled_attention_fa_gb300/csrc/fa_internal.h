@@ -19,7 +19,7 @@ struct FwdParams {
     CUtensorMap tm_q;  // bf16 [B*H][N][d], box {min(d,64), 128, 1}
     CUtensorMap tm_k;  // bf16 [B*H][Nk][d]
     CUtensorMap tm_v;  // bf16 [B*H][Nk][dv]
-    CUtensorMap tm_o;  // O [B*H][N][dv] (bf16 or fp32), box {128 bytes of a row (64 for bf16 d = 32), 128, 1}
+    CUtensorMap tm_o;  // O [B*H][N][dv] (bf16 or fp32), box {128 bytes of a row (64 for bf16 d = 32), 32, 1}
     void* o;           // [B*H][N][dv], bf16 or fp32
     float* lse;        // [B*H][N] or nullptr
     int* status;       // device status word
