@@ -199,7 +199,8 @@ struct Item {
 // items of a pair together carry about the same work as any other pair and the static
 // assignment stays balanced without a global work counter.  Without a mask every item
 // carries the same work and CTA c takes items c, c + G, c + 2G, ...: the last round is then
-// one item, not one pair, short (B=64 H=16 N=1024: 27 items on the busiest CTA instead of 28).
+// one item, not one pair, short (B=64 H=16 N=1024: 27 items on the busiest CTA instead of 28);
+// so does a causal launch with no more items than CTAs (each item then has a CTA of its own).
 // This CTA's items in that order, with each item's head and position in the head
 // advanced by additions: the per-item bookkeeping runs on warps that share their issue slots
 // with exponentiating warps, where a 32-bit division and 64-bit index arithmetic cost hundreds
@@ -208,23 +209,24 @@ struct ItemCursor {
     int item, bh, t, k;
 };
 
-__device__ __forceinline__ ItemCursor first_item(const FwdParams& p, bool causal)
+// `pairs` is the launch's FwdParams::pairs, passed as false by non-causal kernels (never paired).
+__device__ __forceinline__ ItemCursor first_item(const FwdParams& p, bool pairs)
 {
     ItemCursor c;
-    c.item = causal ? 2 * static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+    c.item = pairs ? 2 * static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
     c.bh = c.item / p.n_qp;
     c.t = c.item - c.bh * p.n_qp;
     c.k = 0;
     return c;
 }
 
-__device__ __forceinline__ void next_item(const FwdParams& p, ItemCursor& c, bool causal)
+__device__ __forceinline__ void next_item(const FwdParams& p, ItemCursor& c, bool pairs)
 {
-    if (causal && (c.k & 1) == 0) {  // second item of the pair
+    if (pairs && (c.k & 1) == 0) {  // second item of the pair
         c.item += 1;
         c.t += 1;
     } else {                         // first item of the next round
-        c.item += causal ? 2 * static_cast<int>(gridDim.x) - 1 : static_cast<int>(gridDim.x);
+        c.item += pairs ? 2 * static_cast<int>(gridDim.x) - 1 : static_cast<int>(gridDim.x);
         c.bh += p.step_heads;
         c.t += p.step_rem;
     }
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             int q_loads[2] = {0, 0};  // loads issued into each Q buffer
             long long g = 0;          // K/V tiles issued so far (ring position)
             bool ok = true;
-            for (ItemCursor cur = first_item(p, CAUSAL); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL)) {
+            for (ItemCursor cur = first_item(p, CAUSAL && p.pairs); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs)) {
                 const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (it.n[i] == 0) continue;
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                 return true;
             };
 
-            for (ItemCursor cur = first_item(p, CAUSAL); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL)) {
+            for (ItemCursor cur = first_item(p, CAUSAL && p.pairs); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs)) {
                 const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
                 const int n = i ? it.n[1] : it.n[0];
                 const int q_bar = 2 * (q_uses % C::kQBuf) + i;
@@ -509,7 +511,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         int staged = 0;  // output tiles this warpgroup wrote through the staging tile
         bool ok = true;
 
-        for (ItemCursor cur = first_item(p, CAUSAL); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL)) {
+        for (ItemCursor cur = first_item(p, CAUSAL && p.pairs); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs)) {
             const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
             const int n = wg ? it.n[1] : it.n[0];
             const int rows = wg ? it.rows[1] : it.rows[0];
@@ -718,10 +720,13 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
     const int launch_regs = (dev >= 0 && dev < 64) ? regs[dev] : 0;
     if (launch_regs * kFwdThreads < 256 * kSoftmaxRegs<D> + 128 * kControlRegs<D>)
         return cudaErrorLaunchOutOfResources;  // the register split would not fit
-    const int units = CAUSAL ? (p.n_items + 1) / 2 : p.n_items;  // pairs of items, or items
-    const int grid = units < p.num_ctas ? units : p.num_ctas;
     FwdParams q = p;
-    const long long step = CAUSAL ? 2LL * grid - 1 : grid;  // see next_item
+    // Pairs balance causal work over several rounds; with no more items than CTAs every item gets
+    // a CTA of its own.
+    q.pairs = (CAUSAL && p.n_items > p.num_ctas) ? 1 : 0;
+    const int units = q.pairs ? (p.n_items + 1) / 2 : p.n_items;  // pairs of items, or items
+    const int grid = units < p.num_ctas ? units : p.num_ctas;
+    const long long step = q.pairs ? 2LL * grid - 1 : grid;  // see next_item
     q.step_heads = static_cast<int>(step / p.n_qp);
     q.step_rem = static_cast<int>(step % p.n_qp);
     kern<<<grid, kFwdThreads, C::kSmemBytes, st>>>(q);

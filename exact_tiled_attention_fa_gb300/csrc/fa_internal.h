@@ -33,6 +33,7 @@ struct FwdParams {
     // without a causal mask, 2G - 1 from the second item of a pair under one) as whole heads
     // and a remainder, so that the kernel advances (head, position) without a division
     int step_heads, step_rem;
+    int pairs;          // items go out in heavy/light pairs (causal, more items than CTAs) or singly
 };
 
 // Launch the forward kernel for head size d (= dv), causal flag and output type.
