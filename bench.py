@@ -552,10 +552,9 @@ def run_decode_gqa(fa, dev, stream, args, world, Hkv=None):
     Hkv = GQA["Hkv"] if Hkv is None else Hkv
     q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=GQA["lo"], hi=GQA["hi"], device=dev)
     lens_d = lens.to(dev)
-    n = 0  # the library's automatic split count; the workspace covers either heuristic
-    sms = fa.num_sms(dev)
-    n_ws = max(fa.decode_default_splits(B, Hq, Nk_max, sms), min(-(-6 * sms // (B * Hkv)), -(-Nk_max // 128)))
-    ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n_ws), dtype=torch.uint8, device=dev)
+    n = 0  # the library's automatic split count
+    n_auto = fa.decode_gqa_default_splits(B, Hq, Hkv, Nk_max, fa.num_sms(dev))
+    ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n_auto), dtype=torch.uint8, device=dev)
     o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
     for _ in range(max(args.warmup, 3)):
@@ -577,7 +576,7 @@ def run_decode_gqa(fa, dev, stream, args, world, Hkv=None):
     pk, src = peaks()
     gbs = world * (kv_bytes + other) / (ms / 1e3) / 1e9
     return {"workload": f"GQA split-KV decode B={B} Hq={Hq} Hkv={Hkv} d={d}, lengths U[1024,32768] (seed 0), bf16 O",
-            "group": Hq // Hkv, "unit": "tensor core" if Hq // Hkv not in (1, 2, 4) else "CUDA cores", "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
+            "group": Hq // Hkv, "n_splits": n_auto, "unit": "tensor core" if Hq // Hkv not in (1, 2, 4) else "CUDA cores", "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
             "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2}
 
 

@@ -13,7 +13,7 @@ Entry points (same names as the C ABI, without the ``fa_`` prefix):
   decode_splitkv_gqa  the same with grouped key/value heads (query heads of a group packed)
   decode_splitkv_fused  the same with the combine done by each row's last split (one launch)
   merge_states     log-sum-exp combine of partial states
-  decode_default_splits, decode_workspace_size, get_device_error,
+  decode_default_splits, decode_gqa_default_splits, decode_workspace_size, get_device_error,
   set_wait_timeout_ns, status_string
 """
 from __future__ import annotations
@@ -57,6 +57,8 @@ def _load():
     lib.fa_bwd.restype = i
     lib.fa_decode_default_splits.argtypes = [i, i, i, i]
     lib.fa_decode_default_splits.restype = i
+    lib.fa_decode_gqa_default_splits.argtypes = [i, i, i, i, i]
+    lib.fa_decode_gqa_default_splits.restype = i
     lib.fa_decode_workspace_size.argtypes = [i, i, i, i]
     lib.fa_decode_workspace_size.restype = sz
     lib.fa_decode_splitkv.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, i, vp]
@@ -251,6 +253,10 @@ def decode_default_splits(B, H, Nk_max, num_sms):
     return int(_load().fa_decode_default_splits(B, H, Nk_max, num_sms))
 
 
+def decode_gqa_default_splits(B, Hq, Hkv, Nk_max, num_sms):
+    return int(_load().fa_decode_gqa_default_splits(B, Hq, Hkv, Nk_max, num_sms))
+
+
 def decode_workspace_size(B, H, dv, n_splits):
     return int(_load().fa_decode_workspace_size(B, H, dv, n_splits))
 
@@ -320,11 +326,8 @@ def decode_splitkv_gqa(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out
             or seqlens.numel() != B):
         raise ValueError("shape mismatch between q, caches and seqlens")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
-    if n_splits:
-        n = int(n_splits)
-    else:  # the larger of the two automatic counts (CUDA-core and tensor-core groups)
-        sms = num_sms(dev)
-        n = max(decode_default_splits(B, Hq, Nk_max, sms), min(-(-6 * sms // (B * Hkv)), -(-Nk_max // 128)))
+    # (0 for groups the library rejects; the call below then reports why)
+    n = int(n_splits) if n_splits else decode_gqa_default_splits(B, Hq, Hkv, Nk_max, num_sms(dev))
     if workspace is None:
         workspace = torch.empty(max(decode_workspace_size(B, Hq, dv, max(1, min(n, Nk_max))), 256),
                                 dtype=torch.uint8, device=dev)

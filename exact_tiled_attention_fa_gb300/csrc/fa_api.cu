@@ -364,10 +364,17 @@ cudaError_t merge_rows(const float* o_part, const float* lse_part, int rows, int
 // the tensor core, 8 heads per group 1.2 vs 3.5 TB/s.
 bool gqa_on_cuda_cores(int R) { return R == 1 || R == 2 || R == 4; }
 
+// Tensor-core groups: one CTA (a whole SM) per (b, key/value head, split).  The CTA's time goes
+// to the per-tile softmax chain, not to the bytes, so the count aims at about 1.7 CTAs per SM
+// (the lengths vary, and many of the later splits are short or empty): measured on GB300, d = 128,
+// 32 or 64 query heads, this is within a few per cent of the best count swept for groups of 8,
+// 16 and 32 heads and 4-64 sequences, and 25-70 % above six CTAs per SM for 16- and 32-head groups.
+// At least two splits while the groups alone leave SMs idle; each split at least one 128-key tile.
 int gqa_tc_default_splits(int B, int Hkv, int Nk_max, int sms)
 {
     const long long groups = static_cast<long long>(B) * Hkv;
-    long long n = (6LL * sms + groups - 1) / groups;
+    long long n = 17LL * sms / (10LL * groups);
+    if (n < 2 && groups < 2LL * sms) n = 2;
     const long long max_n = (static_cast<long long>(Nk_max) + fa::kBlockN - 1) / fa::kBlockN;
     if (n > max_n) n = max_n;
     if (n < 1) n = 1;
@@ -397,11 +404,7 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
     if (n == 0) {
         int sms = 0;
         if (sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
-        // one CTA per (b, key/value head, split).  On CUDA cores a CTA's arithmetic grows with
-        // the R heads it carries, so the count follows the B * Hq query heads (R = 4: 4.3 -> 4.8
-        // TB/s against counting B * Hkv items); a tensor-core CTA holds a whole SM, so its splits
-        // are longer (about six per SM in total, each at least one 128-key tile)
-        n = tc ? gqa_tc_default_splits(B, Hkv, Nk_max, sms) : fa_decode_default_splits(B, Hq, Nk_max, sms);
+        n = fa_decode_gqa_default_splits(B, Hq, Hkv, Nk_max, sms);
     }
     if (n > Nk_max) n = Nk_max;
     const size_t part_bytes = fa_decode_workspace_size(B, Hq, dv, n);
@@ -477,6 +480,15 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
 
 extern "C" {
 
+int fa_decode_gqa_default_splits(int B, int Hq, int Hkv, int Nk_max, int num_sms)
+{
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nk_max <= 0 || num_sms <= 0 || Hq % Hkv != 0) return 0;
+    // On CUDA cores a CTA's arithmetic grows with the R heads it carries, so the count follows the
+    // B * Hq query heads (R = 4: 4.3 -> 4.8 TB/s against counting B * Hkv items).
+    return gqa_on_cuda_cores(Hq / Hkv) ? fa_decode_default_splits(B, Hq, Nk_max, num_sms)
+                                       : gqa_tc_default_splits(B, Hkv, Nk_max, num_sms);
+}
+
 fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,
                             float* lse, void* workspace, size_t ws_bytes, int B, int H, int Nk_max, int d, int dv,
                             float scale, int n_splits, fa_dtype o_dtype, void* stream)
@@ -488,10 +500,15 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
 int fa_fwd_splitkv_default_splits(int B, int H, int N, int Nk, int num_sms)
 {
     if (B <= 0 || H <= 0 || N <= 0 || Nk <= 0 || num_sms <= 0) return 0;
-    // Enough (head, query tile, split) CTAs for two per SM, each split at least one key tile.
+    // The split kernel holds an SM per CTA, and a CTA costs about six key tiles beyond its own
+    // (set-up, pipeline fill, partial write, its share of the merge), so a second wave of shorter
+    // splits loses to one wave of longer ones: the count is the largest for which every (head,
+    // query tile, split) CTA runs at once, each split at least one 128-key tile.  Measured on
+    // GB300 over five shapes (d = 64 and 128, causal and not, 4-64 query tiles), this was the best
+    // count swept in each (B=1 H=8 N=512 Nk=32K d=128 causal: 4 splits 557 TFLOP/s, 10 splits 462).
     const long long tiles = static_cast<long long>(B) * H * ((N + fa::kBlockM - 1) / fa::kBlockM);
     const long long max_n = (static_cast<long long>(Nk) + fa::kBlockN - 1) / fa::kBlockN;
-    long long n = (2LL * num_sms + tiles - 1) / tiles;
+    long long n = num_sms / tiles;
     if (n > max_n) n = max_n;
     if (n < 1) n = 1;
     return static_cast<int>(n);

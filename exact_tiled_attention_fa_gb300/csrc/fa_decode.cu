@@ -270,12 +270,14 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* o, size_
     o[i] = __float2bfloat16_rn(v);
 }
 
-constexpr int kMergeMaxPerLane = 16;  // dv <= 512
-
-// One warp per row: combine the row's valid parts.
-template <typename OutT>
+// One warp per row: combine the row's valid parts.  Lane l holds columns VEC * (l + 32 i),
+// i < IT (VEC = 4: float4 loads; IT * 128 >= dv).  The parts are added in increasing order,
+// one FMA per part and column, but the loads of U parts are issued together, so a row with
+// many parts pays about one memory latency per U parts instead of one per part.
+template <typename OutT, int VEC, int IT>
 __global__ void __launch_bounds__(128) fa_merge_kernel(const MergeParams p)
 {
+    constexpr int U = IT >= 8 ? 1 : 8 / IT;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + warp;
@@ -307,26 +309,93 @@ __global__ void __launch_bounds__(128) fa_merge_kernel(const MergeParams p)
     for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     const float L = M + log2f(sum) * kLn2;
 
-    float acc[kMergeMaxPerLane];
+    float acc[IT][VEC];
 #pragma unroll
-    for (int i = 0; i < kMergeMaxPerLane; ++i) acc[i] = 0.f;
-    for (int s = 0; s < n_valid; ++s) {
-        const float x = lse_row[s * p.lse_part_stride];
-        if (x == -INFINITY) continue;
-        const float w = ex2((x - L) * kLog2e);
-        const float* op = o_row + static_cast<size_t>(s) * p.o_part_stride;
+    for (int i = 0; i < IT; ++i)
 #pragma unroll
-        for (int i = 0; i < kMergeMaxPerLane; ++i) {
-            const int c = lane + 32 * i;
-            if (c < p.dv) acc[i] = fmaf(w, op[c], acc[i]);
+        for (int e = 0; e < VEC; ++e) acc[i][e] = 0.f;
+    for (int base = 0; base < n_valid; base += 32) {
+        // lane l weighs part base + l; the warp walks the non-empty ones in order
+        const int s = base + lane;
+        const float x = s < n_valid ? lse_row[s * p.lse_part_stride] : -INFINITY;
+        const float w_lane = x == -INFINITY ? 0.f : ex2((x - L) * kLog2e);
+        unsigned live = __ballot_sync(0xffffffffu, x != -INFINITY);
+        while (live != 0u) {
+            // U parts per batch; slots past the last live part re-read the batch's first part
+            // (finite: it was written) with weight 0, so every load is unconditional and in flight
+            // together, and fmaf(0, v, acc) leaves acc as it was
+            const int j0 = __ffs(live) - 1;
+            float w[U];
+            const float* op[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = live != 0u ? __ffs(live) - 1 : j0;
+                const float wj = __shfl_sync(0xffffffffu, w_lane, j);
+                w[u] = live != 0u ? wj : 0.f;
+                op[u] = o_row + static_cast<long long>(base + j) * p.o_part_stride;
+                live &= live - 1u;
+            }
+            if constexpr (VEC == 4) {
+                // U * IT = 8 float4 loads per lane, issued by one statement
+                static_assert(U * IT == 8, "eight loads per batch");
+                const void* a[8];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int i = 0; i < IT; ++i) {
+                        const int c = 4 * (lane + 32 * i);
+                        a[u * IT + i] = op[u] + (c < p.dv ? c : 0);  // columns past dv: read, never stored
+                    }
+                uint32_t v[32];
+                ld_stream_v4x8(a, v);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int i = 0; i < IT; ++i)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int k = (u * IT + i) * 4 + e;
+                            acc[i][e] = fmaf(w[u], __uint_as_float(v[k]), acc[i][e]);
+                        }
+            } else {
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int i = 0; i < IT; ++i) {
+                        const int c = lane + 32 * i;
+                        const float x = __ldg(op[u] + (c < p.dv ? c : 0));
+                        acc[i][0] = fmaf(w[u], x, acc[i][0]);
+                    }
+            }
         }
     }
 #pragma unroll
-    for (int i = 0; i < kMergeMaxPerLane; ++i) {
-        const int c = lane + 32 * i;
-        if (c < p.dv) store_out<OutT>(out, c, acc[i]);
+    for (int i = 0; i < IT; ++i) {
+        const int c = VEC * (lane + 32 * i);
+        if (c < p.dv) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) store_out<OutT>(out, c + e, acc[i][e]);
+        }
     }
     if (p.lse != nullptr && lane == 0) p.lse[row] = L;
+}
+
+template <typename OutT>
+cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t st)
+{
+    const unsigned grid = static_cast<unsigned>((p.rows + 3) / 4);
+    // float4 loads when every part row starts on 16 bytes (dv <= 512)
+    const bool vec4 = p.dv % 4 == 0 && p.o_part_stride % 4 == 0 && p.o_row_stride % 4 == 0 &&
+                      (reinterpret_cast<uintptr_t>(p.o_parts) & 15u) == 0;
+    if (!vec4)
+        fa_merge_kernel<OutT, 1, 16><<<grid, 128, 0, st>>>(p);
+    else if (p.dv <= 128)
+        fa_merge_kernel<OutT, 4, 1><<<grid, 128, 0, st>>>(p);
+    else if (p.dv <= 256)
+        fa_merge_kernel<OutT, 4, 2><<<grid, 128, 0, st>>>(p);
+    else
+        fa_merge_kernel<OutT, 4, 4><<<grid, 128, 0, st>>>(p);
+    return cudaGetLastError();
 }
 
 template <int D>
@@ -371,12 +440,8 @@ cudaError_t launch_decode_d(const DecodeParams& p, fa_dtype o_dtype, cudaStream_
 
 cudaError_t launch_merge(const MergeParams& p, fa_dtype o_dtype, cudaStream_t st)
 {
-    const unsigned grid = static_cast<unsigned>((p.rows + 3) / 4);
-    if (o_dtype == FA_F32)
-        fa_merge_kernel<float><<<grid, 128, 0, st>>>(p);
-    else
-        fa_merge_kernel<__nv_bfloat16><<<grid, 128, 0, st>>>(p);
-    return cudaGetLastError();
+    if (p.dv <= 0 || p.dv > 512) return cudaErrorInvalidValue;
+    return o_dtype == FA_F32 ? launch_merge_t<float>(p, st) : launch_merge_t<__nv_bfloat16>(p, st);
 }
 
 cudaError_t launch_decode(const DecodeParams& p, int d, fa_dtype o_dtype, cudaStream_t st)

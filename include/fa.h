@@ -169,6 +169,16 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
                             int n_splits, fa_dtype o_dtype, void* stream);
 
 /*
+ * Split count fa_decode_splitkv_gqa uses when asked for n_splits = 0, for Hq query heads over Hkv
+ * key/value heads on a device with `num_sms` multiprocessors.  Groups of R = Hq / Hkv = 1, 2 or
+ * 4 heads (CUDA cores) take fa_decode_default_splits(B, Hq, Nk_max, num_sms).  Other groups
+ * (tensor core, one CTA per multiprocessor) take floor(1.7 * num_sms / (B * Hkv)) splits, raised
+ * to 2 while B * Hkv < 2 * num_sms, then clamped to [1, ceil(Nk_max / 128)].  Pure host
+ * function.  Returns 0 on invalid arguments (a non-positive size, or Hkv not dividing Hq).
+ */
+int fa_decode_gqa_default_splits(int B, int Hq, int Hkv, int Nk_max, int num_sms);
+
+/*
  * Split-KV decode with grouped key/value heads (GQA): Hq query heads share Hkv key/value heads,
  * query head h reading key/value head h / R with R = Hq / Hkv.  The R query heads of a group are
  * packed together ("flash_lab.py" section 4 `split_kv_decode`, q of shape [R, d]; section 4
@@ -182,9 +192,8 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
  *   o          o_dtype [B, Hq, 1, dv]      (device, written)
  *   lse        fp32 [B, Hq, 1]             (device, written; may be NULL)
  *   workspace  ws_bytes >= fa_decode_workspace_size(B, Hq, dv, n) bytes, where n is n_splits or,
- *              for n_splits = 0, fa_decode_default_splits(B, Hq, Nk_max, <SMs of the device>) for
- *              groups of 1, 2 or 4 heads and min(ceil(6 * SMs / (B * Hkv)), ceil(Nk_max / 128)) for
- *              other group sizes (fa_decode_workspace_size of the larger of the two always suffices).
+ *              for n_splits = 0, fa_decode_gqa_default_splits(B, Hq, Hkv, Nk_max, <SMs of the
+ *              device>).
  *   Hkv >= 1 dividing Hq, R = Hq / Hkv <= 128 (larger groups return FA_ERR_UNSUPPORTED).
  *   Hkv = Hq is fa_decode_splitkv.  Groups of 1, 2 or 4 heads run on CUDA cores; other group
  *   sizes on the tensor core, where the R query rows are the rows of a 128-row tile, splits are
@@ -221,8 +230,9 @@ fa_status fa_decode_splitkv_fused(const void* q, const void* k_cache, const void
 
 /*
  * Split count fa_fwd_splitkv uses for n_splits = 0 on a device with `num_sms` multiprocessors:
- * enough (head, query tile, split) work items for two per multiprocessor, each split at least
- * one 128-key tile.  Pure host function; 0 on invalid arguments.
+ * the largest count for which the B*H*ceil(N/128) query tiles times the splits fit one CTA per
+ * multiprocessor (one wave), at least 1 and at most ceil(Nk/128) (each split at least one
+ * 128-key tile).  Pure host function; 0 on invalid arguments.
  */
 int fa_fwd_splitkv_default_splits(int B, int H, int N, int Nk, int num_sms);
 

@@ -103,6 +103,11 @@ def test_fwd_splitkv_rejects_bad_arguments(lib):
     ds = lib.fa_fwd_splitkv_default_splits
     assert ds(1, 1, 1, 100000, 152) >= 2 and ds(64, 16, 1024, 1024, 152) == 1
     assert 1 <= ds(8, 8, 77, 513, 152) <= 5
+    # one wave: the most splits for which query tiles x splits fit one CTA per SM
+    assert ds(1, 8, 512, 32768, 152) == 4 and ds(1, 4, 128, 131072, 152) == 38 and ds(2, 8, 384, 16384, 152) == 3
+    for (B, H, N, Nk) in ((1, 8, 512, 32768), (1, 3, 200, 50000), (2, 5, 129, 9000), (1, 1, 64, 1000)):
+        tiles, n = B * H * -(-N // 128), ds(B, H, N, Nk, 152)
+        assert n == min(max(1, 152 // tiles), -(-Nk // 128))
 
 
 def test_merge_rejects_bad_arguments(lib):
@@ -126,6 +131,19 @@ def test_workspace_and_split_heuristic(lib):
         assert 1 <= n <= max(1, -(-Nk // 256))
     # more SMs never means fewer splits
     assert ds(4, 8, 32768, 152) >= ds(4, 8, 32768, 76)
+
+
+def test_gqa_split_heuristic(lib):
+    g, ds = lib.fa_decode_gqa_default_splits, lib.fa_decode_default_splits
+    assert g(0, 32, 8, 1024, 152) == 0 and g(1, 6, 4, 1024, 152) == 0 and g(1, 8, 8, 1024, 0) == 0
+    # groups of 1, 2 and 4 heads (CUDA cores) follow the B * Hq query heads
+    for (B, Hq, Hkv) in ((16, 32, 8), (16, 32, 16), (16, 32, 32), (3, 8, 2)):
+        assert g(B, Hq, Hkv, 32768, 152) == ds(B, Hq, 32768, 152)
+    # other groups (tensor core): floor(1.7 * SMs / (B * Hkv)), at least 2 while the groups leave
+    # SMs idle, clamped to [1, ceil(Nk_max / 128)]
+    assert g(16, 32, 4, 32768, 152) == 4 and g(16, 32, 2, 32768, 152) == 8 and g(16, 32, 1, 32768, 152) == 16
+    assert g(64, 32, 4, 4096, 152) == 2 and g(1000, 32, 4, 4096, 152) == 1
+    assert g(4, 32, 1, 256, 152) == 2 and g(1, 128, 1, 100, 152) == 1
 
 
 def test_status_strings(lib):
