@@ -270,6 +270,26 @@ __device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* o, size_
     o[i] = __float2bfloat16_rn(v);
 }
 
+// Eight streaming 16-byte global loads in one statement: all 32 results are defined together,
+// so the eight requests are issued back to back and are in flight at once.
+__device__ __forceinline__ void ld_stream_v4x8(const void* const (&p)[8], uint32_t (&r)[32])
+{
+    asm volatile(
+        "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%32];\n\t"
+        "ld.global.nc.L1::no_allocate.v4.u32 {%4, %5, %6, %7}, [%33];\n\t"
+        "ld.global.nc.L1::no_allocate.v4.u32 {%8, %9, %10, %11}, [%34];\n\t"
+        "ld.global.nc.L1::no_allocate.v4.u32 {%12, %13, %14, %15}, [%35];\n\t"
+        "ld.global.nc.L1::no_allocate.v4.u32 {%16, %17, %18, %19}, [%36];\n\t"
+        "ld.global.nc.L1::no_allocate.v4.u32 {%20, %21, %22, %23}, [%37];\n\t"
+        "ld.global.nc.L1::no_allocate.v4.u32 {%24, %25, %26, %27}, [%38];\n\t"
+        "ld.global.nc.L1::no_allocate.v4.u32 {%28, %29, %30, %31}, [%39];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "l"(p[0]), "l"(p[1]), "l"(p[2]), "l"(p[3]), "l"(p[4]), "l"(p[5]), "l"(p[6]), "l"(p[7]));
+}
+
 // One warp per row: combine the row's valid parts.  Lane l holds columns VEC * (l + 32 i),
 // i < IT (VEC = 4: float4 loads; IT * 128 >= dv).  The parts are added in increasing order,
 // one FMA per part and column, but the loads of U parts are issued together, so a row with
