@@ -57,6 +57,158 @@ struct DecCfg {
     static constexpr int kKeysPerIter = kSteps * kKeysPerStep;    // keys per warp per iteration
 };
 
+template <typename OutT>
+__device__ __forceinline__ void store_out(OutT* o, size_t i, float v);
+template <>
+__device__ __forceinline__ void store_out<float>(float* o, size_t i, float v)
+{
+    o[i] = v;
+}
+template <>
+__device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* o, size_t i, float v)
+{
+    o[i] = __float2bfloat16_rn(v);
+}
+
+// Eight 16-byte global loads in one statement: all 32 results are defined together, so the
+// eight requests are issued back to back and are in flight at once.
+#define FA_LD_V4X8(OP)                                                                                            \
+    asm volatile(OP " {%0, %1, %2, %3}, [%32];\n\t" OP " {%4, %5, %6, %7}, [%33];\n\t" OP                     \
+                    " {%8, %9, %10, %11}, [%34];\n\t" OP " {%12, %13, %14, %15}, [%35];\n\t" OP                 \
+                    " {%16, %17, %18, %19}, [%36];\n\t" OP " {%20, %21, %22, %23}, [%37];\n\t" OP               \
+                    " {%24, %25, %26, %27}, [%38];\n\t" OP " {%28, %29, %30, %31}, [%39];"                      \
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),         \
+                   "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),      \
+                   "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),   \
+                   "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),   \
+                   "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])                                           \
+                 : "l"(p[0]), "l"(p[1]), "l"(p[2]), "l"(p[3]), "l"(p[4]), "l"(p[5]), "l"(p[6]), "l"(p[7]))
+
+// kL2: read at L2 (`ld.global.cg`: partial states that other CTAs of the running kernel wrote);
+// otherwise through the non-coherent path without L1 allocation (written before the kernel).
+template <bool kL2>
+__device__ __forceinline__ void ld_v4x8(const void* const (&p)[8], uint32_t (&r)[32])
+{
+    if constexpr (kL2)
+        FA_LD_V4X8("ld.global.cg.v4.u32");
+    else
+        FA_LD_V4X8("ld.global.nc.L1::no_allocate.v4.u32");
+}
+#undef FA_LD_V4X8
+
+template <bool kL2>
+__device__ __forceinline__ float ld_part(const float* p)
+{
+    if constexpr (kL2)
+        return __ldcg(p);
+    else
+        return __ldg(p);
+}
+
+// Log-sum-exp combine of one row's first n_valid partial states by one warp ("flash_lab.py"
+// section 1 `merge_states`: lse = log sum_s exp(lse_s), o = sum_s exp(lse_s - lse) o_s).
+// store_o(c, value) receives columns c < dv (lane l: VEC * (l + 32 i) + e, i < IT, with
+// IT * 32 * VEC >= dv) and store_lse(L) the row's lse from lane 0; with every part empty
+// (lse = -inf) the row is 0 and its lse -inf.  Empty parts are never read.  The parts are
+// added in increasing order, one FMA per part and column, but the loads of U parts are issued
+// together (VEC = 4: eight float4 loads by one statement), so a row pays about one memory
+// latency per U parts rather than one per part.  (The empty row leaves through its own stores:
+// with the two exits joined, the compiler interleaved the loads with the FMAs, 40 -> 32
+// registers, and a 256-part merge took 41 us instead of 27.)
+template <int VEC, int IT, bool kL2, typename StoreO, typename StoreL>
+__device__ __forceinline__ void merge_row(const float* lse_row, long long lse_stride, const float* o_row,
+                                          long long o_stride, int n_valid, int dv, int lane, StoreO store_o,
+                                          StoreL store_lse)
+{
+    constexpr int U = IT >= 8 ? 1 : 8 / IT;
+    float M = -INFINITY;
+    for (int s = lane; s < n_valid; s += 32) M = fmaxf(M, ld_part<kL2>(lse_row + s * lse_stride));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (M == -INFINITY) {  // every part empty: O = 0, LSE = -inf
+        for (int c = lane; c < dv; c += 32) store_o(c, 0.f);
+        if (lane == 0) store_lse(-INFINITY);
+        return;
+    }
+    float sum = 0.f;
+    for (int s = lane; s < n_valid; s += 32) {
+        const float x = ld_part<kL2>(lse_row + s * lse_stride);
+        if (x != -INFINITY) sum += ex2((x - M) * kLog2e);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    const float L = M + log2f(sum) * kLn2;
+
+    float acc[IT][VEC];
+#pragma unroll
+    for (int i = 0; i < IT; ++i)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[i][e] = 0.f;
+    for (int base = 0; base < n_valid; base += 32) {
+        // lane l weighs part base + l; the warp walks the non-empty ones in order
+        const int s = base + lane;
+        const float x = s < n_valid ? ld_part<kL2>(lse_row + s * lse_stride) : -INFINITY;
+        const float w_lane = x == -INFINITY ? 0.f : ex2((x - L) * kLog2e);
+        unsigned live = __ballot_sync(0xffffffffu, x != -INFINITY);
+        while (live != 0u) {
+            // U parts per batch; slots past the last live part re-read the batch's first part
+            // (finite: it was written) with weight 0, so every load is unconditional and in flight
+            // together, and fmaf(0, v, acc) leaves acc as it was
+            const int j0 = __ffs(live) - 1;
+            float w[U];
+            const float* op[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = live != 0u ? __ffs(live) - 1 : j0;
+                const float wj = __shfl_sync(0xffffffffu, w_lane, j);
+                w[u] = live != 0u ? wj : 0.f;
+                op[u] = o_row + static_cast<long long>(base + j) * o_stride;
+                live &= live - 1u;
+            }
+            if constexpr (VEC == 4) {
+                static_assert(U * IT == 8, "eight loads per batch");
+                const void* a[8];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int i = 0; i < IT; ++i) {
+                        const int c = 4 * (lane + 32 * i);
+                        a[u * IT + i] = op[u] + (c < dv ? c : 0);  // columns past dv: read, never stored
+                    }
+                uint32_t v[32];
+                ld_v4x8<kL2>(a, v);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int i = 0; i < IT; ++i)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int k = (u * IT + i) * 4 + e;
+                            acc[i][e] = fmaf(w[u], __uint_as_float(v[k]), acc[i][e]);
+                        }
+            } else {
+                static_assert(VEC == 1, "float or float4 columns");
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+#pragma unroll
+                    for (int i = 0; i < IT; ++i) {
+                        const int c = lane + 32 * i;
+                        acc[i][0] = fmaf(w[u], ld_part<kL2>(op[u] + (c < dv ? c : 0)), acc[i][0]);
+                    }
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+        const int c = VEC * (lane + 32 * i);
+        if (c < dv) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) store_o(c + e, acc[i][e]);
+        }
+    }
+    if (lane == 0) store_lse(L);
+}
+
 // One CTA per (split, KV head g, sequence b).  The R query heads g*R .. g*R+R-1 share the
 // KV head ("flash_lab.py" section 4: the query heads of a GQA group are packed as the rows
 // of q), so each K/V element is read once and used R times.  R = 1 is plain multi-head
@@ -238,66 +390,27 @@ __global__ void __launch_bounds__(kDecWarps * 32) fa_decode_split_kernel(const D
     __syncthreads();
     if (!is_last) return;
     __threadfence();
-    for (int idx = threadIdx.x; idx < R * D; idx += blockDim.x) {
-        const int r = idx / D;
-        const int c = idx - r * D;
-        const size_t row = bq0 + r;
-        const float* lse_row = p.lse_part + row * p.n_splits;
-        float M = -INFINITY;
-        for (int t = 0; t < n_valid; ++t) M = fmaxf(M, __ldcg(lse_row + t));
-        float sum = 0.f;
-        for (int t = 0; t < n_valid; ++t) sum += ex2((__ldcg(lse_row + t) - M) * kLog2e);
-        const float L = M + log2f(sum) * kLn2;
-        float o = 0.f;
-        for (int t = 0; t < n_valid; ++t)
-            o = fmaf(ex2((__ldcg(lse_row + t) - L) * kLog2e), __ldcg(p.o_part + (row * p.n_splits + t) * D + c), o);
-        store_row_value(p, row * D + c, o);
-        if (c == 0 && p.lse != nullptr) p.lse[row] = L;
+    if (warp < R) {  // warp r merges query row r (merge_row, partials read at L2)
+        const size_t row = bq0 + warp;
+        merge_row<4, 1, true>(
+            p.lse_part + row * p.n_splits, 1, p.o_part + row * p.n_splits * D, D, n_valid, D, lane,
+            [o = p.o, f32 = p.o_dtype == FA_F32, row](int c, float v) {
+                if (f32)
+                    reinterpret_cast<float*>(o)[row * D + c] = v;
+                else
+                    reinterpret_cast<__nv_bfloat16*>(o)[row * D + c] = __float2bfloat16_rn(v);
+            },
+            [lse = p.lse, row](float L) {
+                if (lse != nullptr) lse[row] = L;
+            });
     }
     if (threadIdx.x == 0) p.counters[bkv] = 0u;  // ready for the next call
 }
 
-template <typename OutT>
-__device__ __forceinline__ void store_out(OutT* o, size_t i, float v);
-template <>
-__device__ __forceinline__ void store_out<float>(float* o, size_t i, float v)
-{
-    o[i] = v;
-}
-template <>
-__device__ __forceinline__ void store_out<__nv_bfloat16>(__nv_bfloat16* o, size_t i, float v)
-{
-    o[i] = __float2bfloat16_rn(v);
-}
-
-// Eight streaming 16-byte global loads in one statement: all 32 results are defined together,
-// so the eight requests are issued back to back and are in flight at once.
-__device__ __forceinline__ void ld_stream_v4x8(const void* const (&p)[8], uint32_t (&r)[32])
-{
-    asm volatile(
-        "ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%32];\n\t"
-        "ld.global.nc.L1::no_allocate.v4.u32 {%4, %5, %6, %7}, [%33];\n\t"
-        "ld.global.nc.L1::no_allocate.v4.u32 {%8, %9, %10, %11}, [%34];\n\t"
-        "ld.global.nc.L1::no_allocate.v4.u32 {%12, %13, %14, %15}, [%35];\n\t"
-        "ld.global.nc.L1::no_allocate.v4.u32 {%16, %17, %18, %19}, [%36];\n\t"
-        "ld.global.nc.L1::no_allocate.v4.u32 {%20, %21, %22, %23}, [%37];\n\t"
-        "ld.global.nc.L1::no_allocate.v4.u32 {%24, %25, %26, %27}, [%38];\n\t"
-        "ld.global.nc.L1::no_allocate.v4.u32 {%28, %29, %30, %31}, [%39];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "l"(p[0]), "l"(p[1]), "l"(p[2]), "l"(p[3]), "l"(p[4]), "l"(p[5]), "l"(p[6]), "l"(p[7]));
-}
-
-// One warp per row: combine the row's valid parts.  Lane l holds columns VEC * (l + 32 i),
-// i < IT (VEC = 4: float4 loads; IT * 128 >= dv).  The parts are added in increasing order,
-// one FMA per part and column, but the loads of U parts are issued together, so a row with
-// many parts pays about one memory latency per U parts instead of one per part.
+// One warp per row: combine the row's valid parts (merge_row).
 template <typename OutT, int VEC, int IT>
 __global__ void __launch_bounds__(128) fa_merge_kernel(const MergeParams p)
 {
-    constexpr int U = IT >= 8 ? 1 : 8 / IT;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * 4 + warp;
@@ -307,97 +420,15 @@ __global__ void __launch_bounds__(128) fa_merge_kernel(const MergeParams p)
         const int n = clamp_len(p.seqlens[row / p.H], p.Nk_max, p.status);
         n_valid = min(p.n_parts, (n + p.chunk - 1) / p.chunk);
     }
-    const float* lse_row = p.lse_parts + static_cast<size_t>(row) * p.lse_row_stride;
-    const float* o_row = p.o_parts + static_cast<size_t>(row) * p.o_row_stride;
-
-    float M = -INFINITY;
-    for (int s = lane; s < n_valid; s += 32) M = fmaxf(M, lse_row[s * p.lse_part_stride]);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     OutT* out = reinterpret_cast<OutT*>(p.o) + static_cast<size_t>(row) * p.dv;
-    if (M == -INFINITY) {  // every part empty: O = 0, LSE = -inf
-        for (int c = lane; c < p.dv; c += 32) store_out<OutT>(out, c, 0.f);
-        if (p.lse != nullptr && lane == 0) p.lse[row] = -INFINITY;
-        return;
-    }
-    float sum = 0.f;
-    for (int s = lane; s < n_valid; s += 32) {
-        const float x = lse_row[s * p.lse_part_stride];
-        if (x != -INFINITY) sum += ex2((x - M) * kLog2e);
-    }
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const float L = M + log2f(sum) * kLn2;
-
-    float acc[IT][VEC];
-#pragma unroll
-    for (int i = 0; i < IT; ++i)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) acc[i][e] = 0.f;
-    for (int base = 0; base < n_valid; base += 32) {
-        // lane l weighs part base + l; the warp walks the non-empty ones in order
-        const int s = base + lane;
-        const float x = s < n_valid ? lse_row[s * p.lse_part_stride] : -INFINITY;
-        const float w_lane = x == -INFINITY ? 0.f : ex2((x - L) * kLog2e);
-        unsigned live = __ballot_sync(0xffffffffu, x != -INFINITY);
-        while (live != 0u) {
-            // U parts per batch; slots past the last live part re-read the batch's first part
-            // (finite: it was written) with weight 0, so every load is unconditional and in flight
-            // together, and fmaf(0, v, acc) leaves acc as it was
-            const int j0 = __ffs(live) - 1;
-            float w[U];
-            const float* op[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int j = live != 0u ? __ffs(live) - 1 : j0;
-                const float wj = __shfl_sync(0xffffffffu, w_lane, j);
-                w[u] = live != 0u ? wj : 0.f;
-                op[u] = o_row + static_cast<long long>(base + j) * p.o_part_stride;
-                live &= live - 1u;
-            }
-            if constexpr (VEC == 4) {
-                // U * IT = 8 float4 loads per lane, issued by one statement
-                static_assert(U * IT == 8, "eight loads per batch");
-                const void* a[8];
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int i = 0; i < IT; ++i) {
-                        const int c = 4 * (lane + 32 * i);
-                        a[u * IT + i] = op[u] + (c < p.dv ? c : 0);  // columns past dv: read, never stored
-                    }
-                uint32_t v[32];
-                ld_stream_v4x8(a, v);
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int i = 0; i < IT; ++i)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int k = (u * IT + i) * 4 + e;
-                            acc[i][e] = fmaf(w[u], __uint_as_float(v[k]), acc[i][e]);
-                        }
-            } else {
-#pragma unroll
-                for (int u = 0; u < U; ++u)
-#pragma unroll
-                    for (int i = 0; i < IT; ++i) {
-                        const int c = lane + 32 * i;
-                        const float x = __ldg(op[u] + (c < p.dv ? c : 0));
-                        acc[i][0] = fmaf(w[u], x, acc[i][0]);
-                    }
-            }
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < IT; ++i) {
-        const int c = VEC * (lane + 32 * i);
-        if (c < p.dv) {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) store_out<OutT>(out, c + e, acc[i][e]);
-        }
-    }
-    if (p.lse != nullptr && lane == 0) p.lse[row] = L;
+    float* lse = p.lse;
+    merge_row<VEC, IT, false>(
+        p.lse_parts + static_cast<size_t>(row) * p.lse_row_stride, p.lse_part_stride,
+        p.o_parts + static_cast<size_t>(row) * p.o_row_stride, p.o_part_stride, n_valid, p.dv, lane,
+        [out](int c, float v) { store_out<OutT>(out, c, v); },
+        [lse, row](float L) {
+            if (lse != nullptr) lse[row] = L;
+        });
 }
 
 template <typename OutT>
