@@ -94,7 +94,8 @@ def test_full_decode_config():
 
 
 @pytest.mark.parametrize("n_parts,rows,dv,empty", [(1, 5, 128, 0.0), (16, 333, 128, 0.3), (999, 7, 64, 0.5),
-                                                   (3, 64, 512, 0.0), (4, 10, 33, 1.0)])
+                                                   (3, 64, 512, 0.0), (4, 10, 33, 1.0), (16, 50, 256, 0.2),
+                                                   (77, 9, 32, 0.4)])
 def test_merge_states_against_oracle(n_parts, rows, dv, empty):
     o_parts, lse_parts = merge_inputs(n_parts, rows, dv, seed=n_parts, empty_frac=empty, device=DEV)
     o_ref, lse_ref = oracle.merge_lse(o_parts.cpu(), lse_parts.cpu())
@@ -106,6 +107,26 @@ def test_merge_states_against_oracle(n_parts, rows, dv, empty):
     if fin.any():
         assert np.abs(a[fin] - b[fin]).max() <= 1e-5 * max(1.0, np.abs(b[fin]).max())
     assert np.abs(to_np(o) - o_ref).max() <= 1e-5
+
+
+@pytest.mark.parametrize("dv,offset", [(128, 0), (33, 0), (64, 1), (512, 0)])
+def test_merge_states_never_reads_empty_parts(dv, offset):
+    """Empty parts (lse = -inf) may hold anything: a split with no visible key writes nothing.
+    With NaN there the merge must equal the oracle on the zero-filled states.  offset = 1 starts
+    the parts 4 bytes past a 16-byte boundary (the scalar-load form of the merge)."""
+    n_parts, rows = 37, 21
+    o_parts, lse_parts = merge_inputs(n_parts, rows, dv, seed=dv + offset, empty_frac=0.6, device=DEV)
+    o_ref, lse_ref = oracle.merge_lse(o_parts.cpu(), lse_parts.cpu())
+    buf = torch.empty(n_parts * rows * dv + offset, dtype=torch.float32, device=DEV)
+    o_bad = buf[offset:].view(n_parts, rows, dv)
+    o_bad.copy_(torch.where(torch.isneginf(lse_parts)[..., None], torch.full_like(o_parts, float("nan")), o_parts))
+    o, lse = fa().merge_states(o_bad, lse_parts, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    a, b = to_np(lse), lse_ref
+    assert np.array_equal(np.isneginf(a), np.isneginf(b))
+    fin = ~np.isneginf(b)
+    assert np.abs(a[fin] - b[fin]).max() <= 1e-5 * max(1.0, np.abs(b[fin]).max())
+    assert np.isfinite(to_np(o)).all() and np.abs(to_np(o) - o_ref).max() <= 1e-5
 
 
 def oracle_gqa_compact(q, k, v, lens, scale):
