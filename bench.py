@@ -521,12 +521,35 @@ def run_decode(fa, dev, stream, args, world):
              "fused_us": 1e3 * time_calls(lambda: fa.decode_splitkv_fused(qs, ks, vs, ls_d, wsf2, n_splits=ns, out=os_,
                                                                           return_lse=False),
                                           dev, stream, 5, 50, world)}
+    # the same calls replayed from a CUDA graph of 20 calls: no per-call launch cost
+    short["graph_two_launches_us"] = graph_us(lambda: fa.decode_splitkv(qs, ks, vs, ls_d, n_splits=ns, out=os_,
+                                                                        workspace=ws2, return_lse=False),
+                                              dev, stream, world)
+    short["graph_fused_us"] = graph_us(lambda: fa.decode_splitkv_fused(qs, ks, vs, ls_d, wsf2, n_splits=ns, out=os_,
+                                                                       return_lse=False),
+                                       dev, stream, world)
     assert fa.get_device_error(dev) == fa.FA_OK
     return {"workload": "split-KV decode B=16 H=32 d=128, lengths U[1024,32768] (seed 0), bf16 O",
             "n_splits": n, "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
             "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2,
             "fused_combine": {"ms": ms_f, "gbs": world * (kv_bytes + other) / (ms_f / 1e3) / 1e9, "launches_per_call": 1},
             "short_context": short}
+
+
+def graph_us(call, dev, stream, world, reps=20):
+    """Microseconds per call with `reps` calls captured into one CUDA graph and the graph replayed
+    (after one eager call on a side stream for the first-use set-up)."""
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            call()
+    return 1e3 * time_calls(g.replay, dev, stream, 3, 10, world) / reps
 
 
 def time_calls(call, dev, stream, warmup, steps, world):

@@ -40,6 +40,11 @@
  *     nothing.  Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream) and never synchronise, except
  *     fa_get_device_error.
+ *   - CUDA graphs: after the first call on a device (which caches kernel attributes and
+ *     device addresses), a call launches kernels on `stream` and does nothing else on the
+ *     device, so every entry point but fa_get_device_error may be captured into a CUDA
+ *     graph and replayed; the tensor maps are encoded at capture time from the pointers
+ *     and sizes given, so a replay reads and writes the same buffers.
  *   - Errors: every argument is checked on the host before any launch; a bad argument
  *     returns a status and launches nothing.  A launch failure returns FA_ERR_CUDA.
  *     Failures the device detects (a bounded wait that ran out, a sequence length out
