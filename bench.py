@@ -637,8 +637,62 @@ def run_splitkv_prefill(fa, dev, stream, args, world):
     return out
 
 
+def _case_call(fa, dev, name):
+    """(callable, description) for one named workload of the suite, inputs built on `dev`."""
+    fwd_cases = {"fwd-c1": 0, "fwd-c1-causal": 1, "fwd-c3a": 2, "fwd-c3a-causal": 3, "fwd-c3b-causal": 4,
+                 "fwd-c4": 5}
+    if name in fwd_cases or name in ("fwd-c2", "fwd-c2-causal"):
+        if name in fwd_cases:
+            desc, B, H, N, Nk, d, mult, causal = OTHER_FWD[fwd_cases[name]]
+        else:
+            B, H, N, Nk, d, mult, causal = FWD["B"], FWD["H"], FWD["N"], FWD["Nk"], FWD["d"], 1.0, name.endswith("causal")
+            desc = WORKLOAD + (" causal" if causal else " non-causal")
+        q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=0, mult=mult, device=dev)
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        return (lambda: fa.fwd(q, k, v, causal=causal, out=o, lse=lse)), desc
+    if name in ("gqa4", "gqa8"):
+        B, Hq, Nk_max, d = GQA["B"], GQA["Hq"], GQA["Nk_max"], GQA["d"]
+        Hkv = Hq // (4 if name == "gqa4" else 8)
+        q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=GQA["lo"], hi=GQA["hi"], device=dev)
+        lens_d = lens.to(dev)
+        n = fa.decode_gqa_default_splits(B, Hq, Hkv, Nk_max, fa.num_sms(dev))
+        ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n), dtype=torch.uint8, device=dev)
+        o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
+        return (lambda: fa.decode_splitkv_gqa(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws),
+                f"GQA decode B={B} Hq={Hq} Hkv={Hkv} d={d}")
+    if name == "decode":
+        B, H, Nk_max, d = DEC["B"], DEC["H"], DEC["Nk_max"], DEC["d"]
+        q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=0, lo=DEC["lo"], hi=DEC["hi"], device=dev)
+        lens_d = lens.to(dev)
+        n = fa.decode_default_splits(B, H, Nk_max, fa.num_sms(dev))
+        ws = torch.empty(fa.decode_workspace_size(B, H, d, n), dtype=torch.uint8, device=dev)
+        o = torch.empty((B, H, 1, d), dtype=torch.bfloat16, device=dev)
+        return (lambda: fa.decode_splitkv(q, k, v, lens_d, n_splits=n, out=o, workspace=ws, return_lse=False),
+                f"split-KV decode B={B} H={H} d={d}")
+    raise SystemExit(f"unknown --case {name}")
+
+
+def run_case(args, local):
+    """One workload alone, `warmup` untimed and `steps` timed calls (for profiling captures)."""
+    import exact_tiled_attention_fa_gb300 as fa
+    fa.library()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    call, desc = _case_call(fa, dev, args.case)
+    ms = time_calls(call, dev, stream, args.warmup, args.steps, 1)
+    assert fa.get_device_error(dev) == fa.FA_OK
+    print(json.dumps({"case": args.case, "workload": desc, "calls": args.steps, "ms_per_call": ms}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--case", default=None,
+                    help="run one workload alone (fwd-c1, fwd-c1-causal, fwd-c2, fwd-c2-causal, fwd-c3a, "
+                         "fwd-c3a-causal, fwd-c3b-causal, fwd-c4, decode, gqa4, gqa8) for profiling")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
@@ -660,6 +714,8 @@ def main():
     DEC["B"] = args.decode_batch
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.case:
+        return run_case(args, local)
     return run_ours(args, world, rank, local)
 
 

@@ -4,7 +4,7 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
 leg may import this package.  It shares no code with the CUDA path: the C
 library ``fa_oracle.c`` (built here with gcc into ``liboracle.so``) is the
 plain definition of standard attention and of its backward in float64, and
-``numpy_oracle`` is an independent numpy restatement of the same pages.
+``numpy_oracle`` is a second, independent numpy statement of the same definitions.
 
 Inputs are torch tensors or numpy arrays.  bf16 tensors are handed to the C
 library as raw bit patterns and widened exactly there; everything else is

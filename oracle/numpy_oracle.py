@@ -1,268 +1,303 @@
-"""numpy FP64 restatement of the pages' attention algorithms -- TEST INFRASTRUCTURE ONLY.
+"""numpy FP64 second statement of exact attention -- TEST INFRASTRUCTURE ONLY.
 
 Only the tests, the smoke check and the benchmark's CPU-baseline leg may use
 anything under ``oracle/``.  This module shares no code with the CUDA path.
 
-It restates, in float64 and in the pages' own notation, the algorithms of
-"flash_lab.py -- FlashAttention, flash-decoding and megakernel in numpy"
-(CS349E lecture 11 shared module):
+What it states, in float64, and where the pages define it
+("flash_lab.py -- FlashAttention, flash-decoding and megakernel in numpy",
+CS349E lecture 11 shared module):
 
-* section 1 (online softmax): ``softmax_3pass``, ``softmax_online``,
-  ``partial_state``, ``merge_states``;
-* section 2 (standard attention): ``causal_mask``, ``standard_attention``;
-* section 2 (standard attention backward): ``standard_attention_bwd``;
-* section 3 (FlashAttention): ``flash_fwd_tiled`` -- the FlashAttention-2 loop
-  order (outer loop over query tiles, inner loop over key/value tiles, the
-  running max m and sum l rescaled by exp(m_old - m_new), one division by l
-  at the end, L = m + log l, and the causal "stop at the first fully masked
-  tile" rule), and ``flash_bwd_tiled`` -- the FlashAttention-2 form of the
-  backward (outer loop over key/value tiles, P recomputed as exp(S - L));
-* section 4 (flash-decoding): ``split_kv_decode`` -- split the keys into
-  segments, normalise each segment's output, keep its log-sum-exp, merge.
+* ``attention_definition`` / ``attention_bwd_definition``: exact attention and
+  its gradients with the score matrix materialised (section 2, standard
+  attention and its backward); the value every tiled form must reach.
+* ``RowState``: the per-row streaming normaliser of section 1 -- a running
+  maximum, a running sum of exponentials taken relative to it and an
+  accumulator of exponential-weighted value rows.  Absorbing a block whose
+  maximum exceeds the running one re-expresses the old sum and accumulator
+  relative to the new maximum (they are multiplied by exp(old - new)).
+* ``segment_state`` / ``combine``: a partial result kept in log-sum-exp form,
+  (normalised output, log of the segment's normaliser), and the exact merge of
+  two such states (section 1's merge, section 4's combine).  The merge is
+  written here in that form: the merged log-normaliser is the log of the sum of
+  the two normalisers, and each side's output is weighted by its share.
+* ``tiled_forward`` / ``tiled_backward``: the FlashAttention-2 loop orders of
+  section 3 as a walk over the (query tile, key tile) grid that visits exactly
+  the tiles holding at least one visible (query, key) pair (``tile_visible``,
+  derived below from the causal convention), built from ``RowState``.
+* ``split_decode``: section 4's split-KV decoding with near-equal integer
+  segment bounds; segments are combined with ``combine``.
 
-The C library in this directory (``fa_oracle.c``) is the fast form of the
-same definition used for large parity checks; this module is the second,
-independent statement used to pin it on small shapes and to model the tiled
-algorithm's masking and skipping on the CPU.
+The causal convention is that of "02_flash_forward.py -- FlashAttention forward"
+demo 1: query i of N sits at position Nk - N + i, key j at position j, and a
+key is visible when its position does not exceed the query's.
+
+The C library in this directory (``fa_oracle.c``) is the fast statement of the
+same definition used for large parity checks; this module pins it on small
+shapes and models the tiled kernels' masking and tile skipping on the CPU.
 """
 from __future__ import annotations
 
 import math
+from functools import reduce
 
 import numpy as np
 
+NEG_INF = -np.inf
+
 
 # --------------------------------------------------------------------------
-# section 1: online softmax
+# positions and visibility
 # --------------------------------------------------------------------------
-def softmax_3pass(x):
-    """Safe softmax along the last axis: max, then sum of exp(x - max), then divide."""
+def visibility(N, Nk, causal, q_lo=0, q_hi=None, k_lo=0, k_hi=None):
+    """Boolean block [q_lo:q_hi, k_lo:k_hi] of the N x Nk visibility matrix.
+
+    Without a mask every key is visible.  With one, query row i sits at
+    position Nk - N + i and sees key j exactly when j <= Nk - N + i.
+    """
+    q_hi = N if q_hi is None else q_hi
+    k_hi = Nk if k_hi is None else k_hi
+    rows, cols = q_hi - q_lo, k_hi - k_lo
+    if not causal:
+        return np.ones((rows, cols), dtype=bool)
+    last_key = (Nk - N) + np.arange(q_lo, q_hi)  # position of each query = its last visible key
+    return np.arange(k_lo, k_hi)[None, :] <= last_key[:, None]
+
+
+def tile_visible(N, Nk, causal, q_lo, q_hi, k_lo):
+    """Whether the tile of queries [q_lo, q_hi) and keys starting at k_lo holds a visible pair.
+
+    Visibility only grows with the query index (its position Nk - N + i grows)
+    and only shrinks with the key index, so the most visible corner of a tile
+    is (its last query, its first key): the tile holds a visible pair iff that
+    corner is visible, i.e. k_lo <= Nk - N + (q_hi - 1).  Without a mask every
+    tile does.
+    """
+    return (not causal) or k_lo <= (Nk - N) + (q_hi - 1)
+
+
+# --------------------------------------------------------------------------
+# softmax: the plain definition and the streaming normaliser
+# --------------------------------------------------------------------------
+def softmax_safe(x):
+    """Softmax along the last axis in three passes: the maximum, the sum of
+    exponentials relative to it, the division."""
     x = np.asarray(x, dtype=np.float64)
-    m = x.max(axis=-1, keepdims=True)
-    e = np.exp(x - m)
-    return e / e.sum(axis=-1, keepdims=True)
+    top = np.max(x, axis=-1, keepdims=True)
+    w = np.exp(x - top)
+    return w / np.sum(w, axis=-1, keepdims=True)
 
 
-def softmax_online(x, block=128):
-    """One pass for (m, l) over blocks, rescaling l by exp(m - m_new); a second pass divides."""
+class RowState:
+    """Streaming normaliser of a block of rows.
+
+    Holds, per row, the largest score absorbed so far (``top``; -inf while
+    nothing visible has been seen), the sum of exp(score - top) over absorbed
+    scores (``total``) and, when value rows are supplied, the sum of
+    exp(score - top) * value (``acc``).  Masked scores are -inf and contribute
+    exp(-inf) = 0.
+    """
+
+    def __init__(self, rows, width=0):
+        self.top = np.full(rows, NEG_INF)
+        self.total = np.zeros(rows)
+        self.acc = np.zeros((rows, width))
+
+    @staticmethod
+    def _anchor(top):
+        # A row with nothing visible has top = -inf; measuring its exponentials
+        # from 0 instead keeps every exp argument free of (-inf) - (-inf).
+        return np.where(np.isfinite(top), top, 0.0)
+
+    def absorb(self, scores, values=None):
+        """Fold a block of scores [rows, n] (and value rows [n, width]) into the state."""
+        scores = np.asarray(scores, dtype=np.float64)
+        block_top = scores.max(axis=1) if scores.shape[1] else np.full(scores.shape[0], NEG_INF)
+        new_top = np.maximum(self.top, block_top)
+        new_anchor = self._anchor(new_top)
+        # the old sums were taken relative to the old maximum; re-express them relative to the
+        # new one (a row that had seen nothing has empty sums: factor 0)
+        shrink = np.exp(np.where(np.isfinite(self.top), self.top - new_anchor, NEG_INF))
+        w = np.exp(scores - new_anchor[:, None])
+        self.total = self.total * shrink + w.sum(axis=1)
+        if values is not None:
+            self.acc = self.acc * shrink[:, None] + w @ np.asarray(values, dtype=np.float64)
+        self.top = new_top
+
+    def log_normaliser(self):
+        """log of sum over absorbed scores of exp(score); -inf for a row that saw nothing."""
+        seen = self.total > 0
+        return np.where(seen, self._anchor(self.top) + np.log(np.where(seen, self.total, 1.0)), NEG_INF)
+
+    def output(self):
+        """acc / total: the softmax-weighted mean of the absorbed value rows (0 where nothing was seen)."""
+        seen = self.total > 0
+        return np.where(seen[:, None], self.acc / np.where(seen, self.total, 1.0)[:, None], 0.0)
+
+
+def softmax_streaming(x, block):
+    """Softmax along the last axis of a 2-D array from one streaming pass over
+    column blocks of width ``block`` (for the normaliser) and one final pass."""
     x = np.asarray(x, dtype=np.float64)
-    m = np.full(x.shape[:-1] + (1,), -np.inf)
-    l = np.zeros(x.shape[:-1] + (1,))
-    for start in range(0, x.shape[-1], block):
-        xb = x[..., start:start + block]
-        m_new = np.maximum(m, xb.max(axis=-1, keepdims=True))
-        l = l * np.exp(m - m_new) + np.exp(xb - m_new).sum(axis=-1, keepdims=True)
-        m = m_new
-    return np.exp(x - m) / l
-
-
-def partial_state(x, v=None):
-    """(m, l, o) of one segment: m = max, l = sum exp(x - m), o = sum exp(x - m) v."""
-    x = np.asarray(x, dtype=np.float64)
-    m = x.max(axis=-1)
-    p = np.exp(x - m[..., None])
-    l = p.sum(axis=-1)
-    o = None if v is None else p @ np.asarray(v, dtype=np.float64)
-    return m, l, o
-
-
-def merge_states(a, b):
-    """Associative, commutative merge of two (m, l, o) states; an all -inf state has weight 0."""
-    ma, la, oa = a
-    mb, lb, ob = b
-    m = np.maximum(ma, mb)
-    with np.errstate(invalid="ignore"):
-        wa = np.where(np.isneginf(ma), 0.0, np.exp(ma - m))
-        wb = np.where(np.isneginf(mb), 0.0, np.exp(mb - m))
-    l = la * wa + lb * wb
-    o = None if oa is None else oa * wa[..., None] + ob * wb[..., None]
-    return m, l, o
+    st = RowState(x.shape[0])
+    for c in range(0, x.shape[1], block):
+        st.absorb(x[:, c:c + block])
+    return np.exp(x - st.log_normaliser()[:, None])
 
 
 # --------------------------------------------------------------------------
-# section 2: standard attention
+# partial states in log-sum-exp form, and their merge
 # --------------------------------------------------------------------------
-def causal_mask(nq, nk, q0=0, k0=0, offset=0):
-    """Boolean [nq, nk]: True where allowed.  Query q0+r sits at offset+q0+r, key k0+c at k0+c."""
-    qpos = offset + q0 + np.arange(nq)[:, None]
-    kpos = k0 + np.arange(nk)[None, :]
-    return kpos <= qpos
+def segment_state(scores, values):
+    """(o, lse) of one segment: o = softmax(scores) @ values over the segment, lse = log sum exp(scores).
+
+    A row whose scores are all -inf has o = 0 and lse = -inf (it carries no weight)."""
+    st = RowState(np.shape(scores)[0], np.shape(values)[1])
+    st.absorb(scores, values)
+    return st.output(), st.log_normaliser()
 
 
-def standard_attention(Q, K, V, causal=False, scale=None):
-    """S = Q K^T * scale, causal mask (offset Nk - N), 3-pass softmax, O = P V.
+def combine(a, b):
+    """Exact merge of two log-sum-exp-form states covering disjoint key sets.
 
-    Returns (O, LSE, P).  A row with no visible key gets O = 0, LSE = -inf and
-    a zero P row (the reading the C oracle also takes).
+    With Z = exp(lse) the normaliser of each side, the union has Z = Z_a + Z_b
+    and its output is the Z-weighted mean of the two outputs.  In logs:
+    lse = logaddexp(lse_a, lse_b) and the weight of side a is exp(lse_a - lse).
+    A side with lse = -inf has weight 0; if both are empty the result is
+    (0, -inf)."""
+    (oa, la), (ob, lb) = a, b
+    lse = np.logaddexp(la, lb)
+    empty = np.isneginf(lse)
+    ref = np.where(empty, 0.0, lse)
+    wa = np.exp(la - ref)  # exp(-inf) = 0 for an empty side
+    wb = np.exp(lb - ref)
+    return wa[:, None] * oa + wb[:, None] * ob, lse
+
+
+# --------------------------------------------------------------------------
+# exact attention: the definitions
+# --------------------------------------------------------------------------
+def attention_definition(Q, K, V, causal=False, scale=None):
+    """O = softmax(mask(Q K^T * scale)) V with the full score matrix; LSE = log of each row's normaliser.
+
+    Returns (O, LSE, P).  A row with no visible key gets O = 0, LSE = -inf and a zero P row.
     """
     Q, K, V = (np.asarray(t, dtype=np.float64) for t in (Q, K, V))
     N, d = Q.shape
     Nk = K.shape[0]
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    S = (Q @ K.T) * scale
-    if causal:
-        S = np.where(causal_mask(N, Nk, offset=Nk - N), S, -np.inf)
-    m = S.max(axis=1) if Nk > 0 else np.full(N, -np.inf)
-    empty = np.isneginf(m)
-    m_safe = np.where(empty, 0.0, m)
-    E = np.exp(S - m_safe[:, None])
-    l = E.sum(axis=1)
-    with np.errstate(invalid="ignore", divide="ignore"):
-        P = np.where(empty[:, None], 0.0, E / np.where(empty, 1.0, l)[:, None])
-        lse = np.where(empty, -np.inf, m_safe + np.log(np.where(empty, 1.0, l)))
-    O = P @ V
-    return O, lse, P
+    vis = visibility(N, Nk, causal)
+    S = np.where(vis, scale * (Q @ K.T), NEG_INF)
+    has_key = vis.any(axis=1)
+    P = np.zeros_like(S)
+    P[has_key] = softmax_safe(S[has_key])
+    lse = np.full(N, NEG_INF)
+    if has_key.any():
+        rows = S[has_key]
+        top = rows.max(axis=1)
+        lse[has_key] = top + np.log(np.exp(rows - top[:, None]).sum(axis=1))
+    return P @ V, lse, P
 
 
-def standard_attention_bwd(Q, K, V, dO, causal=False, scale=None, return_terms=False):
-    """Backward of standard attention with the full P materialised.
+def attention_bwd_definition(Q, K, V, dO, causal=False, scale=None, return_terms=False):
+    """Gradients of sum(O * dO) with the full P materialised.
 
-    dV = P^T dO; dP = dO V^T; D_i = sum_c dO_ic O_ic; dS = P o (dP - D);
-    dQ = dS K scale; dK = dS^T Q scale.  Returns (dQ, dK, dV), followed by
+    With O = P V and P = softmax of the scaled, masked scores:
+    dV = P^T dO; dP = dO V^T; D_i = sum_c dO_ic O_ic; dS = P * (dP - D)
+    (the softmax Jacobian applied row by row); the scores are scale * Q K^T, so
+    dQ = scale dS K and dK = scale dS^T Q.  Returns (dQ, dK, dV), followed by
     (P, dS) when ``return_terms``.
     """
     Q, K, V, dO = (np.asarray(t, dtype=np.float64) for t in (Q, K, V, dO))
-    d = Q.shape[1]
-    scale = 1.0 / math.sqrt(d) if scale is None else scale
-    O, _, P = standard_attention(Q, K, V, causal, scale)
-    D = np.sum(dO * O, axis=1)
-    dV = P.T @ dO
+    scale = 1.0 / math.sqrt(Q.shape[1]) if scale is None else scale
+    O, _, P = attention_definition(Q, K, V, causal, scale)
     dP = dO @ V.T
+    D = np.einsum("ic,ic->i", dO, O)
     dS = P * (dP - D[:, None])
-    if return_terms:
-        return dS @ K * scale, dS.T @ Q * scale, dV, P, dS
-    return dS @ K * scale, dS.T @ Q * scale, dV
+    grads = (scale * (dS @ K), scale * (dS.T @ Q), P.T @ dO)
+    return grads + (P, dS) if return_terms else grads
 
 
 # --------------------------------------------------------------------------
-# section 3: FlashAttention, FlashAttention-2 loop order (tiled model)
+# the tiled loop orders (models of the kernels' walks)
 # --------------------------------------------------------------------------
-def flash_fwd_tiled(Q, K, V, Br, Bc, causal=False, scale=None):
-    """Tiled forward in the FlashAttention-2 order.
+def _tiles(n, size):
+    return [(lo, min(lo + size, n)) for lo in range(0, n, size)]
 
-    For each query tile (Br rows) keep m, l and the unnormalised accumulator
-    on chip; for each key tile (Bc keys) form the masked score tile, update
-    m_new = max(m, rowmax), alpha = exp(m - m_new), P = exp(S - m_new),
-    l = alpha l + rowsum P, acc = alpha acc + P V; stop at the first tile
-    whose first key lies after the tile's last query position (every later
-    tile is masked too).  At the end O = acc / l and L = m + log l.
 
-    Returns (O, L, visited) where ``visited`` lists the (query tile, key
-    tile) pairs that were computed, for checking the skipping rule.
+def tiled_forward(Q, K, V, Br, Bc, causal=False, scale=None):
+    """Query tiles of Br rows each walk the key tiles of Bc keys that hold a visible pair,
+    folding each masked score tile and its value rows into a ``RowState``; O and LSE come
+    from the state once the walk ends.
+
+    Returns (O, LSE, visited), ``visited`` the (query tile, key tile) indices computed.
     """
     Q, K, V = (np.asarray(t, dtype=np.float64) for t in (Q, K, V))
     N, d = Q.shape
     Nk, dv = V.shape
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    off = Nk - N
-    O = np.zeros((N, dv))
-    L = np.full(N, -np.inf)
-    visited = []
-    for i0 in range(0, N, Br):
-        br = min(Br, N - i0)
-        m = np.full(br, -np.inf)
-        l = np.zeros(br)
-        acc = np.zeros((br, dv))
-        for j0 in range(0, Nk, Bc):
-            if causal and off + i0 + br - 1 < j0:
-                break
-            bc = min(Bc, Nk - j0)
-            visited.append((i0 // Br, j0 // Bc))
-            S = (Q[i0:i0 + br] @ K[j0:j0 + bc].T) * scale
-            if causal:
-                S = np.where(causal_mask(br, bc, i0, j0, off), S, -np.inf)
-            m_new = np.maximum(m, S.max(axis=1))
-            m_use = np.where(np.isneginf(m_new), 0.0, m_new)
-            alpha = np.where(np.isneginf(m), 0.0, np.exp(m - m_use))
-            P = np.exp(S - m_use[:, None])
-            l = alpha * l + P.sum(axis=1)
-            acc = alpha[:, None] * acc + P @ V[j0:j0 + bc]
-            m = m_new
-        seen = l > 0
-        with np.errstate(invalid="ignore", divide="ignore"):
-            O[i0:i0 + br] = np.where(seen[:, None], acc / np.where(seen, l, 1.0)[:, None], 0.0)
-            L[i0:i0 + br] = np.where(seen, m + np.log(np.where(seen, l, 1.0)), -np.inf)
+    O, L, visited = np.zeros((N, dv)), np.full(N, NEG_INF), []
+    for ti, (q_lo, q_hi) in enumerate(_tiles(N, Br)):
+        st = RowState(q_hi - q_lo, dv)
+        for tj, (k_lo, k_hi) in enumerate(_tiles(Nk, Bc)):
+            if not tile_visible(N, Nk, causal, q_lo, q_hi, k_lo):
+                continue
+            visited.append((ti, tj))
+            S = scale * (Q[q_lo:q_hi] @ K[k_lo:k_hi].T)
+            st.absorb(np.where(visibility(N, Nk, causal, q_lo, q_hi, k_lo, k_hi), S, NEG_INF), V[k_lo:k_hi])
+        O[q_lo:q_hi], L[q_lo:q_hi] = st.output(), st.log_normaliser()
     return O, L, visited
 
 
-def flash_bwd_tiled(Q, K, V, O, dO, L, Br, Bc, causal=False, scale=None):
-    """Tiled backward in the FlashAttention-2 order (recompute S and P from L).
+def tiled_backward(Q, K, V, O, dO, L, Br, Bc, causal=False, scale=None):
+    """Key tiles own their dK and dV; each walks the query tiles that hold a visible pair with it,
+    rebuilding that tile's probabilities from the forward's log-normaliser L
+    (P = exp(S - L), 0 for a row with L = -inf), and adds its share of dQ.
 
-    D_i = sum dO_i o O_i first.  The outer loop walks key/value tiles j (their
-    dK_j, dV_j accumulate on chip), the inner loop walks query tiles i, skipping
-    a tile whose last query position lies before the key tile's first key.
-    Per (i, j): S = Q_i K_j^T scale (masked), P = exp(S - L_i),
-    dV_j += P^T dO_i, dP = dO_i V_j^T, dS = P o (dP - D_i),
-    dQ_i += dS K_j scale, dK_j += dS^T Q_i scale.
-
-    Returns (dQ, dK, dV, visited) with ``visited`` the (query tile, key tile)
-    pairs computed.  A row with L = -inf (no visible key) gets P = 0.
+    Returns (dQ, dK, dV, visited).
     """
     Q, K, V, O, dO = (np.asarray(t, dtype=np.float64) for t in (Q, K, V, O, dO))
     L = np.asarray(L, dtype=np.float64)
     N, d = Q.shape
     Nk, dv = V.shape
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    off = Nk - N
-    D = (dO * O).sum(axis=1)
-    dQ, dK, dV = np.zeros((N, d)), np.zeros((Nk, d)), np.zeros((Nk, dv))
-    visited = []
-    for j0 in range(0, Nk, Bc):
-        bc = min(Bc, Nk - j0)
-        dKj, dVj = np.zeros((bc, d)), np.zeros((bc, dv))
-        for i0 in range(0, N, Br):
-            br = min(Br, N - i0)
-            if causal and off + i0 + br - 1 < j0:
+    D = np.einsum("ic,ic->i", dO, O)
+    dQ, dK, dV, visited = np.zeros((N, d)), np.zeros((Nk, d)), np.zeros((Nk, dv)), []
+    for tj, (k_lo, k_hi) in enumerate(_tiles(Nk, Bc)):
+        Kj, Vj = K[k_lo:k_hi], V[k_lo:k_hi]
+        for ti, (q_lo, q_hi) in enumerate(_tiles(N, Br)):
+            if not tile_visible(N, Nk, causal, q_lo, q_hi, k_lo):
                 continue
-            visited.append((i0 // Br, j0 // Bc))
-            S = (Q[i0:i0 + br] @ K[j0:j0 + bc].T) * scale
-            if causal:
-                S = np.where(causal_mask(br, bc, i0, j0, off), S, -np.inf)
-            Li = L[i0:i0 + br, None]
-            with np.errstate(invalid="ignore"):
-                P = np.where(np.isneginf(Li), 0.0, np.exp(S - np.where(np.isneginf(Li), 0.0, Li)))
-            dVj += P.T @ dO[i0:i0 + br]
-            dP = dO[i0:i0 + br] @ V[j0:j0 + bc].T
-            dS = P * (dP - D[i0:i0 + br, None])
-            dQ[i0:i0 + br] += dS @ K[j0:j0 + bc] * scale
-            dKj += dS.T @ Q[i0:i0 + br] * scale
-        dK[j0:j0 + bc] = dKj
-        dV[j0:j0 + bc] = dVj
+            visited.append((ti, tj))
+            vis = visibility(N, Nk, causal, q_lo, q_hi, k_lo, k_hi)
+            Li = L[q_lo:q_hi]
+            finite = np.isfinite(Li)
+            S = scale * (Q[q_lo:q_hi] @ Kj.T)
+            P = np.exp(np.where(vis, S, NEG_INF) - np.where(finite, Li, 0.0)[:, None]) * finite[:, None]
+            g = dO[q_lo:q_hi]
+            dS = P * ((g @ Vj.T) - D[q_lo:q_hi, None])
+            dV[k_lo:k_hi] += P.T @ g
+            dK[k_lo:k_hi] += scale * (dS.T @ Q[q_lo:q_hi])
+            dQ[q_lo:q_hi] += scale * (dS @ Kj)
     return dQ, dK, dV, visited
 
 
 # --------------------------------------------------------------------------
-# section 4: flash-decoding (split KV, merge by log-sum-exp)
+# split-KV decoding
 # --------------------------------------------------------------------------
-def split_bounds(S, n_splits):
-    """Segment boundaries for splitting S keys into n_splits parts (linspace, rounded)."""
-    return np.linspace(0, S, n_splits + 1).round().astype(int)
+def split_bounds(n_keys, n_splits):
+    """n_splits + 1 near-equal integer cut points of [0, n_keys]: cut s is floor(s * n_keys / n_splits).
+    With more splits than keys some segments are empty."""
+    return [(s * n_keys) // n_splits for s in range(n_splits + 1)]
 
 
-def split_state(q, K, V, a, b, scale):
-    """Normalised output o_s and log-sum-exp lse_s of queries q over keys [a, b)."""
-    s = (q @ K[a:b].T) * scale
-    m = s.max(axis=1, keepdims=True)
-    p = np.exp(s - m)
-    l = p.sum(axis=1, keepdims=True)
-    return (p @ V[a:b]) / l, (m + np.log(l))[:, 0]
+def split_decode(q, K, V, n_splits, scale=None, bounds=None):
+    """Queries q [R, d] over keys K [n, d], values V [n, dv]: each non-empty segment of keys gives a
+    log-sum-exp-form state, and the states are merged with ``combine``.
 
-
-def merge_lse(parts):
-    """lse = log sum_s exp(lse_s) (max-shifted); o = sum_s exp(lse_s - lse) o_s."""
-    lses = np.stack([p[1] for p in parts])
-    top = lses.max(axis=0)
-    lse = top + np.log(np.exp(lses - top).sum(axis=0))
-    o = sum(np.exp(ls - lse)[:, None] * o_s for o_s, ls in parts)
-    return o, lse
-
-
-def split_kv_decode(q, K, V, n_splits, scale=None, bounds=None):
-    """Split the keys into segments, attend within each, merge.  Empty segments are skipped."""
+    Returns (o, lse, parts) with ``parts`` the per-segment (o_s, lse_s)."""
     q, K, V = (np.asarray(t, dtype=np.float64) for t in (q, K, V))
-    S, d = K.shape
-    scale = 1.0 / math.sqrt(d) if scale is None else scale
-    bounds = split_bounds(S, n_splits) if bounds is None else np.asarray(bounds)
-    parts = [split_state(q, K, V, a, b, scale) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
-    o, lse = merge_lse(parts)
+    scale = 1.0 / math.sqrt(q.shape[1]) if scale is None else scale
+    cuts = split_bounds(K.shape[0], n_splits) if bounds is None else list(bounds)
+    parts = [segment_state(scale * (q @ K[a:b].T), V[a:b]) for a, b in zip(cuts[:-1], cuts[1:]) if b > a]
+    o, lse = reduce(combine, parts)
     return o, lse, parts

@@ -53,6 +53,17 @@ def brute_attention(Q, K, V, causal, scale):
     return np.array(O), np.array(L)
 
 
+def brute_visible(N, Nk, causal):
+    """Boolean [N, Nk] visibility, element by element: query i at position Nk - N + i sees key j
+    when j is at or before that position ("02_flash_forward.py" demo 1)."""
+    out = np.ones((N, Nk), dtype=bool)
+    if causal:
+        for i in range(N):
+            for j in range(Nk):
+                out[i, j] = j <= Nk - N + i
+    return out
+
+
 def load_golden(name):
     with open(os.path.join(GOLDEN, name)) as f:
         g = json.load(f)

@@ -53,7 +53,7 @@ def magnitudes(q, k, v, do, causal, scale):
     Q, K, V, G = (to_np(t).reshape((-1,) + tuple(t.shape[-2:])) for t in (q, k, v, do))
     out = [[], [], []]
     for h in range(Q.shape[0]):
-        _, _, _, P, dS = no.standard_attention_bwd(Q[h], K[h], V[h], G[h], causal, scale, return_terms=True)
+        _, _, _, P, dS = no.attention_bwd_definition(Q[h], K[h], V[h], G[h], causal, scale, return_terms=True)
         R = (np.abs(G[h]) * (P @ np.abs(V[h]))).sum(axis=1)
         E = np.abs(dS) + P * R[:, None]
         out[0].append(scale * E @ np.abs(K[h]))

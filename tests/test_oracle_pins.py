@@ -23,7 +23,7 @@ def c_attention(Q, K, V, causal, scale):
 
 
 def np_attention(Q, K, V, causal, scale):
-    O, L, _ = no.standard_attention(Q, K, V, causal, scale)
+    O, L, _ = no.attention_definition(Q, K, V, causal, scale)
     return O, L
 
 
@@ -72,7 +72,7 @@ def test_invariants():
     s = 0.25
     O, L = oracle.attention(Q, K, V, causal=False, scale=s)
     # rows of P sum to 1
-    _, _, P = no.standard_attention(Q, K, V, False, s)
+    _, _, P = no.attention_definition(Q, K, V, False, s)
     assert np.abs(P.sum(axis=1) - 1).max() < 1e-13
     # a constant added to every score leaves O alone and shifts LSE (extra coordinate trick)
     c = 3.5
@@ -115,29 +115,49 @@ def test_large_values_stable():
 def test_online_softmax_equals_3pass():
     rng = np.random.default_rng(0)
     x = rng.standard_normal((5, 300)) * 4
-    assert np.abs(no.softmax_3pass(x) - no.softmax_online(x, block=37)).max() < 1e-15
+    assert np.abs(no.softmax_safe(x) - no.softmax_streaming(x, block=37)).max() < 1e-15
+    # a block that raises the maximum by far more than exp's range must rescale, not overflow
+    x[:, 200] += 900.0
+    assert np.abs(no.softmax_safe(x) - no.softmax_streaming(x, block=37)).max() < 1e-15
+
+
+def test_segment_state_is_the_library_definition():
+    """(o, lse) of one segment against scipy's logsumexp and softmax (independent library routines)."""
+    from scipy.special import logsumexp, softmax
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((7, 90)) * 5
+    x[3, :] = -np.inf  # a row with nothing visible
+    x[5, 10:] = -np.inf
+    v = rng.standard_normal((90, 3))
+    o, lse = no.segment_state(x, v)
+    live = np.arange(7) != 3
+    assert np.abs(lse[live] - logsumexp(x[live], axis=1)).max() < 1e-13
+    assert np.abs(o[live] - softmax(x[live], axis=1) @ v).max() < 1e-13
+    assert np.isneginf(lse[3]) and np.all(o[3] == 0)
 
 
 def test_merge_states_any_split_any_order():
     rng = np.random.default_rng(2)
     x = rng.standard_normal((6, 500)) * 3
     v = rng.standard_normal((500, 4))
-    mf, lf, of = no.partial_state(x, v)
+    o_full, lse_full = no.segment_state(x, v)
+    empty = (np.zeros((6, 4)), np.full(6, -np.inf))
     for trial in range(5):
         cuts = np.sort(rng.choice(np.arange(1, 500), size=rng.integers(1, 12), replace=False))
         bounds = [0, *cuts.tolist(), 500]
-        states = [no.partial_state(x[:, a:b], v[a:b]) for a, b in zip(bounds[:-1], bounds[1:])]
+        states = [no.segment_state(x[:, a:b], v[a:b]) for a, b in zip(bounds[:-1], bounds[1:])]
         # an empty (fully masked) segment must not change anything
-        states.append((np.full(6, -np.inf), np.zeros(6), np.zeros((6, 4))))
+        states.append(empty)
         order = rng.permutation(len(states))
         pool = [states[i] for i in order]
         while len(pool) > 1:  # random tree: merge a random adjacent pair
             k = int(rng.integers(0, len(pool) - 1))
-            pool[k:k + 2] = [no.merge_states(pool[k], pool[k + 1])]
-        m, l, o = pool[0]
-        assert np.abs(m - mf).max() == 0
-        assert np.abs(l / lf - 1).max() < 1e-13
-        assert np.abs(o - of).max() < 1e-12
+            pool[k:k + 2] = [no.combine(pool[k], pool[k + 1])]
+        o, lse = pool[0]
+        assert np.abs(lse - lse_full).max() < 1e-13
+        assert np.abs(o - o_full).max() < 1e-12
+    o, lse = no.combine(empty, empty)
+    assert np.all(o == 0) and np.all(np.isneginf(lse))
 
 
 @pytest.mark.parametrize("n_splits", [1, 3, 16, 999])
@@ -145,7 +165,7 @@ def test_split_kv_decode_equals_oracle(n_splits):
     rng = np.random.default_rng(0)
     q = rng.standard_normal((4, 32))
     K, V = rng.standard_normal((1000, 32)), rng.standard_normal((1000, 32))
-    o, lse, parts = no.split_kv_decode(q, K, V, n_splits)
+    o, lse, parts = no.split_decode(q, K, V, n_splits)
     O, L = oracle.attention(q, K, V, causal=False, scale=1 / math.sqrt(32))
     assert np.abs(o - O).max() < 1e-13 and np.abs(lse - L).max() < 1e-13
     # the C combine of the same split states, in a shuffled order, agrees too
@@ -172,10 +192,10 @@ def test_tiled_model_matches_oracle_and_skips_exactly_masked_tiles(N, Nk, Br, Bc
     Q, K, V = rng.standard_normal((N, d)), rng.standard_normal((Nk, d)), rng.standard_normal((Nk, d))
     for causal in (False, True):
         O, L = oracle.attention(Q, K, V, causal=causal, scale=0.25)
-        Ot, Lt, visited = no.flash_fwd_tiled(Q, K, V, Br, Bc, causal, scale=0.25)
+        Ot, Lt, visited = no.tiled_forward(Q, K, V, Br, Bc, causal, scale=0.25)
         assert pins._close(Ot, O, 1e-12) and pins._close(Lt, L, 1e-12)
         # a tile is visited iff some element of it is visible (the skip rule drops only fully masked tiles)
-        allowed = no.causal_mask(N, Nk, offset=Nk - N) if causal else np.ones((N, Nk), bool)
+        allowed = pins.brute_visible(N, Nk, causal)
         expect = {(i // Br, j // Bc) for i in range(0, N, Br) for j in range(0, Nk, Bc)
                   if allowed[i:i + Br, j:j + Bc].any()}
         assert set(visited) == expect
@@ -267,7 +287,7 @@ def c_attention_bwd(Q, K, V, dO, causal, scale, lib=None):
 
 
 def np_attention_bwd(Q, K, V, dO, causal, scale):
-    return no.standard_attention_bwd(Q, K, V, dO, causal, scale)
+    return no.attention_bwd_definition(Q, K, V, dO, causal, scale)
 
 
 @pytest.mark.parametrize("impl", [c_attention_bwd, np_attention_bwd], ids=["c", "numpy"])
@@ -286,11 +306,11 @@ def test_tiled_bwd_model_matches_oracle_and_skips_exactly_masked_tiles(N, Nk, Br
     dO = rng.standard_normal((N, dv))
     for causal in (False, True):
         O, L = oracle.attention(Q, K, V, causal=causal, scale=0.3)
-        dQ, dK, dV, visited = no.flash_bwd_tiled(Q, K, V, O, dO, L, Br, Bc, causal, 0.3)
+        dQ, dK, dV, visited = no.tiled_backward(Q, K, V, O, dO, L, Br, Bc, causal, 0.3)
         ref = oracle.attention_bwd(Q, K, V, dO, causal=causal, scale=0.3)
         for a, b in zip((dQ, dK, dV), ref):
             assert np.abs(a - b).max() < 1e-12
-        mask = no.causal_mask(N, Nk, offset=Nk - N) if causal else np.ones((N, Nk), bool)
+        mask = pins.brute_visible(N, Nk, causal)
         want = {(i, j) for i in range(-(-N // Br)) for j in range(-(-Nk // Bc))
                 if mask[i * Br:(i + 1) * Br, j * Bc:(j + 1) * Bc].any()}
         assert set(visited) == want
