@@ -32,6 +32,14 @@
 //                    hundred cycles, so each issuer handles only its own query tile,
 //                    and K_j / V_j share one barrier.
 //   warp 11          idle (completes the control warpgroup).
+// For d = 128 without a mask (kernels with long, uniform items whose row-store epilogue is
+// costly) a fourth warpgroup, warps 12-15, takes the epilogue of both query tiles: once an
+// item's last P V has completed it reads O_i out of TMEM, releases the columns for the next
+// item's first P V and stores O / l, while the softmax warps hand over 1 / l and move on to
+// the next item at once (its S already computed).  The control warpgroup is then warps 8-11 as
+// above.  (For d <= 64, and under a causal mask, this role costs more than it saves: the
+// softmax warpgroups lose the registers it takes, and with short causal items one warpgroup
+// doing both tiles' epilogues falls behind.)
 // Tensor memory (512 columns): S0, S1 (128 fp32 columns each), O0, O1 (d each) and
 // P0, P1 (64 columns of packed bf16 each).  For d = 128 there is no room left, so
 // P_i overwrites the first half of S_i (already read into registers); S_i(j+1) is
@@ -64,6 +72,13 @@ namespace fa {
 constexpr int kFwdThreads = 384;  // 12 warps = 3 warpgroups
 constexpr int kWarpProducer = 8;
 constexpr int kWarpMma = 9;       // warps 9 and 10 issue the MMAs of Q0 and Q1; warp 11 idles
+constexpr int kWarpCorr = 12;     // warps 12-15: correction warpgroup (kernels with kCorr only)
+
+// Whether the kernel has a correction warpgroup (16 warps) doing the epilogue.
+template <int D, bool CAUSAL>
+constexpr bool kCorr = D == 128 && !CAUSAL;
+template <int D, bool CAUSAL>
+constexpr int kThreads = kCorr<D, CAUSAL> ? 512 : kFwdThreads;
 // Registers per thread after the split: the producer / MMA warpgroup gives registers to the
 // two softmax warpgroups.  The split needs kFwdThreads * (registers at launch) >=
 // 256 * kSoftmaxRegs + 128 * kControlRegs; the launcher checks this before every launch,
@@ -74,6 +89,11 @@ template <int D>
 constexpr int kSoftmaxRegs = D == 128 ? 224 : 216;
 template <int D>
 constexpr int kControlRegs = D == 128 ? 56 : 72;
+// With a correction warpgroup (512 threads, 128 registers each at launch): 256 * 184 + 128 * 72
+// + 128 * 72 = 65536, the splits for which ptxas reports no spills in any role.
+constexpr int kCorrSoftmaxRegs = 184;
+constexpr int kCorrRegs = 72;
+constexpr int kCorrControlRegs = 72;
 
 // barrier slots
 constexpr int kMaxStages = 8;
@@ -88,7 +108,9 @@ enum : int {
     kBarSFree = 18,                         // +tile (2): the softmax has read S_i out of TMEM
     kBarKVFull = 20,                        // +stage: K_j and V_j landed
     kBarKVEmpty = kBarKVFull + kMaxStages,  // +stage: both issuers are done with the stage
-    kBarCount = kBarKVEmpty + kMaxStages
+    kBarLFull = kBarKVEmpty + kMaxStages,   // +tile (2): the softmax wrote the item's 1 / l rows (kCorr)
+    kBarOFree = kBarLFull + 2,              // +tile (2): the correction warps read O_i and 1 / l (kCorr)
+    kBarCount = kBarOFree + 2
 };
 
 template <int D, int OutBytes>
@@ -117,7 +139,8 @@ struct FwdCfg {
     static constexpr bool kAlternate = D <= 64;  // causal items alternate their query tiles (decode_item)
     static constexpr int kOffStage = kOffV + kStages * kTileBytes;
     static constexpr int kStageTileBytes = kStoreO ? kBlockM * D * OutBytes : 0;
-    static constexpr int kOffBar = kOffStage + 2 * kStageTileBytes;
+    static constexpr int kOffInvL = kOffStage + 2 * kStageTileBytes;  // fp32 1 / l per row (kCorr)
+    static constexpr int kOffBar = kOffInvL + (D == 128 ? 2 * kBlockM * 4 : 0);
     static constexpr int kNumBars = 48;
     static_assert(kStages <= kMaxStages && kBarCount <= kNumBars, "barrier slots");
     static constexpr int kUsedBytes = kOffBar + kNumBars * 8 + 16 + 1024;  // + 1 KB alignment slack
@@ -269,8 +292,70 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, const ItemCursor
     return it;
 }
 
+// Correction warpgroup (kCorr kernels, d = 128): the epilogue of both query tiles.  Warp w reads
+// TMEM lanes 32 (w mod 4) .. 32 (w mod 4) + 31, i.e. those rows of O0 and of O1.  For each item
+// and query tile with rows: once the item's last P V has completed (OReady) and the softmax has
+// written the rows' 1 / l (LFull), it reads O_i 32 columns at a time and stores the rows of
+// O / l; then it releases the columns (OFree: the next item's first P V may overwrite them and
+// the softmax may write the next 1 / l).
 template <int D, bool CAUSAL, typename OutT>
-__global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p)
+__device__ __forceinline__ void fwd_correction(const FwdParams& p, const uint8_t* smem, uint32_t bar0, uint32_t tmem,
+                                               volatile int* abort_flag)
+{
+    using C = FwdCfg<D, static_cast<int>(sizeof(OutT))>;
+    auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int r = 32 * (warp & 3) + lane;  // row within a query tile == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+    const float* inv_l = reinterpret_cast<const float*>(smem + C::kOffInvL);
+    const unsigned long long limit = p.wait_limit_ns;
+    int done[2] = {0, 0};  // items whose O_i this warpgroup has read, per query tile
+    bool ok = true;
+    for (ItemCursor cur = first_item(p, CAUSAL && p.pairs); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs)) {
+        const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int rows = it.rows[i];
+            if (rows == 0) continue;  // tile lies past N
+            const int n = it.n[i];
+            if (n > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOReady + i), done[i] & 1, limit, abort_flag) &&
+                                                 mbar_wait(bar(kBarLFull + i), done[i] & 1, limit, abort_flag));
+                if (!ok) break;
+                tc_fence_after_sync();
+            }
+            const float inv = n > 0 ? inv_l[i * kBlockM + r] : 0.f;
+            const bool valid = r < rows;
+            OutT* orow = reinterpret_cast<OutT*>(p.o) + (static_cast<size_t>(it.bh) * p.N + static_cast<size_t>(it.r0[i] + r)) * D;
+            const uint32_t t_o = tmem + lane_base + C::col_o(i);
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                float v[32];
+                if (n > 0) {
+                    uint32_t o[32];
+                    tmem_ld32(t_o + 32u * c, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0.f;
+                }
+                if (valid) store_row32<OutT>(orow + 32 * c, v);
+            }
+            if (n > 0) {
+                tc_fence_before_sync();
+                mbar_arrive(bar(kBarOFree + i));
+                ++done[i];
+            }
+        }
+    }
+    if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+}
+
+template <int D, bool CAUSAL, typename OutT>
+__global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p)
 {
     using C = FwdCfg<D, static_cast<int>(sizeof(OutT))>;
     constexpr int S = C::kStages;
@@ -299,6 +384,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             mbar_init(bar(kBarOReady + i), 1);
             mbar_init(bar(kBarDrain + i), 1);
             mbar_init(bar(kBarSFree + i), kBlockM);
+            mbar_init(bar(kBarLFull + i), kBlockM);
+            mbar_init(bar(kBarOFree + i), kBlockM);
         }
         for (int s = 0; s < S; ++s) {
             mbar_init(bar(kBarKVFull + s), 1);
@@ -316,8 +403,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp >= kWarpProducer) {
-      regs_decrease<kControlRegs<D>>();
+    constexpr bool kWithCorr = kCorr<D, CAUSAL>;
+    if (kWithCorr && warp >= kWarpCorr) {
+        if constexpr (kWithCorr) {
+            regs_decrease<kCorrRegs>();
+            // ============================================================ correction / epilogue
+            fwd_correction<D, CAUSAL, OutT>(p, smem, bar0, tmem, abort_flag);
+        }
+    } else if (warp >= kWarpProducer) {
+      regs_decrease<kWithCorr ? kCorrControlRegs : kControlRegs<D>>();
       if (warp == kWarpProducer) {
         // ============================================================ producer
         if (lane == 0) {
@@ -466,6 +560,13 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
                             break;
                         }
                     }
+                    // With a correction warpgroup, the first P V of an item (which overwrites O_i)
+                    // waits until the correction warps have read the previous item's O_i.
+                    if (kWithCorr && j == 0 && q_uses > 0 &&
+                        !mbar_wait(bar(kBarOFree + i), (q_uses - 1) & 1, limit, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     if (!mbar_wait(bar(kBarPFull + i), tiles & 1, limit, abort_flag)) {
                         ok = false;
                         break;
@@ -496,7 +597,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
         }
       }
     } else {
-        regs_increase<kSoftmaxRegs<D>>();
+        regs_increase<kWithCorr ? kCorrSoftmaxRegs : kSoftmaxRegs<D>>();
         // ============================================================ softmax + epilogue
         const int wg = warp >> 2;               // query tile of this warpgroup
         const int r = threadIdx.x & 127;        // row within the tile == TMEM lane
@@ -623,6 +724,23 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fa_fwd_kernel(const __grid_con
             }
             if (!ok) break;
             if (rows == 0) continue;  // tile lies past N: nothing to write
+            if constexpr (kWithCorr) {
+                // Hand 1 / l to the correction warps (once they have read the previous item's),
+                // write LSE and move on: the correction warps store O / l.
+                if (n > 0) {
+                    if (items > 0) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOFree + wg), (items - 1) & 1, limit, abort_flag));
+                        if (!ok) break;
+                    }
+                    reinterpret_cast<float*>(smem + C::kOffInvL)[wg * kBlockM + r] = l > 0.f ? 1.f / l : 0.f;
+                    mbar_arrive(bar(kBarLFull + wg));
+                    ++items;
+                }
+                if (p.lse != nullptr && r < rows)
+                    p.lse[static_cast<size_t>(it.bh) * p.N + static_cast<size_t>(row0 + r)] =
+                        l > 0.f ? (m_run + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+                continue;
+            }
             if (n > 0) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(kBarOReady + wg), items & 1, limit, abort_flag));
                 if (!ok) break;
@@ -718,7 +836,10 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
         regs[dev] = attr.numRegs;
     }
     const int launch_regs = (dev >= 0 && dev < 64) ? regs[dev] : 0;
-    if (launch_regs * kFwdThreads < 256 * kSoftmaxRegs<D> + 128 * kControlRegs<D>)
+    constexpr bool kWithCorr = kCorr<D, CAUSAL>;
+    constexpr int kNeed = kWithCorr ? 256 * kCorrSoftmaxRegs + 128 * (kCorrRegs + kCorrControlRegs)
+                                    : 256 * kSoftmaxRegs<D> + 128 * kControlRegs<D>;
+    if (launch_regs * kThreads<D, CAUSAL> < kNeed)
         return cudaErrorLaunchOutOfResources;  // the register split would not fit
     FwdParams q = p;
     // Pairs balance causal work over several rounds; with no more items than CTAs every item gets
@@ -729,7 +850,7 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
     const long long step = q.pairs ? 2LL * grid - 1 : grid;  // see next_item
     q.step_heads = static_cast<int>(step / p.n_qp);
     q.step_rem = static_cast<int>(step % p.n_qp);
-    kern<<<grid, kFwdThreads, C::kSmemBytes, st>>>(q);
+    kern<<<grid, kThreads<D, CAUSAL>, C::kSmemBytes, st>>>(q);
     return cudaGetLastError();
 }
 
