@@ -219,7 +219,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     if args.decode_only:
-        decode = run_decode(fa, dev, stream, args, world)
+        decode = run_decode(fa, dev, stream, args, world, rank)
         gqa = [run_decode_gqa(fa, dev, stream, args, world, Hkv=h) for h in (8, 4)]
         pre = run_splitkv_prefill(fa, dev, stream, args, world)
         if rank == 0:
@@ -273,8 +273,9 @@ def run_ours(args, world, rank, local):
     barrier(world)
     clocks = sampler.stop()
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
-    nc_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    c_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    nc_all = [e[0].elapsed_time(e[1]) for e in evs]
+    c_all = [e[2].elapsed_time(e[3]) for e in evs]
+    nc_ms, c_ms = statistics.mean(nc_all), statistics.mean(c_all)
     assert fa.get_device_error(dev) == fa.FA_OK
     value = world * args.steps * (f_nc + f_c) / (total_ms / 1e3) / 1e12
 
@@ -285,8 +286,9 @@ def run_ours(args, world, rank, local):
 
     # ---- split-KV decode in the same run
     decode = None
+    hbm = measure_hbm_peaks(dev, stream)
     if not args.no_decode:
-        decode = run_decode(fa, dev, stream, args, world)
+        decode = run_decode(fa, dev, stream, args, world, rank, hbm)
 
     pk, pk_src = peaks()
     peak = float(pk["bf16_tflops"])
@@ -301,15 +303,20 @@ def run_ours(args, world, rank, local):
                    "flops_per_step": f_nc + f_c, "l2": "inputs 403 MB > 129 MB L2 (no flush needed)",
                    "parallelism": f"replicas x{world}"},
         "kernels": {
-            "fa_fwd non-causal": {"ms": nc_ms, "tflops": achieved, "frac_of_peak": achieved / peak},
+            "fa_fwd non-causal": {"ms": nc_ms, "tflops": achieved, "frac_of_peak": achieved / peak,
+                                  "timing": {"ms_median": statistics.median(nc_all), "ms_min": min(nc_all),
+                                             "ms_max": max(nc_all), "calls": len(nc_all)}},
             "fa_fwd causal": {"ms": c_ms, "tflops": f_c / (c_ms / 1e3) / 1e12,
-                              "frac_of_peak": f_c / (c_ms / 1e3) / 1e12 / peak},
+                              "frac_of_peak": f_c / (c_ms / 1e3) / 1e12 / peak,
+                              "timing": {"ms_median": statistics.median(c_all), "ms_min": min(c_all),
+                                         "ms_max": max(c_all), "calls": len(c_all)}},
         },
         "roofline": {"kernel": "fa_fwd_kernel<64, non-causal, bf16>", "bound": "tensor", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"{pk_src} bf16_tflops (burst; kernel timed in short launches)",
                      "algorithmic_flops_per_launch": f_nc},
         "e2e": e2e,
+        "hbm_peaks_live": hbm,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
@@ -318,7 +325,7 @@ def run_ours(args, world, rank, local):
         line["decode_gqa"] = [run_decode_gqa(fa, dev, stream, args, world, Hkv=h) for h in (8, 4)]
         line["splitkv_prefill"] = run_splitkv_prefill(fa, dev, stream, args, world)
     if not args.no_extra:
-        line["other_fwd_configs"] = run_other_fwd(fa, dev, stream, args, world)
+        line["other_fwd_configs"] = run_other_fwd(fa, dev, stream, args, world, rank)
     if not args.no_bwd:
         line["backward"] = run_bwd(fa, dev, stream, args, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -400,42 +407,143 @@ def run_e2e(fa, dev, stream, args, world, inputs, outputs, scale, flops_per_step
 
 
 # The other forward configurations of the parity suite, timed the same way (not the headline):
-# (name, B, H, N, Nk, d, input multiplier, causal)
+# (name, B, H, N, Nk, d, input multiplier, causal, oracle sample: heads, query rows or None for all)
 OTHER_FWD = (
-    ("single head 256x256 d=64", 1, 1, 256, 256, 64, 1.0, False),
-    ("single head 256x256 d=64 causal", 1, 1, 256, 256, 64, 1.0, True),
-    ("ragged 4097 d=128 x2", 4, 16, 4097, 4097, 128, 2.0, False),
-    ("ragged 4097 d=128 x2 causal", 4, 16, 4097, 4097, 128, 2.0, True),
-    ("ragged 77x513 d=32 x2 causal", 8, 8, 77, 513, 32, 2.0, True),
-    ("long causal 16384 d=128", 2, 32, 16384, 16384, 128, 1.0, True),
+    ("single head 256x256 d=64", 1, 1, 256, 256, 64, 1.0, False, 1, None),
+    ("single head 256x256 d=64 causal", 1, 1, 256, 256, 64, 1.0, True, 1, None),
+    ("ragged 4097 d=128 x2", 4, 16, 4097, 4097, 128, 2.0, False, 4, None),
+    ("ragged 4097 d=128 x2 causal", 4, 16, 4097, 4097, 128, 2.0, True, 4, None),
+    ("ragged 77x513 d=32 x2", 8, 8, 77, 513, 32, 2.0, False, 64, None),
+    ("ragged 77x513 d=32 x2 causal", 8, 8, 77, 513, 32, 2.0, True, 64, None),
+    ("long causal 16384 d=128", 2, 32, 16384, 16384, 128, 1.0, True, 4, (0, 2048)),
 )
 
 
-def run_other_fwd(fa, dev, stream, args, world):
+def visible_pairs(N, Nk, causal, r0=0, r1=None):
+    """(query, key) pairs that attend: all of them without a mask; with one, query i (position
+    Nk - N + i) sees keys 0 .. Nk - N + i."""
+    r1 = N if r1 is None else r1
+    if not causal:
+        return (r1 - r0) * Nk
+    off = Nk - N
+    return sum(min(Nk, max(0, off + i + 1)) for i in range(r0, r1))
+
+
+def time_stats(call, dev, stream, world, warmup=3, min_calls=100, min_s=0.5, blocks=5, max_block=10000):
+    """Milliseconds per call from `blocks` blocks of back-to-back calls, each block timed with
+    CUDA events on `stream`; blocks are sized so that together they make at least `min_calls`
+    calls and last at least `min_s` seconds.  Returns the median, min and max block (max over
+    ranks) and the number of timed calls."""
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(3):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    est = max(e0.elapsed_time(e1) / 3, 1e-4)
+    per_block = max(math.ceil(min_calls / blocks), math.ceil(min_s * 1e3 / blocks / est))
+    per_block = min(per_block, max_block)
+    times = []
+    for _ in range(blocks):
+        e0.record(stream)
+        for _ in range(per_block):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        times.append(max_over_ranks(e0.elapsed_time(e1) / per_block, world))
+    return {"ms": statistics.median(times), "ms_min": min(times), "ms_max": max(times), "calls": per_block * blocks}
+
+
+def oracle_fwd_sample(B, H, N, Nk, d, mult, causal, heads, rows, seed=0):
+    """Time the FP64 C oracle on `heads` of the B*H heads (inputs drawn on the host from the
+    workload's distribution) over query rows `rows` (all when None).  Returns a cpu_baseline dict
+    with the sample's time and TFLOP/s and the time of the full configuration extrapolated by
+    FLOPs (labelled as such)."""
+    import oracle
+    oracle.build()
+    g = torch.Generator().manual_seed(seed)
+    q, k, v = (torch.randn(shape, generator=g).to(torch.bfloat16) * mult
+               for shape in ((heads, N, d), (heads, Nk, d), (heads, Nk, d)))
+    threads = oracle.cores()
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, causal=causal, scale=1 / math.sqrt(d), rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    r0, r1 = rows if rows is not None else (0, N)
+    fl = 4.0 * d * heads * visible_pairs(N, Nk, causal, r0, r1)
+    full = 4.0 * d * B * H * visible_pairs(N, Nk, causal)
+    desc = f"{heads} of {B * H} heads" + (f", query rows {r0}..{r1 - 1}" if rows is not None else ", all rows")
+    return {"value": fl / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle", "seconds": dt,
+            "sample": desc + f", FP64 C oracle on {threads} threads (visible-pair FLOPs)",
+            "full_config_seconds_extrapolated": dt * full / fl}
+
+
+def run_other_fwd(fa, dev, stream, args, world, rank):
     pk, _ = peaks()
     peak = float(pk["bf16_tflops"])
     out = {}
-    for name, B, H, N, Nk, d, mult, causal in OTHER_FWD:
+    for name, B, H, N, Nk, d, mult, causal, o_heads, o_rows in OTHER_FWD:
         q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=0, mult=mult, device=dev)
         o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
-        for _ in range(max(args.warmup, 3)):
-            fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
-        steps = max(5, args.steps // 10)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(steps):
-            fa.fwd(q, k, v, causal=causal, out=o, lse=lse)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+        call = lambda: fa.fwd(q, k, v, causal=causal, out=o, lse=lse)  # noqa: E731
+        st = time_stats(call, dev, stream, world, warmup=max(args.warmup, 3))
         fl = fwd_flops(B, H, N, Nk, d, causal)
-        out[name] = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12, "frac_of_peak": fl / (ms / 1e3) / 1e12 / peak,
-                     "flops": fl}
+        fl_exact = 4.0 * d * B * H * visible_pairs(N, Nk, causal)
+        ms = st["ms"]
+        rec = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12, "frac_of_peak": fl / (ms / 1e3) / 1e12 / peak,
+               "flops": fl, "flops_exact_visible_pairs": fl_exact,
+               "tflops_exact": fl_exact / (ms / 1e3) / 1e12, "timing": st}
+        if ms < 0.05:  # launch-bound: also the per-call time with no host launch cost (CUDA graph of 20 calls)
+            rec["graph_us_per_call"] = graph_us(call, dev, stream, world)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            rec["cpu_baseline"] = oracle_fwd_sample(B, H, N, Nk, d, mult, causal, o_heads, o_rows)
+        out[name] = rec
         del q, k, v, o, lse
     assert fa.get_device_error(dev) == fa.FA_OK
     return out
+
+
+def measure_hbm_peaks(dev, stream):
+    """Live HBM denominators on this GPU: a device-to-device copy of 2 GiB (read + write bytes)
+    and two read-dominated streams over a 4 GiB bf16 matrix (cuBLAS GEMV, which reads the matrix
+    once, and a sum reduction); best of 10 each, CUDA events."""
+    n = 1 << 30
+    a = torch.empty(n, dtype=torch.bfloat16, device=dev).uniform_()
+    b = torch.empty_like(a)
+    A = torch.empty((1 << 16, 1 << 15), dtype=torch.bfloat16, device=dev).uniform_()
+    x = torch.empty(1 << 15, dtype=torch.bfloat16, device=dev).uniform_()
+
+    def best(fn, nbytes):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ms = []
+        for _ in range(10):
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            ms.append(e0.elapsed_time(e1))
+        return nbytes / (min(ms) / 1e3) / 1e9
+
+    copy = best(lambda: b.copy_(a), 2 * a.numel() * 2)
+    gemv = best(lambda: torch.mv(A, x), A.numel() * 2)
+    red = best(lambda: A.view(torch.int64).max(), A.numel() * 2)
+    del a, b, A, x
+    torch.cuda.empty_cache()
+    return {"copy_gbs": copy, "read_gemv_gbs": gemv, "read_max_gbs": red,
+            "method": "best of 10 CUDA-event-timed launches: b.copy_(a) over 1 Gi bf16 (read + write bytes); "
+                      "torch.mv of a [65536, 32768] bf16 matrix (cuBLAS GEMV) and the int64 max reduction of "
+                      "the same 4 GiB (read only)"}
+
+
+# DRAM peak that ncu's gpu__dram_throughput is a percentage of, on this GB300 pool: the decode
+# capture in profiles/fa_decode_split_kernel_d128.md reads 6.76 TB/s at 85.4 % of it.
+NCU_DRAM_PEAK_GBS = 6760.0 / 0.854
 
 
 def bwd_flops(B, H, N, Nk, d, causal):
@@ -457,27 +565,39 @@ def run_bwd(fa, dev, stream, args, world):
            "peak_source": f"{src} bf16_tflops"}
     for causal in (False, True):
         o, lse = fa.fwd(q, k, v, causal=causal)
-        for _ in range(max(args.warmup, 3)):
-            fa.bwd(q, k, v, o, lse, do, causal=causal, grads=grads, workspace=ws)
-        steps = max(5, args.steps // 10)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
         barrier(world)
-        e0.record(stream)
-        for _ in range(steps):
-            fa.bwd(q, k, v, o, lse, do, causal=causal, grads=grads, workspace=ws)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+        st = time_stats(lambda: fa.bwd(q, k, v, o, lse, do, causal=causal, grads=grads, workspace=ws),
+                        dev, stream, world, warmup=max(args.warmup, 3))
+        ms = st["ms"]
         fl = bwd_flops(B, H, N, Nk, d, causal)
         tf = world * fl / (ms / 1e3) / 1e12
         out["causal" if causal else "non-causal"] = {"ms": ms, "tflops": tf, "frac_of_peak": tf / peak / world,
-                                                     "flops": fl}
+                                                     "flops": fl, "timing": st}
     assert fa.get_device_error(dev) == fa.FA_OK
     return out
 
 
-def run_decode(fa, dev, stream, args, world):
+def oracle_decode_all(q, k, v, lens):
+    """Time the FP64 C oracle on every (sequence, head) of a decode batch: each sequence's valid
+    cache prefix is copied to the host first (outside the timed region)."""
+    import oracle
+    oracle.build()
+    threads = oracle.cores()
+    dt, kv_bytes = 0.0, 0
+    for b, n in enumerate(lens.tolist()):
+        qb = q[b:b + 1].cpu()
+        kb = k[b:b + 1, :, :n].contiguous().cpu()
+        vb = v[b:b + 1, :, :n].contiguous().cpu()
+        t0 = time.perf_counter()
+        oracle.decode(qb, kb, vb, [n], threads=threads)
+        dt += time.perf_counter() - t0
+        kv_bytes += 2 * kb.numel() * 2
+    return {"value": kv_bytes / dt / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle", "seconds": dt,
+            "sample": f"all {q.shape[0] * q.shape[1]} (sequence, head) pairs, FP64 C oracle on {threads} threads "
+                      "(bf16 K/V bytes of the cached prefixes / time)"}
+
+
+def run_decode(fa, dev, stream, args, world, rank=0, hbm=None):
     B, H, Nk_max, d = DEC["B"], DEC["H"], DEC["Nk_max"], DEC["d"]
     q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=0, lo=DEC["lo"], hi=DEC["hi"], device=dev)
     lens_d = lens.to(dev)
@@ -485,19 +605,11 @@ def run_decode(fa, dev, stream, args, world):
     ws = torch.empty(fa.decode_workspace_size(B, H, d, n), dtype=torch.uint8, device=dev)
     o = torch.empty((B, H, 1, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
-    for _ in range(args.warmup):
-        fa.decode_splitkv(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
-    torch.cuda.synchronize(dev)
-    steps = max(args.steps // 4, 5)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    e0.record(stream)
-    for _ in range(steps):
-        fa.decode_splitkv(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    st = time_stats(lambda: fa.decode_splitkv(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws),
+                    dev, stream, world, warmup=max(args.warmup, 3))
     barrier(world)
-    ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+    ms = st["ms"]
     assert fa.get_device_error(dev) == fa.FA_OK
     kv_bytes = sum(2 * H * int(n_b) * d * 2 for n_b in lens.tolist())
     other = B * H * (d * 2 + d * 2 + 4)
@@ -506,7 +618,8 @@ def run_decode(fa, dev, stream, args, world):
     # the same decode with the combine fused into the split kernel (one launch per call)
     wsf = fa.decode_fused_workspace(B, H, Nk_max, d, n_splits=n, device=dev)
     fused = lambda: fa.decode_splitkv_fused(q, k, v, lens_d, wsf, n_splits=n, out=o, lse=lse)  # noqa: E731
-    ms_f = time_calls(fused, dev, stream, max(args.warmup, 3), steps, world)
+    st_f = time_stats(fused, dev, stream, world, warmup=max(args.warmup, 3))
+    ms_f = st_f["ms"]
     # a short-context decode, where the second launch is a visible share of the call
     qs, ks, vs, ls = decode_inputs(1, 32, 2048, d, d, seed=1, lo=2048, hi=2048, device=dev)
     ls_d = ls.to(dev)
@@ -514,26 +627,35 @@ def run_decode(fa, dev, stream, args, world):
     ns = fa.decode_default_splits(1, 32, 2048, fa.num_sms(dev))
     ws2 = torch.empty(fa.decode_workspace_size(1, 32, d, ns), dtype=torch.uint8, device=dev)
     wsf2 = fa.decode_fused_workspace(1, 32, 2048, d, n_splits=ns, device=dev)
+    two = lambda: fa.decode_splitkv(qs, ks, vs, ls_d, n_splits=ns, out=os_, workspace=ws2, return_lse=False)  # noqa: E731
+    one = lambda: fa.decode_splitkv_fused(qs, ks, vs, ls_d, wsf2, n_splits=ns, out=os_, return_lse=False)  # noqa: E731
     short = {"workload": f"B=1 H=32 Nk=2048 d={d}", "n_splits": ns,
-             "two_launches_us": 1e3 * time_calls(lambda: fa.decode_splitkv(qs, ks, vs, ls_d, n_splits=ns, out=os_,
-                                                                           workspace=ws2, return_lse=False),
-                                                 dev, stream, 5, 50, world),
-             "fused_us": 1e3 * time_calls(lambda: fa.decode_splitkv_fused(qs, ks, vs, ls_d, wsf2, n_splits=ns, out=os_,
-                                                                          return_lse=False),
-                                          dev, stream, 5, 50, world)}
-    # the same calls replayed from a CUDA graph of 20 calls: no per-call launch cost
-    short["graph_two_launches_us"] = graph_us(lambda: fa.decode_splitkv(qs, ks, vs, ls_d, n_splits=ns, out=os_,
-                                                                        workspace=ws2, return_lse=False),
-                                              dev, stream, world)
-    short["graph_fused_us"] = graph_us(lambda: fa.decode_splitkv_fused(qs, ks, vs, ls_d, wsf2, n_splits=ns, out=os_,
-                                                                       return_lse=False),
-                                       dev, stream, world)
+             "two_launches_us": 1e3 * time_stats(two, dev, stream, world)["ms"],
+             "fused_us": 1e3 * time_stats(one, dev, stream, world)["ms"],
+             # the same calls replayed from a CUDA graph of 20 calls: no per-call launch cost
+             "graph_two_launches_us": graph_us(two, dev, stream, world),
+             "graph_fused_us": graph_us(one, dev, stream, world)}
     assert fa.get_device_error(dev) == fa.FA_OK
-    return {"workload": "split-KV decode B=16 H=32 d=128, lengths U[1024,32768] (seed 0), bf16 O",
-            "n_splits": n, "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
-            "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2,
-            "fused_combine": {"ms": ms_f, "gbs": world * (kv_bytes + other) / (ms_f / 1e3) / 1e9, "launches_per_call": 1},
-            "short_context": short}
+    out = {"workload": "split-KV decode B=16 H=32 d=128, lengths U[1024,32768] (seed 0), bf16 O",
+           "n_splits": n, "ms": ms, "timing": st, "gbs": gbs, "kv_bytes": kv_bytes,
+           "frac_of_hbm": gbs / float(pk["hbm_gbs"]), "frac_of_8tbs": gbs / 8000.0, "peak_source": src,
+           "launches_per_call": 2,
+           "fused_combine": {"ms": ms_f, "timing": st_f, "gbs": world * (kv_bytes + other) / (ms_f / 1e3) / 1e9,
+                             "launches_per_call": 1},
+           "short_context": short}
+    if hbm is not None:
+        # against the larger of the live copy and read-stream bandwidths of this GPU
+        read_peak = max(hbm["copy_gbs"], hbm["read_gemv_gbs"], hbm["read_max_gbs"])
+        out["frac_of_live_read_peak"] = gbs / world / read_peak
+        out["live_read_peak_gbs"] = read_peak
+    # every library stream measured reads slower than this kernel, so the bound that holds is the
+    # DRAM peak ncu reports throughput against
+    out["frac_of_ncu_dram_peak"] = gbs / world / NCU_DRAM_PEAK_GBS
+    if out["frac_of_ncu_dram_peak"] > 1.0:
+        print(f"warning: decode at {out['frac_of_ncu_dram_peak']:.3f} of the DRAM peak: timing suspect", file=sys.stderr)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = oracle_decode_all(q, k, v, lens)
+    return out
 
 
 def graph_us(call, dev, stream, world, reps=20):
@@ -580,26 +702,18 @@ def run_decode_gqa(fa, dev, stream, args, world, Hkv=None):
     ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n_auto), dtype=torch.uint8, device=dev)
     o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
-    for _ in range(max(args.warmup, 3)):
-        _, _ = fa.decode_splitkv_gqa(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
-    torch.cuda.synchronize(dev)
-    steps = max(args.steps // 4, 5)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(world)
-    e0.record(stream)
-    for _ in range(steps):
-        fa.decode_splitkv_gqa(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+    st = time_stats(lambda: fa.decode_splitkv_gqa(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws),
+                    dev, stream, world, warmup=max(args.warmup, 3))
     barrier(world)
-    ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
+    ms = st["ms"]
     assert fa.get_device_error(dev) == fa.FA_OK
     kv_bytes = sum(2 * Hkv * int(n_b) * d * 2 for n_b in lens.tolist())
     other = B * Hq * (d * 2 + d * 2 + 4)
     pk, src = peaks()
     gbs = world * (kv_bytes + other) / (ms / 1e3) / 1e9
     return {"workload": f"GQA split-KV decode B={B} Hq={Hq} Hkv={Hkv} d={d}, lengths U[1024,32768] (seed 0), bf16 O",
-            "group": Hq // Hkv, "n_splits": n_auto, "unit": "tensor core" if Hq // Hkv not in (1, 2, 4) else "CUDA cores", "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
+            "group": Hq // Hkv, "n_splits": n_auto, "timing": st, "unit": "tensor core" if Hq // Hkv not in (1, 2, 4) else "CUDA cores", "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
             "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2}
 
 
@@ -621,18 +735,9 @@ def run_splitkv_prefill(fa, dev, stream, args, world):
     for name, call in (("fa_fwd", lambda: fa.fwd(q, k, v, causal=True, out=o, lse=lse)),
                        ("fa_fwd_splitkv", lambda: fa.fwd_splitkv(q, k, v, causal=True, n_splits=n, out=o, lse=lse,
                                                                  workspace=ws))):
-        for _ in range(max(args.warmup, 3)):
-            call()
-        steps = max(5, args.steps // 10)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(steps):
-            call()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms = max_over_ranks(e0.elapsed_time(e1), world) / steps
-        out[name] = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12}
+        st = time_stats(call, dev, stream, world, warmup=max(args.warmup, 3))
+        ms = st["ms"]
+        out[name] = {"ms": ms, "tflops": fl / (ms / 1e3) / 1e12, "timing": st}
     assert fa.get_device_error(dev) == fa.FA_OK
     return out
 

@@ -101,8 +101,35 @@ def _check(status, where):
         raise FaError(status, where)
 
 
+# The current stream's raw handle; torch's own lookup (a plain int) when it has one, which avoids
+# building a Stream object on every call.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(device):
-    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+    idx = device.index if isinstance(device, torch.device) else int(device)
+    if _raw_stream is not None:
+        return _raw_stream(idx)
+    return torch.cuda.current_stream(idx).cuda_stream
+
+
+class _on_device:
+    """Makes `index` the current CUDA device for the call (switching only when it is not)."""
+
+    __slots__ = ("index", "ctx")
+
+    def __init__(self, index):
+        self.index = index
+        self.ctx = None
+
+    def __enter__(self):
+        if torch.cuda.current_device() != self.index:
+            self.ctx = torch.cuda.device(self.index)
+            self.ctx.__enter__()
+
+    def __exit__(self, *exc):
+        if self.ctx is not None:
+            self.ctx.__exit__(*exc)
 
 
 def _odt(dtype):
@@ -114,20 +141,26 @@ def _odt(dtype):
 
 
 def _need(t, name, dtype, device=None):
+    """Checks a tensor argument; returns its CUDA device index.  `device` (a torch.device or an
+    index) is the device the other arguments are on."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
-    if not t.is_cuda:
+    di = t.get_device()
+    if di < 0:
         raise ValueError(f"{name} must be on a CUDA device")
-    if device is not None and t.device != device:
-        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if device is not None:
+        want = device.index if isinstance(device, torch.device) else device
+        if di != want:
+            raise ValueError(f"{name} is on cuda:{di}, expected cuda:{want}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    return di
 
 
 def _ptr(t):
-    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+    return t.data_ptr() if t is not None else None
 
 
 def fwd(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, out=None, lse=None, return_lse=True):
@@ -156,7 +189,7 @@ def fwd(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, out=None, l
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     if lse is not None:
         _need(lse, "lse", torch.float32, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev.index):
         st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, Nk, d, dv, int(bool(causal)),
                         scale, _odt(out.dtype), _stream(dev))
     _check(st, "fa_fwd")
@@ -201,7 +234,7 @@ def bwd(q, k, v, o, lse, do, causal=False, scale=None, out_dtype=torch.bfloat16,
     if workspace is None:
         workspace = torch.empty(bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", torch.uint8, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev.index):
         st = lib.fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv_),
                         _ptr(workspace), workspace.numel(), B, H, N, Nk, d, dv, int(bool(causal)), scale,
                         _odt(o.dtype), _odt(dq.dtype), _stream(dev))
@@ -242,7 +275,7 @@ def fwd_splitkv(q, k, v, causal=False, scale=None, n_splits=0, out_dtype=torch.b
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     if lse is not None:
         _need(lse, "lse", torch.float32, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev.index):
         st = lib.fa_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
                                 B, H, N, Nk, d, dv, int(bool(causal)), scale, n, _odt(out.dtype), _stream(dev))
     _check(st, "fa_fwd_splitkv")
@@ -297,7 +330,7 @@ def decode_splitkv(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out_dty
         lse = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
     if lse is not None:
         _need(lse, "lse", torch.float32, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev.index):
         st = lib.fa_decode_splitkv(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(out), _ptr(lse),
                                    _ptr(workspace), workspace.numel(), B, H, Nk_max, d, dv, scale, n,
                                    _odt(out.dtype), _stream(dev))
@@ -339,7 +372,7 @@ def decode_splitkv_gqa(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out
         lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
     if lse is not None:
         _need(lse, "lse", torch.float32, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev.index):
         st = lib.fa_decode_splitkv_gqa(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(out), _ptr(lse),
                                        _ptr(workspace), workspace.numel(), B, Hq, Hkv, Nk_max, d, dv, scale,
                                        int(n_splits), _odt(out.dtype), _stream(dev))
@@ -383,7 +416,7 @@ def decode_splitkv_fused(q, k_cache, v_cache, seqlens, workspace, scale=None, n_
         lse = torch.empty((B, H, 1), dtype=torch.float32, device=dev)
     if lse is not None:
         _need(lse, "lse", torch.float32, dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev.index):
         st = lib.fa_decode_splitkv_fused(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seqlens), _ptr(out), _ptr(lse),
                                          _ptr(workspace), workspace.numel(), B, H, Nk_max, d, dv, scale,
                                          int(n_splits), _odt(out.dtype), _stream(dev))
@@ -404,7 +437,7 @@ def merge_states(o_parts, lse_parts, out_dtype=torch.float32, out=None, lse=None
         out = torch.empty((rows, dv), dtype=out_dtype, device=dev)
     if lse is None:
         lse = torch.empty((rows,), dtype=torch.float32, device=dev)
-    with torch.cuda.device(dev):
+    with _on_device(dev.index):
         st = lib.fa_merge_states(_ptr(o_parts), _ptr(lse_parts), P, rows, dv, _ptr(out), _ptr(lse),
                                  _odt(out.dtype), _stream(dev))
     _check(st, "fa_merge_states")
@@ -414,7 +447,7 @@ def merge_states(o_parts, lse_parts, out_dtype=torch.float32, out=None, lse=None
 def get_device_error(device=None):
     """Synchronise the current stream and return (and clear) the device status word."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    with torch.cuda.device(dev):
+    with _on_device(dev.index):
         return int(_load().fa_get_device_error(_stream(dev)))
 
 

@@ -73,20 +73,28 @@ cudaError_t current_device(int* dev)
     return cudaSuccess;
 }
 
+// Per-device facts looked up once (under a lock) and then read from a per-thread copy, so that
+// a call takes no lock.
+thread_local int* t_status_ptr[kMaxDevices] = {};
+thread_local int t_num_sms[kMaxDevices] = {};
+
 // Device address of the status word on the current device (looked up once per device).
 cudaError_t status_word(int** out)
 {
     int dev;
     cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_status_ptr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_device_status);
-        if (e != cudaSuccess) return e;
-        g_status_ptr[dev] = static_cast<int*>(p);
+    if (t_status_ptr[dev] == nullptr) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_status_ptr[dev] == nullptr) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_device_status);
+            if (e != cudaSuccess) return e;
+            g_status_ptr[dev] = static_cast<int*>(p);
+        }
+        t_status_ptr[dev] = g_status_ptr[dev];
     }
-    *out = g_status_ptr[dev];
+    *out = t_status_ptr[dev];
     return cudaSuccess;
 }
 
@@ -95,12 +103,15 @@ cudaError_t sm_count(int* out)
     int dev;
     cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return e;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_num_sms[dev] == 0) {
-        e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
+    if (t_num_sms[dev] == 0) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_num_sms[dev] == 0) {
+            e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+            if (e != cudaSuccess) return e;
+        }
+        t_num_sms[dev] = g_num_sms[dev];
     }
-    *out = g_num_sms[dev];
+    *out = t_num_sms[dev];
     return cudaSuccess;
 }
 
@@ -119,9 +130,69 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
     return fn;
 }
 
+// A tensor map is a pure function of (address, sizes, element type, box): encoding one costs on
+// the order of a microsecond of host time, a visible share of a short call.  Each host thread
+// keeps the last kMapCache maps it encoded and reuses one whose key matches (device addresses are
+// unique across the process's devices, so the key needs no device).
+struct MapKey {
+    const void* ptr;
+    int BH, rows, d, kind, box_rows;  // kind: 0 bf16 input, 1 bf16 output, 2 fp32 output
+    bool operator==(const MapKey& o) const
+    {
+        return ptr == o.ptr && BH == o.BH && rows == o.rows && d == o.d && kind == o.kind && box_rows == o.box_rows;
+    }
+};
+constexpr int kMapCache = 16;
+struct MapCache {
+    MapKey key[kMapCache];
+    CUtensorMap map[kMapCache];
+    bool used[kMapCache] = {};
+    int next = 0;
+    bool find(const MapKey& k, CUtensorMap* m) const
+    {
+        for (int i = 0; i < kMapCache; ++i)
+            if (used[i] && key[i] == k) {
+                *m = map[i];
+                return true;
+            }
+        return false;
+    }
+    void put(const MapKey& k, const CUtensorMap& m)
+    {
+        key[next] = k;
+        map[next] = m;
+        used[next] = true;
+        next = (next + 1) % kMapCache;
+    }
+};
+thread_local MapCache t_maps;
+
+bool encode_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d);
+bool encode_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t, int box_rows);
+
+// bf16 input tensor [BH][rows][d] (see encode_map), from the thread's cache when possible.
+bool make_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d)
+{
+    const MapKey k{ptr, BH, rows, d, 0, fa::kBlockM};
+    if (t_maps.find(k, m)) return true;
+    if (!encode_map(m, ptr, BH, rows, d)) return false;
+    t_maps.put(k, *m);
+    return true;
+}
+
+// Output tensor map (see encode_out_map), from the thread's cache when possible.
+bool make_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t, int box_rows)
+{
+    const MapKey k{ptr, BH, rows, d, t == FA_F32 ? 2 : 1, box_rows};
+    if (t_maps.find(k, m)) return true;
+    if (!encode_out_map(m, ptr, BH, rows, d, t, box_rows)) return false;
+    t_maps.put(k, *m);
+    return true;
+}
+
 // bf16 tensor [BH][rows][d] as a 3-D tiled map with a {min(d,64), 128, 1} box,
 // swizzled so that each box row is one swizzle span (64 or 128 bytes).
-bool make_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d)
+bool encode_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d)
 {
     auto enc = encode_fn();
     if (enc == nullptr) return false;
@@ -141,7 +212,7 @@ bool make_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d)
 // box_rows rows of one column block (128 bytes of a row, or the whole 64-byte row of bf16 d = 32),
 // swizzled to match the staging tiles the kernels write (the forward stores 32-row quarters, one
 // per warp; the backward whole 128-row tiles).
-bool make_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t, int box_rows)
+bool encode_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t, int box_rows)
 {
     auto enc = encode_fn();
     if (enc == nullptr) return false;

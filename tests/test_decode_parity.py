@@ -86,11 +86,12 @@ def test_full_decode_config():
     B, H, Nk_max, d = 16, 32, 32768, 128
     q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=0, lo=1024, hi=32768, device=DEV)
     scale = 1.0 / math.sqrt(d)
-    o, lse = fa().decode_splitkv(q, k, v, lens.to(DEV), scale=scale, n_splits=0, out_dtype=torch.float32)
-    torch.cuda.synchronize()
-    assert fa().get_device_error() == 0
     o_ref, lse_ref = oracle_decode_compact(q, k, v, lens, scale)
-    assert_close(o, lse, o_ref, lse_ref, what="decode B16 H32 Nk<=32768")
+    for dt in (torch.float32, torch.bfloat16):  # fp32 O, and the benchmark's bf16 O
+        o, lse = fa().decode_splitkv(q, k, v, lens.to(DEV), scale=scale, n_splits=0, out_dtype=dt)
+        torch.cuda.synchronize()
+        assert fa().get_device_error() == 0
+        assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16), what=f"decode B16 H32 Nk<=32768 {dt}")
 
 
 @pytest.mark.parametrize("n_parts,rows,dv,empty", [(1, 5, 128, 0.0), (16, 333, 128, 0.3), (999, 7, 64, 0.5),
@@ -165,20 +166,27 @@ def test_gqa_decode(d, R, n_splits):
         assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16), what=f"gqa d={d} R={R} n={n_splits}")
 
 
-def test_gqa_full_size_sampled():
-    """The benchmark's GQA workload (B=16, Hq=32, Hkv=8, d=128, lengths U[1024, 32768]) in its
-    launch configuration; 24 seeded query heads against the oracle."""
-    B, Hq, Hkv, Nk_max, d = 16, 32, 8, 32768, 128
+@pytest.mark.parametrize("Hkv", [8, 4], ids=["R4_cuda_cores", "R8_tensor_core"])
+def test_gqa_full_size_sampled(Hkv):
+    """The benchmark's GQA workloads (B=16, Hq=32 over Hkv=8 or 4, d=128, lengths U[1024, 32768]) in
+    their launch configuration, with fp32 O and with the benchmark's bf16 O; 24 seeded query heads
+    against the oracle."""
+    B, Hq, Nk_max, d = 16, 32, 32768, 128
     q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=1024, hi=Nk_max, device=DEV)
-    o, lse = fa().decode_splitkv_gqa(q, k, v, lens.to(DEV), out_dtype=torch.float32)
-    torch.cuda.synchronize()
-    assert fa().get_device_error() == 0
     R = Hq // Hkv
+    refs = {}
     for idx in sample_slices_gqa(B * Hq, 24):
         b, h = divmod(idx, Hq)
         n = int(lens[b])
-        o_ref, l_ref = oracle.attention(q[b, h].cpu(), k[b, h // R, :n].cpu(), v[b, h // R, :n].cpu(), scale=1 / math.sqrt(d))
-        assert_close(o[b, h], lse[b, h], o_ref, l_ref, what=f"gqa full b={b} h={h}")
+        refs[(b, h)] = oracle.attention(q[b, h].cpu(), k[b, h // R, :n].cpu(), v[b, h // R, :n].cpu(),
+                                        scale=1 / math.sqrt(d))
+    for dt in (torch.float32, torch.bfloat16):
+        o, lse = fa().decode_splitkv_gqa(q, k, v, lens.to(DEV), out_dtype=dt)
+        torch.cuda.synchronize()
+        assert fa().get_device_error() == 0
+        for (b, h), (o_ref, l_ref) in refs.items():
+            assert_close(o[b, h], lse[b, h], o_ref, l_ref, bf16_out=(dt == torch.bfloat16),
+                         what=f"gqa full R={R} b={b} h={h} {dt}")
 
 
 def sample_slices_gqa(total, k):

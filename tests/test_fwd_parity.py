@@ -129,10 +129,12 @@ def test_gpt2_medium_shape_bf16_out_sampled(causal):
     _sampled_check(64, 16, 1024, 1024, 64, 1.0, causal, 4, out_dtype=torch.bfloat16)
 
 
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_ragged_4097_sampled(causal):
-    """B=4, H=16, N=Nk=4097, d=128, inputs x2: 3 heads, first and last 384 rows (the ragged tail tile)."""
-    _sampled_check(4, 16, 4097, 4097, 128, 2.0, causal, 3, rows=[(0, 384), (3713, 4097)])
+def test_ragged_4097_sampled(causal, out_dtype):
+    """B=4, H=16, N=Nk=4097, d=128, inputs x2: 3 heads, first and last 384 rows (the ragged tail tile),
+    with fp32 O and with the benchmark's bf16 O."""
+    _sampled_check(4, 16, 4097, 4097, 128, 2.0, causal, 3, rows=[(0, 384), (3713, 4097)], out_dtype=out_dtype)
 
 
 def test_ragged_77_513_full():
@@ -141,14 +143,17 @@ def test_ragged_77_513_full():
     scale = 1.0 / math.sqrt(32)
     for causal in (False, True):
         o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=causal, scale=scale)
-        o, lse = run(q, k, v, causal, scale)
-        assert_close(o, lse, o_ref, lse_ref, what=f"77x513 causal={causal}")
+        for dt in (torch.float32, torch.bfloat16):
+            o, lse = run(q, k, v, causal, scale, dt)
+            assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16), what=f"77x513 causal={causal} {dt}")
 
 
-def test_long_causal_sampled():
-    """B=2, H=32, N=Nk=16384, d=128, causal: 4 heads x first 2048 rows, and the last 128 rows of one head."""
-    _sampled_check(2, 32, 16384, 16384, 128, 1.0, True, 4, rows=[(0, 2048)])
-    _sampled_check(2, 32, 16384, 16384, 128, 1.0, True, 1, rows=[(16256, 16384)])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32", "bf16"])
+def test_long_causal_sampled(out_dtype):
+    """B=2, H=32, N=Nk=16384, d=128, causal: 4 heads x first 2048 rows, and the last 128 rows of one head,
+    with fp32 O and with the benchmark's bf16 O."""
+    _sampled_check(2, 32, 16384, 16384, 128, 1.0, True, 4, rows=[(0, 2048)], out_dtype=out_dtype)
+    _sampled_check(2, 32, 16384, 16384, 128, 1.0, True, 1, rows=[(16256, 16384)], out_dtype=out_dtype)
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
