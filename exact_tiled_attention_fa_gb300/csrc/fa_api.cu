@@ -27,6 +27,8 @@ cudaError_t launch_splitkv_32(const SplitParams& p, bool causal, bool varlen, cu
 cudaError_t launch_splitkv_64(const SplitParams& p, bool causal, bool varlen, cudaStream_t st);
 cudaError_t launch_splitkv_128(const SplitParams& p, bool causal, bool varlen, cudaStream_t st);
 
+cudaError_t launch_gqa_tc(const SplitParams& p, cudaStream_t st);
+
 cudaError_t launch_splitkv(const SplitParams& p, int d, bool causal, bool varlen, cudaStream_t st)
 {
     switch (d) {
@@ -167,15 +169,15 @@ struct MapCache {
 };
 thread_local MapCache t_maps;
 
-bool encode_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d);
+bool encode_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d, int box_rows);
 bool encode_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t, int box_rows);
 
 // bf16 input tensor [BH][rows][d] (see encode_map), from the thread's cache when possible.
-bool make_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d)
+bool make_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d, int box_rows = fa::kBlockM)
 {
-    const MapKey k{ptr, BH, rows, d, 0, fa::kBlockM};
+    const MapKey k{ptr, BH, rows, d, 0, box_rows};
     if (t_maps.find(k, m)) return true;
-    if (!encode_map(m, ptr, BH, rows, d)) return false;
+    if (!encode_map(m, ptr, BH, rows, d, box_rows)) return false;
     t_maps.put(k, *m);
     return true;
 }
@@ -190,16 +192,16 @@ bool make_out_map(CUtensorMap* m, void* ptr, int BH, int rows, int d, fa_dtype t
     return true;
 }
 
-// bf16 tensor [BH][rows][d] as a 3-D tiled map with a {min(d,64), 128, 1} box,
+// bf16 tensor [BH][rows][d] as a 3-D tiled map with a {min(d,64), box_rows, 1} box,
 // swizzled so that each box row is one swizzle span (64 or 128 bytes).
-bool encode_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d)
+bool encode_map(CUtensorMap* m, const void* ptr, int BH, int rows, int d, int box_rows)
 {
     auto enc = encode_fn();
     if (enc == nullptr) return false;
     const int cb = d < 64 ? d : 64;
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(BH)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
-    cuuint32_t box[3] = {static_cast<cuuint32_t>(cb), static_cast<cuuint32_t>(fa::kBlockM), 1};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(cb), static_cast<cuuint32_t>(box_rows), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -491,7 +493,12 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
         if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
         fa::SplitParams sp;
         const long long groups = static_cast<long long>(B) * Hkv;
-        if (!make_map(&sp.tm_q, q, static_cast<int>(groups), R, d) ||
+        // d = 128 with 5-32 query heads per group: the transposed kernel (keys on the TMEM lanes,
+        // the group's heads on 16 or 32 columns); otherwise the heads are rows of a 128-row tile
+        const bool transposed = d == 128 && R >= 5 && R <= 32;
+        const int q_box = transposed ? (R <= 16 ? 16 : 32) : fa::kBlockM;
+        if (!transposed && groups > 65535) return FA_ERR_UNSUPPORTED;  // grid z
+        if (!make_map(&sp.tm_q, q, static_cast<int>(groups), R, d, q_box) ||
             !make_map(&sp.tm_k, k_cache, static_cast<int>(groups), Nk_max, d) ||
             !make_map(&sp.tm_v, v_cache, static_cast<int>(groups), Nk_max, dv))
             return FA_ERR_CUDA;
@@ -511,7 +518,8 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
         sp.scale_log2 = scale * 1.4426950408889634f;
         sp.wait_limit_ns = g_wait_ns.load();
         cudaStream_t st = static_cast<cudaStream_t>(stream);
-        if (fa::launch_splitkv(sp, d, false, true, st) != cudaSuccess) return FA_ERR_CUDA;
+        if ((transposed ? fa::launch_gqa_tc(sp, st) : fa::launch_splitkv(sp, d, false, true, st)) != cudaSuccess)
+            return FA_ERR_CUDA;
         return merge_rows(sp.o_part, sp.lse_part, B * Hq, n_eff, dv, o, lse, status, o_dtype, st) == cudaSuccess
                    ? FA_OK
                    : FA_ERR_CUDA;

@@ -1,0 +1,444 @@
+// fa_gqa_kernel.cuh -- grouped-query split-KV decode on the tensor core with the product
+// transposed, for sm_103a (head size 128, 5 to 32 query heads per key/value head).
+//
+// Algorithm: "flash_lab.py -- FlashAttention, flash-decoding and megakernel in numpy",
+// section 4 `split_kv_decode` with the R query heads of a key/value head packed together (q of
+// shape [R, d]; `decode_attention_time` method "fd"): each split of a sequence's cached keys
+// gives, for every query head h of the group, the split's normalised output o_s[h] and
+// log-sum-exp lse_s[h]; the merge kernel combines the splits.  Within a split the key tiles are
+// walked with the online softmax of section 1 (running max m and sum l per query head, the
+// accumulator rescaled by exp(m_old - m_new)).
+//
+// Why transposed.  With R query heads as the rows of a 128-row tile, R of 128 rows are live, and
+// the per-tile cost of a row-per-thread softmax (128 exponentials per thread) is paid for R rows
+// of work.  Here the tile is turned around: S^T = K_j Q^T puts the 128 keys of the tile on the
+// TMEM lanes and the query heads on NQ columns (R padded to a multiple of 16), so thread t (the
+// key of lane t) handles R scores per tile; the per-head maximum over the tile's keys is a
+// reduction across threads (warp shuffles, then the four warps through shared memory).  The
+// thread writes its key's weights P^T into shared memory as the rows of a K-major B operand,
+// and the output accumulates transposed, O^T += V_j^T P^T (A = the V tile read MN-major, M = the
+// 128 value columns), so TMEM lane t of O^T is value column t and the rescale by exp(m_old -
+// m_new) multiplies column h by that head's factor.
+//
+// One CTA per (split, group = (sequence, key/value head)); six warps:
+//   warps 0-3  compute: thread t owns key t of S^T and value column t of O^T.
+//   warp 4     TMA producer: the group's NQ query rows once, K_j and V_j into a ring.
+//   warp 5     tcgen05 issuer: S^T(j+1) as soon as S^T(j) has been read, O^T += V_j^T P^T(j).
+// Tensor memory: S^T in columns [0, NQ), O^T in [NQ, 2 NQ).
+// Cache rows past a sequence's length may hold anything (the tests fill them with NaN): their
+// scores are masked, and before the last tile's product the compute threads zero those V rows
+// in shared memory (a weight of 0 times NaN would still be NaN).
+// Every barrier wait is bounded; a wait that runs out records FA_ERR_TIMEOUT, the roles drain
+// what they have in flight and the CTA returns.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "fa_internal.h"
+#include "fa_kernel_common.cuh"
+#include "ptx.cuh"
+
+namespace fa {
+
+constexpr int kGqThreads = 192;
+constexpr int kGqWarpProducer = 4;
+constexpr int kGqWarpMma = 5;
+constexpr int kGqD = 128;  // head size of this kernel
+
+enum : int {
+    kGbQFull = 0,
+    kGbSFull = 1,
+    kGbSFree = 2,   // the compute threads have read S^T (count 128)
+    kGbPFull = 3,   // P^T written and O^T rescaled (count 128)
+    kGbPVDone = 4,
+    kGbOReady = 5,
+    kGbDrain = 6,
+    kGbKVFull = 8,   // + stage
+    kGbKVEmpty = 12, // + stage
+    kGbRed = 16,     // + tile parity: the four compute warps' partial maxima (or sums) are in (count 4)
+    kGbCount = 18
+};
+
+template <int NQ>
+struct GqCfg {
+    static_assert(NQ == 16 || NQ == 32, "padded query heads per group");
+    static constexpr int kNQ = NQ;
+    static constexpr int kStages = 3;
+    static constexpr int kRowBytes = 128;                       // one 64-element column block row
+    static constexpr int kBlkBytes = kBlockN * kRowBytes;       // 128 rows of one column block
+    static constexpr int kTileBytes = 2 * kBlkBytes;            // 128 x 128 bf16 (K or V tile)
+    static constexpr int kQBlkBytes = NQ * kRowBytes;           // NQ query rows of one column block
+    static constexpr int kQBytes = 2 * kQBlkBytes;
+    static constexpr int kPBlkBytes = NQ * kRowBytes;           // P^T: NQ rows x 64 keys
+    static constexpr int kPBytes = 2 * kPBlkBytes;              // NQ rows x 128 keys
+    static constexpr int kOffK = 0;                             // + stage * kTileBytes
+    static constexpr int kOffV = kOffK + kStages * kTileBytes;  // + stage * kTileBytes
+    static constexpr int kOffQ = kOffV + kStages * kTileBytes;
+    static constexpr int kOffP = kOffQ + kQBytes;               // two P^T buffers
+    static constexpr int kOffRed = kOffP + 2 * kPBytes;         // [2][4 warps][NQ] floats for reductions
+    static constexpr int kOffBar = kOffRed + 2 * 4 * NQ * 4;
+    static constexpr int kUsedBytes = kOffBar + kGbCount * 8 + 16;
+    static constexpr int kSmemBytes = kUsedBytes + 1024;        // + alignment slack
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+    static constexpr int kTmemCols = 2 * NQ < 32 ? 32 : 2 * NQ;
+    static constexpr uint32_t kColS = 0, kColO = NQ;
+    // S^T = K Q^T: M = 128 keys, N = NQ heads, both operands K-major
+    static constexpr uint32_t kIdescS = idesc_bf16(kBlockN, NQ, false);
+    // O^T += V^T P^T: M = 128 value columns (A = V read MN-major), N = NQ heads (B = P^T, K-major)
+    static constexpr uint32_t kIdescO = idesc_bf16_a_mn(kGqD, NQ);
+};
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, unsigned short v)
+{
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// Grid: (n_splits, key/value heads, sequences).  RH: query heads per group rounded up to a
+// multiple of 8 (the heads the compute threads handle); the MMAs use NQ = max(RH, 16) columns.
+// The query map is [groups][R][128] with a box of NQ rows (rows past R are zero-filled), the K/V
+// maps [groups][Nk][128] with 128-row boxes.
+template <int RH>
+__global__ void __launch_bounds__(kGqThreads, 1) fa_gqa_kernel(const __grid_constant__ SplitParams p)
+{
+    using C = GqCfg<(RH < 16 ? 16 : RH)>;
+    constexpr int S = C::kStages;
+    extern __shared__ uint8_t gq_smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gq_smem_raw) + 1023) &
+                                               ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = smem_u32(smem);
+    auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * static_cast<uint32_t>(i); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + kGbCount * 8);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const unsigned long long limit = p.wait_limit_ns;
+
+    // ---- work item: split s of group g = (sequence b, key/value head)
+    const int s = blockIdx.x;
+    const int b = blockIdx.z;
+    const int g = b * p.groups_per_batch + blockIdx.y;
+    const int R = p.rows_per_group;
+    int len = p.seqlens[b];
+    if (len < 0 || len > p.Nk) {
+        if (threadIdx.x == 0) atomicCAS(p.status, 0, FA_ERR_INVALID_ARG);
+        len = len < 0 ? 0 : p.Nk;
+    }
+    const int kl = s * p.chunk;  // the split's keys: [kl, kh)
+    const int kh = min(len, kl + p.chunk);
+    const int j_begin = kl / kBlockN;
+    const int nt = kh > kl ? (kh - kl + kBlockN - 1) / kBlockN : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(kGbQFull), 1);
+        mbar_init(bar(kGbSFull), 1);
+        mbar_init(bar(kGbSFree), kBlockN);
+        mbar_init(bar(kGbPFull), kBlockN);
+        mbar_init(bar(kGbPVDone), 1);
+        mbar_init(bar(kGbOReady), 1);
+        mbar_init(bar(kGbDrain), 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(bar(kGbKVFull + i), 1);
+            mbar_init(bar(kGbKVEmpty + i), 1);
+        }
+        mbar_init(bar(kGbRed + 0), 4);
+        mbar_init(bar(kGbRed + 1), 4);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == kGqWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == kGqWarpProducer) {
+        // ============================================================ producer
+        if (lane == 0 && nt > 0) {
+            prefetch_tensormap(&p.tm_q);
+            prefetch_tensormap(&p.tm_k);
+            prefetch_tensormap(&p.tm_v);
+            const uint64_t pol = policy_evict_first();  // each K/V tile is read by one CTA only
+            mbar_arrive_expect_tx(bar(kGbQFull), C::kQBytes);
+            for (int cb = 0; cb < 2; ++cb)
+                tma_load_3d(sbase + C::kOffQ + cb * C::kQBlkBytes, &p.tm_q, bar(kGbQFull), cb * 64, 0, g, pol);
+            int issued = 0;
+            bool ok = true;
+            for (int t = 0; t < nt; ++t) {
+                const int st = t % S;
+                if (t >= S && !mbar_wait(bar(kGbKVEmpty + st), static_cast<uint32_t>(t / S - 1) & 1, limit, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int k0 = (j_begin + t) * kBlockN;
+                mbar_arrive_expect_tx(bar(kGbKVFull + st), 2 * C::kTileBytes);
+                for (int cb = 0; cb < 2; ++cb) {
+                    tma_load_3d(sbase + C::kOffK + st * C::kTileBytes + cb * C::kBlkBytes, &p.tm_k, bar(kGbKVFull + st),
+                                cb * 64, k0, g, pol);
+                    tma_load_3d(sbase + C::kOffV + st * C::kTileBytes + cb * C::kBlkBytes, &p.tm_v, bar(kGbKVFull + st),
+                                cb * 64, k0, g, pol);
+                }
+                ++issued;
+            }
+            if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+            mbar_wait(bar(kGbQFull), 0, kDrainLimitNs, nullptr);
+            for (int t = issued - S < 0 ? 0 : issued - S; t < issued; ++t)
+                mbar_wait(bar(kGbKVFull + t % S), static_cast<uint32_t>(t / S) & 1, kDrainLimitNs, nullptr);
+        }
+    } else if (warp == kGqWarpMma) {
+        // ============================================================ MMA issuer
+        if (lane == 0 && nt > 0) {
+            bool ok = true;
+            auto wait = [&](int bb, int parity) -> bool {
+                ok = ok && mbar_wait(bar(bb), static_cast<uint32_t>(parity) & 1, limit, abort_flag);
+                return ok;
+            };
+            // S^T = K_j Q^T: A = the K tile (128 keys, K-major), B = the NQ query rows (K-major).
+            auto issue_s = [&](int st) {
+                const uint64_t a0 = smem_desc(sbase + C::kOffK + st * C::kTileBytes, 16, 1024, kSwizzle128B);
+                const uint64_t b0 = smem_desc(sbase + C::kOffQ, 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int kk = 0; kk < kGqD / 16; ++kk) {
+                    const uint32_t oa = ((kk / 4) * C::kBlkBytes + (kk % 4) * 32) >> 4;
+                    const uint32_t ob = ((kk / 4) * C::kQBlkBytes + (kk % 4) * 32) >> 4;
+                    umma_ss(tmem + C::kColS, a0 + oa, b0 + ob, C::kIdescS, kk > 0 ? 1u : 0u);
+                }
+            };
+            // O^T += V_j^T P^T: A = the V tile read MN-major (its 128 value columns contiguous per
+            // key row; the two 64-column blocks kBlkBytes apart), B = P^T (NQ rows of keys, K-major).
+            auto issue_pv = [&](int st, int pbuf, bool accumulate) {
+                const uint64_t a0 = smem_desc(sbase + C::kOffV + st * C::kTileBytes, C::kBlkBytes, 1024, kSwizzle128B);
+                const uint64_t b0 = smem_desc(sbase + C::kOffP + pbuf * C::kPBytes, 16, 1024, kSwizzle128B);
+#pragma unroll
+                for (int kk = 0; kk < kBlockN / 16; ++kk) {
+                    const uint32_t oa = (kk * 16 * C::kRowBytes) >> 4;
+                    const uint32_t ob = ((kk / 4) * C::kPBlkBytes + (kk % 4) * 32) >> 4;
+                    umma_ss(tmem + C::kColO, a0 + oa, b0 + ob, C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
+                }
+            };
+            if (wait(kGbQFull, 0) && wait(kGbKVFull, 0)) {
+                tc_fence_after_sync();
+                issue_s(0);
+                umma_commit(bar(kGbSFull));
+            }
+            for (int t = 0; ok && t < nt; ++t) {
+                const int st = t % S;
+                if (t + 1 < nt) {  // S^T(t+1) as soon as the compute threads have read S^T(t)
+                    const int sn = (t + 1) % S;
+                    if (!wait(kGbKVFull + sn, (t + 1) / S) || !wait(kGbSFree, t)) break;
+                    tc_fence_after_sync();
+                    issue_s(sn);
+                    umma_commit(bar(kGbSFull));
+                }
+                if (!wait(kGbPFull, t)) break;
+                tc_fence_after_sync();
+                issue_pv(st, t & 1, t > 0);
+                umma_commit(bar(kGbPVDone));
+                umma_commit(bar(kGbKVEmpty + st));
+            }
+            umma_commit(bar(kGbOReady));
+            if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+            umma_commit(bar(kGbDrain));
+            mbar_wait(bar(kGbDrain), 0, kDrainLimitNs, nullptr);
+        }
+    } else {
+        // ============================================================ compute
+        constexpr int NQ = C::kNQ;
+        const int k = threadIdx.x;  // key k of S^T and value column k of O^T (TMEM lane k)
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t t_s = tmem + lane_base + C::kColS;
+        const uint32_t t_o = tmem + lane_base + C::kColO;
+        float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+        const float sl2 = p.scale_log2;
+        float m_run[RH], l[RH];  // per head: running max (base 2, scale folded in), this key's share of l
+#pragma unroll
+        for (int h = 0; h < RH; ++h) {
+            m_run[h] = -INFINITY;
+            l[h] = 0.f;
+        }
+        // The four warps' values of each head combined through shared memory (use: exchange number,
+        // alternating between two buffers and barriers).  False if the wait ran out.
+        auto exchange = [&](float (&v)[RH], int use, bool is_max) -> bool {
+            float* rb = red + (use & 1) * 4 * RH;
+            if (lane == 0) {
+#pragma unroll
+                for (int h = 0; h < RH; ++h) rb[warp * RH + h] = v[h];
+                mbar_arrive(bar(kGbRed + (use & 1)));
+            }
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(kGbRed + (use & 1)), static_cast<uint32_t>(use >> 1) & 1, limit,
+                                                   abort_flag)))
+                return false;
+#pragma unroll
+            for (int h = 0; h < RH; ++h)
+                v[h] = is_max ? fmaxf(fmaxf(rb[h], rb[RH + h]), fmaxf(rb[2 * RH + h], rb[3 * RH + h]))
+                              : (rb[h] + rb[RH + h]) + (rb[2 * RH + h] + rb[3 * RH + h]);
+            return true;
+        };
+        bool ok = true;
+        for (int t = 0; t < nt; ++t) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kGbSFull), t & 1, limit, abort_flag));
+            if (!ok) break;
+            tc_fence_after_sync();
+            uint32_t u[NQ];
+            if constexpr (NQ == 16) tmem_ld16(t_s, u);
+            else tmem_ld32(t_s, u);
+            tmem_ld_wait();
+            tc_fence_before_sync();
+            mbar_arrive(bar(kGbSFree));
+            const int k0 = (j_begin + t) * kBlockN;
+            const bool live = k0 + k < kh;  // keys past the split or the sequence weigh 0
+            float sv[RH], mx[RH];
+#pragma unroll
+            for (int h = 0; h < RH; ++h) {
+                sv[h] = live ? __uint_as_float(u[h]) : -INFINITY;
+                mx[h] = sv[h];
+            }
+            // each head's maximum over the tile's 128 keys
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int h = 0; h < RH; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+            ok = exchange(mx, t, true);
+            if (!ok) break;
+            // new running maxima and rescale factors: the same in every thread
+            float alpha[RH];
+            bool grew = false;
+#pragma unroll
+            for (int h = 0; h < RH; ++h) {
+                const float mt = mx[h] * sl2;
+                alpha[h] = 1.f;
+                if (mt > m_run[h]) {
+                    alpha[h] = ex2(m_run[h] - mt);  // 0 when m_run = -inf
+                    m_run[h] = mt;
+                    grew = true;
+                }
+            }
+            // this key's weights: P^T row h, column k of the K-major 128-byte-swizzled B operand
+            const uint32_t pb = sbase + C::kOffP + (t & 1) * C::kPBytes + (k >> 6) * C::kPBlkBytes;
+            const int e = k & 63;
+#pragma unroll
+            for (int h = 0; h < RH; ++h) {
+                const float mu = m_run[h] == -INFINITY ? 0.f : m_run[h];
+                const float pv = ex2(fmaf(sv[h], sl2, -mu));
+                l[h] = fmaf(l[h], alpha[h], pv);
+                st_shared_u16(pb + h * C::kRowBytes + ((static_cast<uint32_t>((e >> 3) ^ (h & 7))) << 4) + (e & 7) * 2,
+                              __bfloat16_as_ushort(__float2bfloat16_rn(pv)));
+            }
+            if (k0 + kBlockN > len) {
+                // V rows past the sequence may hold anything: zero them before the product reads
+                // them (their weight is 0, but 0 * NaN would poison O).  Row k of each 128-row column
+                // block is one 128-byte line whatever the swizzle.
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kGbKVFull + t % S), static_cast<uint32_t>(t / S) & 1, limit,
+                                                       abort_flag));
+                if (!ok) break;
+                if (k0 + k >= len) {
+                    const uint32_t vrow = sbase + C::kOffV + (t % S) * C::kTileBytes + k * C::kRowBytes;
+#pragma unroll
+                    for (int cb = 0; cb < 2; ++cb)
+#pragma unroll
+                        for (int c16 = 0; c16 < C::kRowBytes; c16 += 16)
+                            st_shared_v4(vrow + cb * C::kBlkBytes + c16, 0u, 0u, 0u, 0u);
+                }
+            }
+            fence_proxy_async_shared();
+            // O^T columns of heads whose maximum grew, once the previous product has completed
+            if (t > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(kGbPVDone), (t - 1) & 1, limit, abort_flag));
+                if (!ok) break;
+                tc_fence_after_sync();
+                if (grew) {  // the same in every thread
+                    uint32_t o[NQ];
+                    if constexpr (NQ == 16) tmem_ld16(t_o, o);
+                    else tmem_ld32(t_o, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < RH; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
+                    if constexpr (NQ == 16) tmem_st16(t_o, o);
+                    else tmem_st32(t_o, o);
+                    tmem_st_wait();
+                }
+            }
+            tc_fence_before_sync();
+            mbar_arrive(bar(kGbPFull));
+        }
+        if (ok && nt > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(kGbOReady), 0, limit, abort_flag));
+            if (ok) tc_fence_after_sync();
+        }
+        // epilogue: each head's sum over all keys of the split, then the split's normalised
+        // output (thread k writes value column k of every head: coalesced rows) and log-sum-exp
+        // (o = 0, lse = -inf for a split with no key).
+        if (ok && nt > 0) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+                for (int h = 0; h < RH; ++h) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+            ok = exchange(l, nt, false);
+        }
+        if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
+        if (ok) {  // uniform across the warp (from __all_sync)
+            uint32_t o[NQ];
+            if (nt > 0) {
+                if constexpr (NQ == 16) tmem_ld16(t_o, o);
+                else tmem_ld32(t_o, o);
+                tmem_ld_wait();
+            }
+            const size_t row0 = static_cast<size_t>(g) * R;
+#pragma unroll
+            for (int h = 0; h < RH; ++h) {
+                if (h < R) {
+                    const size_t slot = (row0 + h) * p.n_splits + s;
+                    const float val = (nt > 0 && l[h] > 0.f) ? __uint_as_float(o[h]) / l[h] : 0.f;
+                    p.o_part[slot * kGqD + k] = val;
+                    if (k == h)
+                        p.lse_part[slot] = (nt > 0 && l[h] > 0.f) ? (m_run[h] + lg2_approx(l[h])) * 0.69314718055994531f
+                                                                  : -INFINITY;
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == kGqWarpMma) {
+        __syncwarp();
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+}
+
+template <int RH>
+cudaError_t launch_gqa_t(const SplitParams& p, cudaStream_t st)
+{
+    using C = GqCfg<(RH < 16 ? 16 : RH)>;
+    auto kern = fa_gqa_kernel<RH>;
+    static bool configured[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    dim3 grid(p.n_splits, p.groups_per_batch, p.n_groups / p.groups_per_batch);
+    kern<<<grid, kGqThreads, C::kSmemBytes, st>>>(p);
+    return cudaGetLastError();
+}
+
+// Query heads per group R in [5, 32], head size 128.
+inline cudaError_t launch_gqa(const SplitParams& p, cudaStream_t st)
+{
+    const int R = p.rows_per_group;
+    if (R <= 8) return launch_gqa_t<8>(p, st);
+    if (R <= 16) return launch_gqa_t<16>(p, st);
+    if (R <= 32) return launch_gqa_t<32>(p, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace fa

@@ -230,6 +230,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            | (static_cast<uint32_t>(M >> 4) << 24);      // M / 16
 }
 
+// The same with the A operand read MN-major (M contiguous: "transpose A", bit 15) and B K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_a_mn(int M, int N)
+{
+    return idesc_bf16(M, N, false) | (1u << 15);
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05: MMA and commit (issued by one thread)
 // ---------------------------------------------------------------------------

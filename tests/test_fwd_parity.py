@@ -217,16 +217,29 @@ def test_splitkv_bounded_wait_reports_timeout_and_context_survives():
     FA_ERR_TIMEOUT and returns; the next calls are correct."""
     from fa_inputs import gqa_decode_inputs
     q, k, v = attention_inputs(1, 4, 256, 4096, 128, 128, seed=10, device=DEV)
+    # 8 query heads per key/value head: d = 128 runs the transposed kernel, d = 64 the row kernel
     qd, kc, vc, lens = gqa_decode_inputs(2, 16, 2, 2048, 128, 128, seed=10, lo=100, hi=2048, device=DEV)
+    q6, k6, v6, l6 = gqa_decode_inputs(2, 16, 2, 2048, 64, 64, seed=10, lo=100, hi=2048, device=DEV)
     fa().set_wait_timeout_ns(1)
     try:
         fa().fwd_splitkv(q, k, v, causal=True, n_splits=4, out_dtype=torch.float32)
         s1 = fa().get_device_error()
         fa().decode_splitkv_gqa(qd, kc, vc, lens.to(DEV), n_splits=4, out_dtype=torch.float32)
         s2 = fa().get_device_error()
+        fa().decode_splitkv_gqa(q6, k6, v6, l6.to(DEV), n_splits=4, out_dtype=torch.float32)
+        s3 = fa().get_device_error()
     finally:
         fa().set_wait_timeout_ns(0)
-    assert s1 == fa().FA_ERR_TIMEOUT and s2 == fa().FA_ERR_TIMEOUT
+    assert s1 == fa().FA_ERR_TIMEOUT and s2 == fa().FA_ERR_TIMEOUT and s3 == fa().FA_ERR_TIMEOUT
+    o, lse = fa().decode_splitkv_gqa(qd, kc, vc, lens.to(DEV), n_splits=4, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == 0
+    for b in range(2):
+        n = int(lens[b])
+        for h in range(16):
+            o_ref, l_ref = oracle.attention(qd[b, h].cpu(), kc[b, h // 8, :n].cpu(), vc[b, h // 8, :n].cpu(),
+                                            scale=1 / math.sqrt(128))
+            assert_close(o[b, h], lse[b, h], o_ref, l_ref, what=f"gqa after a timed-out launch b={b} h={h}")
     o, lse = fa().fwd_splitkv(q, k, v, causal=True, n_splits=4, out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert fa().get_device_error() == 0
