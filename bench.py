@@ -48,8 +48,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the SHA-256 of the kernel code it was taken on (comments excluded); reported only while the
 # code is unchanged.
 KERNEL_TRAFFIC = {
-    # profiles/fa_fwd_kernel_d64_gpt2medium_prefill.md: non-causal launch, 402.88 MB read + 106.93 MB written
-    "9672e56ce5725a8fb54519150001d94b4501b8064c6cf3effcd3cf2425c97a3f": 509.81e6,
+    # profiles/fa_fwd_kernel_d64_gpt2medium_prefill.md: non-causal launch, 402.75 MB read + 109.46 MB written
+    "738e7799e9bcfc58030b6e9a04f9faa5a953259683a2154e43e628ba81fa6354": 512.21e6,
 }
 
 
@@ -429,11 +429,17 @@ def visible_pairs(N, Nk, causal, r0=0, r1=None):
     return sum(min(Nk, max(0, off + i + 1)) for i in range(r0, r1))
 
 
+# --quick (for profiler launch lists): short timing blocks.  Set by main().
+QUICK = {"on": False}
+
+
 def time_stats(call, dev, stream, world, warmup=3, min_calls=100, min_s=0.5, blocks=5, max_block=10000):
     """Milliseconds per call from `blocks` blocks of back-to-back calls, each block timed with
     CUDA events on `stream`; blocks are sized so that together they make at least `min_calls`
     calls and last at least `min_s` seconds.  Returns the median, min and max block (max over
     ranks) and the number of timed calls."""
+    if QUICK["on"]:
+        warmup, min_calls, min_s, blocks = 1, 2, 0.0, 2
     for _ in range(warmup):
         call()
     torch.cuda.synchronize(dev)
@@ -661,6 +667,8 @@ def run_decode(fa, dev, stream, args, world, rank=0, hbm=None):
 def graph_us(call, dev, stream, world, reps=20):
     """Microseconds per call with `reps` calls captured into one CUDA graph and the graph replayed
     (after one eager call on a side stream for the first-use set-up)."""
+    if QUICK["on"]:
+        return None
     side = torch.cuda.Stream(dev)
     side.wait_stream(torch.cuda.current_stream(dev))
     with torch.cuda.stream(side):
@@ -744,11 +752,11 @@ def run_splitkv_prefill(fa, dev, stream, args, world):
 
 def _case_call(fa, dev, name):
     """(callable, description) for one named workload of the suite, inputs built on `dev`."""
-    fwd_cases = {"fwd-c1": 0, "fwd-c1-causal": 1, "fwd-c3a": 2, "fwd-c3a-causal": 3, "fwd-c3b-causal": 4,
-                 "fwd-c4": 5}
+    fwd_cases = {name: i for i, name in enumerate(("fwd-c1", "fwd-c1-causal", "fwd-c3a", "fwd-c3a-causal", "fwd-c3b",
+                                                   "fwd-c3b-causal", "fwd-c4"))}
     if name in fwd_cases or name in ("fwd-c2", "fwd-c2-causal"):
         if name in fwd_cases:
-            desc, B, H, N, Nk, d, mult, causal = OTHER_FWD[fwd_cases[name]]
+            desc, B, H, N, Nk, d, mult, causal = OTHER_FWD[fwd_cases[name]][:8]
         else:
             B, H, N, Nk, d, mult, causal = FWD["B"], FWD["H"], FWD["N"], FWD["Nk"], FWD["d"], 1.0, name.endswith("causal")
             desc = WORKLOAD + (" causal" if causal else " non-causal")
@@ -797,7 +805,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="run one workload alone (fwd-c1, fwd-c1-causal, fwd-c2, fwd-c2-causal, fwd-c3a, "
-                         "fwd-c3a-causal, fwd-c3b-causal, fwd-c4, decode, gqa4, gqa8) for profiling")
+                         "fwd-c3a-causal, fwd-c3b, fwd-c3b-causal, fwd-c4, decode, gqa4, gqa8) for profiling")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
@@ -812,11 +820,16 @@ def main():
     ap.add_argument("--no-bwd", action="store_true", help="skip the backward measurement")
     ap.add_argument("--bwd-only", action="store_true", help="only the backward (profiling)")
     ap.add_argument("--splitkv-only", action="store_true", help="only the split-KV prefill workload (profiling)")
+    ap.add_argument("--quick", action="store_true",
+                    help="short timing blocks and no CPU baselines (for profiler launch lists; not a measurement)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     world, rank, local = dist_setup()
     DEC["B"] = args.decode_batch
+    if args.quick:
+        QUICK["on"] = True
+        args.no_cpu_baseline = True
     if args.impl == "reference":
         return run_reference(args, world, rank)
     if args.case:
