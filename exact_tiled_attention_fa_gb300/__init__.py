@@ -169,30 +169,34 @@ def fwd(q, k, v, causal=False, scale=None, out_dtype=torch.bfloat16, out=None, l
     Returns (O [B,H,N,dv] of ``out_dtype``, LSE fp32 [B,H,N] or None).
     """
     lib = _load()
-    _need(q, "q", torch.bfloat16)
-    dev = q.device
-    _need(k, "k", torch.bfloat16, dev)
-    _need(v, "v", torch.bfloat16, dev)
-    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+    di = _need(q, "q", torch.bfloat16)  # device index; the other tensors must be on it
+    _need(k, "k", torch.bfloat16, di)
+    _need(v, "v", torch.bfloat16, di)
+    if len(q.shape) != 4 or len(k.shape) != 4 or len(v.shape) != 4:
         raise ValueError("q, k, v must be [B, H, rows, head_dim]")
     B, H, N, d = q.shape
     Nk, dv = v.shape[2], v.shape[3]
-    if tuple(k.shape) != (B, H, Nk, d) or tuple(v.shape[:2]) != (B, H):
+    if k.shape != (B, H, Nk, d) or v.shape[:2] != (B, H):
         raise ValueError("shape mismatch between q, k, v")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if out is None:
-        out = torch.empty((B, H, N, dv), dtype=out_dtype, device=dev)
-    _need(out, "out", out.dtype, dev)
-    if tuple(out.shape) != (B, H, N, dv):
+        out = torch.empty((B, H, N, dv), dtype=out_dtype, device=q.device)
+    _need(out, "out", out.dtype, di)
+    if out.shape != (B, H, N, dv):
         raise ValueError("out has the wrong shape")
     if lse is None and return_lse:
-        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if lse is not None:
-        _need(lse, "lse", torch.float32, dev)
-    with _on_device(dev.index):
-        st = lib.fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, Nk, d, dv, int(bool(causal)),
-                        scale, _odt(out.dtype), _stream(dev))
-    _check(st, "fa_fwd")
+        _need(lse, "lse", torch.float32, di)
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr() if lse is not None else None,
+            B, H, N, Nk, d, dv, 1 if causal else 0, scale, _odt(out.dtype))
+    if torch.cuda.current_device() == di:
+        st = lib.fa_fwd(*args, _stream(di))
+    else:
+        with torch.cuda.device(di):
+            st = lib.fa_fwd(*args, _stream(di))
+    if st != FA_OK:
+        raise FaError(st, "fa_fwd")
     return out, lse
 
 
