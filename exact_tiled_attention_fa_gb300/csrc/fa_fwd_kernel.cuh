@@ -79,6 +79,12 @@ template <int D, bool CAUSAL>
 constexpr bool kCorr = D == 128 && !CAUSAL;
 template <int D, bool CAUSAL>
 constexpr int kThreads = kCorr<D, CAUSAL> ? 512 : kFwdThreads;
+// Whether the kernel walks its items in the ordered form (full query pairs first, then the heads'
+// one-tile last pairs; see FwdParams::n_full).  Only the d = 128 kernels without a mask, whose
+// uniform items make the last round's length matter: the extra cursor code costs the d = 64
+// kernels ~0.8 %.
+template <int D, bool CAUSAL>
+constexpr bool kOrderedWalk = kCorr<D, CAUSAL>;
 // Registers per thread after the split: the producer / MMA warpgroup gives registers to the
 // two softmax warpgroups.  The split needs kFwdThreads * (registers at launch) >=
 // 256 * kSoftmaxRegs + 128 * kControlRegs; the launcher checks this before every launch,
@@ -233,18 +239,48 @@ struct ItemCursor {
 };
 
 // `pairs` is the launch's FwdParams::pairs, passed as false by non-causal kernels (never paired).
-__device__ __forceinline__ ItemCursor first_item(const FwdParams& p, bool pairs)
+// Without a mask (`ordered`) t is the query pair itself, and items past BH * n_full are the heads'
+// one-tile last pairs (bh = item - BH * n_full, t = n_qp - 1).
+__device__ __forceinline__ ItemCursor first_item(const FwdParams& p, bool pairs, bool ordered = false)
 {
     ItemCursor c;
     c.item = pairs ? 2 * static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x);
+    c.k = 0;
+    if (ordered) {
+        const int full = p.BH * p.n_full;
+        if (c.item < full) {
+            c.bh = c.item / p.n_full;
+            c.t = c.item - c.bh * p.n_full;
+        } else {
+            c.bh = c.item - full;
+            c.t = p.n_qp - 1;
+        }
+        return c;
+    }
     c.bh = c.item / p.n_qp;
     c.t = c.item - c.bh * p.n_qp;
-    c.k = 0;
     return c;
 }
 
-__device__ __forceinline__ void next_item(const FwdParams& p, ItemCursor& c, bool pairs)
+__device__ __forceinline__ void next_item(const FwdParams& p, ItemCursor& c, bool pairs, bool ordered = false)
 {
+    if (ordered) {  // singly, step G: (head, pair) advanced by additions while in the full pairs
+        c.item += static_cast<int>(gridDim.x);
+        const int full = p.BH * p.n_full;
+        if (c.item < full) {
+            c.bh += p.step_heads;
+            c.t += p.step_rem;
+            if (c.t >= p.n_full) {
+                c.t -= p.n_full;
+                c.bh += 1;
+            }
+        } else {
+            c.bh = c.item - full;
+            c.t = p.n_qp - 1;
+        }
+        c.k += 1;
+        return;
+    }
     if (pairs && (c.k & 1) == 0) {  // second item of the pair
         c.item += 1;
         c.t += 1;
@@ -260,13 +296,15 @@ __device__ __forceinline__ void next_item(const FwdParams& p, ItemCursor& c, boo
     c.k += 1;
 }
 
-__device__ __forceinline__ Item decode_item(const FwdParams& p, const ItemCursor& c, bool causal, bool alternate)
+__device__ __forceinline__ Item decode_item(const FwdParams& p, const ItemCursor& c, bool causal, bool alternate,
+                                            bool ordered = false)
 {
     const int item = c.item;
     Item it;
     it.bh = c.bh;
     const int t = c.t;
-    const int qp = (t & 1) ? (t >> 1) : p.n_qp - 1 - (t >> 1);  // heavy, light, heavy, light, ...
+    // heavy, light, heavy, light, ...; in the ordered walk (no mask, one-tile last pairs) t is the pair
+    const int qp = ordered ? t : (t & 1) ? (t >> 1) : p.n_qp - 1 - (t >> 1);
     it.i0 = qp * 2 * kBlockM;
     const int n_all = (p.Nk + kBlockN - 1) / kBlockN;
     const int off = p.Nk - p.N;
@@ -312,8 +350,8 @@ __device__ __forceinline__ void fwd_correction(const FwdParams& p, const uint8_t
     const unsigned long long limit = p.wait_limit_ns;
     int done[2] = {0, 0};  // items whose O_i this warpgroup has read, per query tile
     bool ok = true;
-    for (ItemCursor cur = first_item(p, CAUSAL && p.pairs); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs)) {
-        const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
+    for (ItemCursor cur = first_item(p, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp)) {
+        const Item it = decode_item(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int rows = it.rows[i];
@@ -424,8 +462,8 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
             int q_loads[2] = {0, 0};  // loads issued into each Q buffer
             long long g = 0;          // K/V tiles issued so far (ring position)
             bool ok = true;
-            for (ItemCursor cur = first_item(p, CAUSAL && p.pairs); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs)) {
-                const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
+            for (ItemCursor cur = first_item(p, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp)) {
+                const Item it = decode_item(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (it.n[i] == 0) continue;
                     const int b = q_loads[i] % C::kQBuf;  // buffer of this load
@@ -522,8 +560,8 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
                 return true;
             };
 
-            for (ItemCursor cur = first_item(p, CAUSAL && p.pairs); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs)) {
-                const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
+            for (ItemCursor cur = first_item(p, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp)) {
+                const Item it = decode_item(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
                 const int n = i ? it.n[1] : it.n[0];
                 const int q_bar = 2 * (q_uses % C::kQBuf) + i;
                 if (n > 0 && !mbar_wait(bar(kBarQFull + q_bar), (q_uses / C::kQBuf) & 1, limit, abort_flag)) {
@@ -612,8 +650,8 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
         int staged = 0;  // output tiles this warpgroup wrote through the staging tile
         bool ok = true;
 
-        for (ItemCursor cur = first_item(p, CAUSAL && p.pairs); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs)) {
-            const Item it = decode_item(p, cur, CAUSAL, C::kAlternate);
+        for (ItemCursor cur = first_item(p, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp)) {
+            const Item it = decode_item(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
             const int n = wg ? it.n[1] : it.n[0];
             const int rows = wg ? it.rows[1] : it.rows[0];
             const int row0 = wg ? it.r0[1] : it.r0[0];  // first query row of this tile
@@ -848,8 +886,12 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
     const int units = q.pairs ? (p.n_items + 1) / 2 : p.n_items;  // pairs of items, or items
     const int grid = units < p.num_ctas ? units : p.num_ctas;
     const long long step = q.pairs ? 2LL * grid - 1 : grid;  // see next_item
-    q.step_heads = static_cast<int>(step / p.n_qp);
-    q.step_rem = static_cast<int>(step % p.n_qp);
+    const int rem_rows = p.N % (2 * kBlockM);
+    q.n_full = (rem_rows > 0 && rem_rows <= kBlockM) ? p.n_qp - 1 : p.n_qp;
+    // pairs per head of the walk: n_full in the ordered walk (no mask, one-tile last pairs), else n_qp
+    const int per_head = (kOrderedWalk<D, CAUSAL> && q.n_full != p.n_qp) ? (q.n_full > 0 ? q.n_full : 1) : p.n_qp;
+    q.step_heads = static_cast<int>(step / per_head);
+    q.step_rem = static_cast<int>(step % per_head);
     kern<<<grid, kThreads<D, CAUSAL>, C::kSmemBytes, st>>>(q);
     return cudaGetLastError();
 }

@@ -34,6 +34,10 @@ struct FwdParams {
     // and a remainder, so that the kernel advances (head, position) without a division
     int step_heads, step_rem;
     int pairs;          // items go out in heavy/light pairs (causal, more items than CTAs) or singly
+    // Without a mask: pairs per head with rows in both query tiles (all but a last pair of at most
+    // 128 rows).  Items 0 .. BH * n_full - 1 are those pairs, head-major; the BH one-tile last
+    // pairs (if any) come after them, so that they fill the last round instead of lengthening it.
+    int n_full;
 };
 
 // Launch the forward kernel for head size d (= dv), causal flag and output type.

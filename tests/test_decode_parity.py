@@ -166,6 +166,24 @@ def test_gqa_decode(d, R, n_splits):
         assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16), what=f"gqa d={d} R={R} n={n_splits}")
 
 
+@pytest.mark.parametrize("R", [8, 40], ids=["R8_transposed", "R40_row_tile"])
+def test_gqa_zero_and_clamped_lengths(R):
+    """Grouped decode on the tensor core (d = 128) with a zero-length sequence, lengths just past a
+    128-key tile and an out-of-range length: the last is clamped to the cache and reported, a sequence
+    with no keys gives O = 0 and LSE = -inf, the others match the oracle."""
+    B, Hkv, Nk_max, d = 4, 2, 640, 128
+    lens_ok = torch.tensor([0, 129, 257, 640], dtype=torch.int32)
+    q, k, v, _ = gqa_decode_inputs(B, Hkv * R, Hkv, Nk_max, d, d, seed=R, device=DEV, seqlens=lens_ok)
+    lens_in = torch.tensor([0, 129, 257, 700], dtype=torch.int32)  # 700 > Nk_max: clamped to 640
+    o, lse = fa().decode_splitkv_gqa(q, k, v, lens_in.to(DEV), n_splits=3, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == fa().FA_ERR_INVALID_ARG
+    assert fa().get_device_error() == 0
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    o_ref, lse_ref = oracle_gqa_compact(q[1:], k[1:], v[1:], lens_ok[1:], 1 / math.sqrt(d))
+    assert_close(o[1:], lse[1:], o_ref, lse_ref, what=f"gqa lengths R={R}")
+
+
 @pytest.mark.parametrize("Hkv", [8, 4], ids=["R4_cuda_cores", "R8_tensor_core"])
 def test_gqa_full_size_sampled(Hkv):
     """The benchmark's GQA workloads (B=16, Hq=32 over Hkv=8 or 4, d=128, lengths U[1024, 32768]) in
