@@ -41,10 +41,20 @@
 
 namespace fa {
 
-constexpr int kGqThreads = 192;
-constexpr int kGqWarpProducer = 4;
-constexpr int kGqWarpMma = 5;
 constexpr int kGqD = 128;  // head size of this kernel
+
+// Warp layout for RH heads per group: one set of four compute warps (thread t = key t / value
+// column t) per 8 or 16 heads, so a thread handles at most 16 heads; then the producer and the
+// issuer.  Each set reads the same TMEM lanes, its own columns.
+template <int RH>
+struct GqShape {
+    static constexpr int kSets = RH >= 16 ? 2 : 1;
+    static constexpr int kRHS = RH / kSets;  // heads per set
+    static constexpr int kCompute = 4 * kSets;
+    static constexpr int kThreads = 32 * (kCompute + 2);
+    static constexpr int kWarpProducer = kCompute;
+    static constexpr int kWarpMma = kCompute + 1;
+};
 
 enum : int {
     kGbQFull = 0,
@@ -56,8 +66,8 @@ enum : int {
     kGbDrain = 6,
     kGbKVFull = 8,   // + stage
     kGbKVEmpty = 12, // + stage
-    kGbRed = 16,     // + tile parity: the four compute warps' partial maxima (or sums) are in (count 4)
-    kGbCount = 18
+    kGbRed = 16,     // + 2 * set + tile parity: a set's four warps' partial maxima (or sums) are in (count 4)
+    kGbCount = 20
 };
 
 template <int NQ>
@@ -76,7 +86,7 @@ struct GqCfg {
     static constexpr int kOffV = kOffK + kStages * kTileBytes;  // + stage * kTileBytes
     static constexpr int kOffQ = kOffV + kStages * kTileBytes;
     static constexpr int kOffP = kOffQ + kQBytes;               // two P^T buffers
-    static constexpr int kOffRed = kOffP + 2 * kPBytes;         // [2][4 warps][NQ] floats for reductions
+    static constexpr int kOffRed = kOffP + 2 * kPBytes;         // [2][sets][4 warps][heads per set] floats
     static constexpr int kOffBar = kOffRed + 2 * 4 * NQ * 4;
     static constexpr int kUsedBytes = kOffBar + kGbCount * 8 + 16;
     static constexpr int kSmemBytes = kUsedBytes + 1024;        // + alignment slack
@@ -99,9 +109,12 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, unsigned short v)
 // The query map is [groups][R][128] with a box of NQ rows (rows past R are zero-filled), the K/V
 // maps [groups][Nk][128] with 128-row boxes.
 template <int RH>
-__global__ void __launch_bounds__(kGqThreads, 1) fa_gqa_kernel(const __grid_constant__ SplitParams p)
+__global__ void __launch_bounds__(GqShape<RH>::kThreads, 1) fa_gqa_kernel(const __grid_constant__ SplitParams p)
 {
     using C = GqCfg<(RH < 16 ? 16 : RH)>;
+    using G = GqShape<RH>;
+    constexpr int kGqWarpProducer = G::kWarpProducer;
+    constexpr int kGqWarpMma = G::kWarpMma;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t gq_smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gq_smem_raw) + 1023) &
@@ -133,8 +146,8 @@ __global__ void __launch_bounds__(kGqThreads, 1) fa_gqa_kernel(const __grid_cons
     if (threadIdx.x == 0) {
         mbar_init(bar(kGbQFull), 1);
         mbar_init(bar(kGbSFull), 1);
-        mbar_init(bar(kGbSFree), kBlockN);
-        mbar_init(bar(kGbPFull), kBlockN);
+        mbar_init(bar(kGbSFree), 32 * G::kCompute);
+        mbar_init(bar(kGbPFull), 32 * G::kCompute);
         mbar_init(bar(kGbPVDone), 1);
         mbar_init(bar(kGbOReady), 1);
         mbar_init(bar(kGbDrain), 1);
@@ -142,8 +155,7 @@ __global__ void __launch_bounds__(kGqThreads, 1) fa_gqa_kernel(const __grid_cons
             mbar_init(bar(kGbKVFull + i), 1);
             mbar_init(bar(kGbKVEmpty + i), 1);
         }
-        mbar_init(bar(kGbRed + 0), 4);
-        mbar_init(bar(kGbRed + 1), 4);
+        for (int i = 0; i < 4; ++i) mbar_init(bar(kGbRed + i), 4);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -247,35 +259,46 @@ __global__ void __launch_bounds__(kGqThreads, 1) fa_gqa_kernel(const __grid_cons
         }
     } else {
         // ============================================================ compute
-        constexpr int NQ = C::kNQ;
-        const int k = threadIdx.x;  // key k of S^T and value column k of O^T (TMEM lane k)
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t t_s = tmem + lane_base + C::kColS;
-        const uint32_t t_o = tmem + lane_base + C::kColO;
+        constexpr int RS = G::kRHS;  // heads of this thread's set
+        const int set = warp >> 2;
+        const int h0 = set * RS;     // first head of the set
+        const int wq = warp & 3;     // warp within the set: TMEM lanes 32 wq .. 32 wq + 31
+        const int k = threadIdx.x & 127;  // key k of S^T and value column k of O^T (TMEM lane k)
+        const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t t_s = tmem + lane_base + C::kColS + static_cast<uint32_t>(h0);
+        const uint32_t t_o = tmem + lane_base + C::kColO + static_cast<uint32_t>(h0);
         float* red = reinterpret_cast<float*>(smem + C::kOffRed);
         const float sl2 = p.scale_log2;
-        float m_run[RH], l[RH];  // per head: running max (base 2, scale folded in), this key's share of l
+        float m_run[RS], l[RS];  // per head: running max (base 2, scale folded in), this key's share of l
 #pragma unroll
-        for (int h = 0; h < RH; ++h) {
-            m_run[h] = -INFINITY;
-            l[h] = 0.f;
+        for (int i = 0; i < RS; ++i) {
+            m_run[i] = -INFINITY;
+            l[i] = 0.f;
         }
-        // The four warps' values of each head combined through shared memory (use: exchange number,
-        // alternating between two buffers and barriers).  False if the wait ran out.
-        auto exchange = [&](float (&v)[RH], int use, bool is_max) -> bool {
-            float* rb = red + (use & 1) * 4 * RH;
+        auto ld_cols = [&](uint32_t taddr, uint32_t (&r)[RS]) {
+            if constexpr (RS == 8) tmem_ld8(taddr, r);
+            else tmem_ld16(taddr, r);
+        };
+        auto st_cols = [&](uint32_t taddr, const uint32_t (&r)[RS]) {
+            if constexpr (RS == 8) tmem_st8(taddr, r);
+            else tmem_st16(taddr, r);
+        };
+        // The set's four warps' values of each head combined through shared memory (use: exchange
+        // number, alternating between two buffers and barriers per set).  False if the wait ran out.
+        auto exchange = [&](float (&v)[RS], int use, bool is_max) -> bool {
+            float* rb = red + ((use & 1) * G::kSets + set) * 4 * RS;
+            const int rbar = kGbRed + 2 * set + (use & 1);
             if (lane == 0) {
 #pragma unroll
-                for (int h = 0; h < RH; ++h) rb[warp * RH + h] = v[h];
-                mbar_arrive(bar(kGbRed + (use & 1)));
+                for (int i = 0; i < RS; ++i) rb[wq * RS + i] = v[i];
+                mbar_arrive(bar(rbar));
             }
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(kGbRed + (use & 1)), static_cast<uint32_t>(use >> 1) & 1, limit,
-                                                   abort_flag)))
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(rbar), static_cast<uint32_t>(use >> 1) & 1, limit, abort_flag)))
                 return false;
 #pragma unroll
-            for (int h = 0; h < RH; ++h)
-                v[h] = is_max ? fmaxf(fmaxf(rb[h], rb[RH + h]), fmaxf(rb[2 * RH + h], rb[3 * RH + h]))
-                              : (rb[h] + rb[RH + h]) + (rb[2 * RH + h] + rb[3 * RH + h]);
+            for (int i = 0; i < RS; ++i)
+                v[i] = is_max ? fmaxf(fmaxf(rb[i], rb[RS + i]), fmaxf(rb[2 * RS + i], rb[3 * RS + i]))
+                              : (rb[i] + rb[RS + i]) + (rb[2 * RS + i] + rb[3 * RS + i]);
             return true;
         };
         bool ok = true;
@@ -283,37 +306,36 @@ __global__ void __launch_bounds__(kGqThreads, 1) fa_gqa_kernel(const __grid_cons
             ok = __all_sync(0xffffffffu, mbar_wait(bar(kGbSFull), t & 1, limit, abort_flag));
             if (!ok) break;
             tc_fence_after_sync();
-            uint32_t u[NQ];
-            if constexpr (NQ == 16) tmem_ld16(t_s, u);
-            else tmem_ld32(t_s, u);
+            uint32_t u[RS];
+            ld_cols(t_s, u);
             tmem_ld_wait();
             tc_fence_before_sync();
             mbar_arrive(bar(kGbSFree));
             const int k0 = (j_begin + t) * kBlockN;
             const bool live = k0 + k < kh;  // keys past the split or the sequence weigh 0
-            float sv[RH], mx[RH];
+            float sv[RS], mx[RS];
 #pragma unroll
-            for (int h = 0; h < RH; ++h) {
-                sv[h] = live ? __uint_as_float(u[h]) : -INFINITY;
-                mx[h] = sv[h];
+            for (int i = 0; i < RS; ++i) {
+                sv[i] = live ? __uint_as_float(u[i]) : -INFINITY;
+                mx[i] = sv[i];
             }
             // each head's maximum over the tile's 128 keys
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-                for (int h = 0; h < RH; ++h) mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], off));
+                for (int i = 0; i < RS; ++i) mx[i] = fmaxf(mx[i], __shfl_xor_sync(0xffffffffu, mx[i], off));
             ok = exchange(mx, t, true);
             if (!ok) break;
-            // new running maxima and rescale factors: the same in every thread
-            float alpha[RH];
+            // new running maxima and rescale factors: the same in every thread of the set
+            float alpha[RS];
             bool grew = false;
 #pragma unroll
-            for (int h = 0; h < RH; ++h) {
-                const float mt = mx[h] * sl2;
-                alpha[h] = 1.f;
-                if (mt > m_run[h]) {
-                    alpha[h] = ex2(m_run[h] - mt);  // 0 when m_run = -inf
-                    m_run[h] = mt;
+            for (int i = 0; i < RS; ++i) {
+                const float mt = mx[i] * sl2;
+                alpha[i] = 1.f;
+                if (mt > m_run[i]) {
+                    alpha[i] = ex2(m_run[i] - mt);  // 0 when m_run = -inf
+                    m_run[i] = mt;
                     grew = true;
                 }
             }
@@ -321,14 +343,15 @@ __global__ void __launch_bounds__(kGqThreads, 1) fa_gqa_kernel(const __grid_cons
             const uint32_t pb = sbase + C::kOffP + (t & 1) * C::kPBytes + (k >> 6) * C::kPBlkBytes;
             const int e = k & 63;
 #pragma unroll
-            for (int h = 0; h < RH; ++h) {
-                const float mu = m_run[h] == -INFINITY ? 0.f : m_run[h];
-                const float pv = ex2(fmaf(sv[h], sl2, -mu));
-                l[h] = fmaf(l[h], alpha[h], pv);
+            for (int i = 0; i < RS; ++i) {
+                const int h = h0 + i;
+                const float mu = m_run[i] == -INFINITY ? 0.f : m_run[i];
+                const float pv = ex2(fmaf(sv[i], sl2, -mu));
+                l[i] = fmaf(l[i], alpha[i], pv);
                 st_shared_u16(pb + h * C::kRowBytes + ((static_cast<uint32_t>((e >> 3) ^ (h & 7))) << 4) + (e & 7) * 2,
                               __bfloat16_as_ushort(__float2bfloat16_rn(pv)));
             }
-            if (k0 + kBlockN > len) {
+            if (set == 0 && k0 + kBlockN > len) {
                 // V rows past the sequence may hold anything: zero them before the product reads
                 // them (their weight is 0, but 0 * NaN would poison O).  Row k of each 128-row column
                 // block is one 128-byte line whatever the swizzle.
@@ -350,15 +373,13 @@ __global__ void __launch_bounds__(kGqThreads, 1) fa_gqa_kernel(const __grid_cons
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(kGbPVDone), (t - 1) & 1, limit, abort_flag));
                 if (!ok) break;
                 tc_fence_after_sync();
-                if (grew) {  // the same in every thread
-                    uint32_t o[NQ];
-                    if constexpr (NQ == 16) tmem_ld16(t_o, o);
-                    else tmem_ld32(t_o, o);
+                if (grew) {  // the same in every thread of the set
+                    uint32_t o[RS];
+                    ld_cols(t_o, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < RH; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h]);
-                    if constexpr (NQ == 16) tmem_st16(t_o, o);
-                    else tmem_st32(t_o, o);
+                    for (int i = 0; i < RS; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha[i]);
+                    st_cols(t_o, o);
                     tmem_st_wait();
                 }
             }
@@ -370,32 +391,32 @@ __global__ void __launch_bounds__(kGqThreads, 1) fa_gqa_kernel(const __grid_cons
             if (ok) tc_fence_after_sync();
         }
         // epilogue: each head's sum over all keys of the split, then the split's normalised
-        // output (thread k writes value column k of every head: coalesced rows) and log-sum-exp
-        // (o = 0, lse = -inf for a split with no key).
+        // output (thread k writes value column k of the set's heads: coalesced rows) and
+        // log-sum-exp (o = 0, lse = -inf for a split with no key).
         if (ok && nt > 0) {
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-                for (int h = 0; h < RH; ++h) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+                for (int i = 0; i < RS; ++i) l[i] += __shfl_xor_sync(0xffffffffu, l[i], off);
             ok = exchange(l, nt, false);
         }
         if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
         if (ok) {  // uniform across the warp (from __all_sync)
-            uint32_t o[NQ];
+            uint32_t o[RS];
             if (nt > 0) {
-                if constexpr (NQ == 16) tmem_ld16(t_o, o);
-                else tmem_ld32(t_o, o);
+                ld_cols(t_o, o);
                 tmem_ld_wait();
             }
             const size_t row0 = static_cast<size_t>(g) * R;
 #pragma unroll
-            for (int h = 0; h < RH; ++h) {
+            for (int i = 0; i < RS; ++i) {
+                const int h = h0 + i;
                 if (h < R) {
                     const size_t slot = (row0 + h) * p.n_splits + s;
-                    const float val = (nt > 0 && l[h] > 0.f) ? __uint_as_float(o[h]) / l[h] : 0.f;
+                    const float val = (nt > 0 && l[i] > 0.f) ? __uint_as_float(o[i]) / l[i] : 0.f;
                     p.o_part[slot * kGqD + k] = val;
-                    if (k == h)
-                        p.lse_part[slot] = (nt > 0 && l[h] > 0.f) ? (m_run[h] + lg2_approx(l[h])) * 0.69314718055994531f
+                    if (k == i)
+                        p.lse_part[slot] = (nt > 0 && l[i] > 0.f) ? (m_run[i] + lg2_approx(l[i])) * 0.69314718055994531f
                                                                   : -INFINITY;
                 }
             }
@@ -427,7 +448,7 @@ cudaError_t launch_gqa_t(const SplitParams& p, cudaStream_t st)
         configured[dev] = true;
     }
     dim3 grid(p.n_splits, p.groups_per_batch, p.n_groups / p.groups_per_batch);
-    kern<<<grid, kGqThreads, C::kSmemBytes, st>>>(p);
+    kern<<<grid, GqShape<RH>::kThreads, C::kSmemBytes, st>>>(p);
     return cudaGetLastError();
 }
 
