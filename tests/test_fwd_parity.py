@@ -30,8 +30,10 @@ def run(q, k, v, causal, scale=None, out_dtype=torch.float32):
 
 # (B, H, N, Nk, d, mult): the single-head 256 x 256 case, the pages' demo shapes (77 x 513 with
 # causal offset 436, 300 x 300, a single query over 1000 keys), several tiles with ragged tails,
-# and N > Nk (causal rows with no visible key).
+# N > Nk (causal rows with no visible key), and 160 heads of 333 rows at d = 128 (320 items for 152
+# CTAs: without a mask the walk crosses from the full query pairs to the one-tile last pairs).
 SMALL = [
+    (4, 40, 333, 333, 128, 1.0),
     (1, 1, 256, 256, 64, 1.0),
     (8, 8, 77, 513, 32, 2.0),
     (2, 3, 300, 300, 64, 1.0),
