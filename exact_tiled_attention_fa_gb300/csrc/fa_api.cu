@@ -437,18 +437,24 @@ cudaError_t merge_rows(const float* o_part, const float* lse_part, int rows, int
 // the tensor core, 8 heads per group 1.2 vs 3.5 TB/s.
 bool gqa_on_cuda_cores(int R) { return R == 1 || R == 2 || R == 4; }
 
-// Tensor-core groups: one CTA (a whole SM) per (b, key/value head, split).  The CTA's time goes
-// to the per-tile softmax chain, not to the bytes, so the count aims at about 1.7 CTAs per SM
-// (the lengths vary, and many of the later splits are short or empty): measured on GB300, d = 128,
-// 32 or 64 query heads, this is within a few per cent of the best count swept for groups of 8,
-// 16 and 32 heads and 4-64 sequences, and 25-70 % above six CTAs per SM for 16- and 32-head groups.
+// Tensor-core groups: one CTA per (b, key/value head, split); groups of 5 to 8 heads at d = 128
+// run two CTAs per SM, the others one.  A CTA's time goes to the per-tile softmax chain more than
+// to the bytes, and the lengths vary (many of the later splits are short or empty), so the count
+// aims at about 1.7 CTAs per CTA slot; splits longer than 32 key tiles are cut down further, so
+// that many groups still spread evenly over the slots.  Measured on GB300, d = 128, 1-32K cached
+// tokens, 32 or 64 query heads over 1-8 key/value heads, 4-64 sequences: within 3 % of the best
+// count swept for 8-, 16- and 32-head groups; 8-head groups of 64 sequences x 4 key/value heads
+// with 2 splits of 32K keys 6.2 TB/s, with 8 splits 6.8.
 // At least two splits while the groups alone leave SMs idle; each split at least one 128-key tile.
-int gqa_tc_default_splits(int B, int Hkv, int Nk_max, int sms)
+int gqa_tc_default_splits(int B, int R, int Hkv, int Nk_max, int sms)
 {
     const long long groups = static_cast<long long>(B) * Hkv;
-    long long n = 17LL * sms / (10LL * groups);
+    const long long slots = static_cast<long long>(sms) * (R >= 5 && R <= 8 ? 2 : 1);
+    long long n = 17LL * slots / (10LL * groups);
     if (n < 2 && groups < 2LL * sms) n = 2;
     const long long max_n = (static_cast<long long>(Nk_max) + fa::kBlockN - 1) / fa::kBlockN;
+    const long long min_n = (max_n + 31) / 32;
+    if (n < min_n) n = min_n;
     if (n > max_n) n = max_n;
     if (n < 1) n = 1;
     return static_cast<int>(n);
@@ -565,7 +571,7 @@ int fa_decode_gqa_default_splits(int B, int Hq, int Hkv, int Nk_max, int num_sms
     // On CUDA cores a CTA's arithmetic grows with the R heads it carries, so the count follows the
     // B * Hq query heads (R = 4: 4.3 -> 4.8 TB/s against counting B * Hkv items).
     return gqa_on_cuda_cores(Hq / Hkv) ? fa_decode_default_splits(B, Hq, Nk_max, num_sms)
-                                       : gqa_tc_default_splits(B, Hkv, Nk_max, num_sms);
+                                       : gqa_tc_default_splits(B, Hq / Hkv, Hkv, Nk_max, num_sms);
 }
 
 fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,

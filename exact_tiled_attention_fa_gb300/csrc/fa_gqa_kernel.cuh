@@ -22,7 +22,7 @@
 //
 // One CTA per (split, group = (sequence, key/value head)); six warps:
 //   warps 0-3  compute: thread t owns key t of S^T and value column t of O^T.
-//   warp 4     TMA producer: the group's NQ query rows once, K_j and V_j into a ring.
+//   warp 4     TMA producer: the group's NQ query rows once, K_j and V_j into rings of their own.
 //   warp 5     tcgen05 issuer: S^T(j+1) as soon as S^T(j) has been read, O^T += V_j^T P^T(j).
 // Tensor memory: S^T in columns [0, NQ), O^T in [NQ, 2 NQ).
 // Cache rows past a sequence's length may hold anything (the tests fill them with NaN): their
@@ -64,17 +64,27 @@ enum : int {
     kGbPVDone = 4,
     kGbOReady = 5,
     kGbDrain = 6,
-    kGbKVFull = 8,   // + stage
-    kGbKVEmpty = 12, // + stage
-    kGbRed = 16,     // + 2 * set + tile parity: a set's four warps' partial maxima (or sums) are in (count 4)
-    kGbCount = 20
+    kGbKFull = 8,    // + K stage (up to 3)
+    kGbKEmpty = 11,  // + K stage: S^T of the tile has completed
+    kGbVFull = 14,   // + V stage (up to 2)
+    kGbVEmpty = 16,  // + V stage: the tile's product has completed
+    kGbRed = 18,     // + 2 * set + tile parity: a set's four warps' partial maxima (or sums) are in (count 4)
+    kGbCount = 22
 };
 
-template <int NQ>
+template <int RH>
 struct GqCfg {
-    static_assert(NQ == 16 || NQ == 32, "padded query heads per group");
+    static constexpr int NQ = RH < 16 ? 16 : RH;  // MMA columns: the heads padded to 16 or 32
+    static_assert(RH == 8 || RH == 16 || RH == 32, "heads per group handled by the compute threads");
     static constexpr int kNQ = NQ;
-    static constexpr int kStages = 3;
+    // K and V go through separate rings: K_j is free once S^T(j) has completed, early in the tile,
+    // V_j only after the product.  With 8 heads two K stages and one V stage keep a CTA at ~109 KB
+    // and 96 registers a thread, so two CTAs share an SM and each one's wait for V is covered by
+    // the other's work.  16 and 32 heads (two warp sets of compute threads) run once per SM with
+    // deeper rings.
+    static constexpr int kKStages = RH == 8 ? 2 : 3;
+    static constexpr int kVStages = RH == 8 ? 1 : 2;
+    static constexpr int kCtasPerSm = RH == 8 ? 2 : 1;
     static constexpr int kRowBytes = 128;                       // one 64-element column block row
     static constexpr int kBlkBytes = kBlockN * kRowBytes;       // 128 rows of one column block
     static constexpr int kTileBytes = 2 * kBlkBytes;            // 128 x 128 bf16 (K or V tile)
@@ -82,15 +92,15 @@ struct GqCfg {
     static constexpr int kQBytes = 2 * kQBlkBytes;
     static constexpr int kPBlkBytes = NQ * kRowBytes;           // P^T: NQ rows x 64 keys
     static constexpr int kPBytes = 2 * kPBlkBytes;              // NQ rows x 128 keys
-    static constexpr int kOffK = 0;                             // + stage * kTileBytes
-    static constexpr int kOffV = kOffK + kStages * kTileBytes;  // + stage * kTileBytes
-    static constexpr int kOffQ = kOffV + kStages * kTileBytes;
+    static constexpr int kOffK = 0;                              // + stage * kTileBytes
+    static constexpr int kOffV = kOffK + kKStages * kTileBytes;  // + stage * kTileBytes
+    static constexpr int kOffQ = kOffV + kVStages * kTileBytes;
     static constexpr int kOffP = kOffQ + kQBytes;               // two P^T buffers
     static constexpr int kOffRed = kOffP + 2 * kPBytes;         // [2][sets][4 warps][heads per set] floats
     static constexpr int kOffBar = kOffRed + 2 * 4 * NQ * 4;
     static constexpr int kUsedBytes = kOffBar + kGbCount * 8 + 16;
     static constexpr int kSmemBytes = kUsedBytes + 1024;        // + alignment slack
-    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert(kSmemBytes * kCtasPerSm <= 228 * 1024 - kCtasPerSm * 1024, "shared memory per SM");
     static constexpr int kTmemCols = 2 * NQ < 32 ? 32 : 2 * NQ;
     static constexpr uint32_t kColS = 0, kColO = NQ;
     // S^T = K Q^T: M = 128 keys, N = NQ heads, both operands K-major
@@ -109,13 +119,15 @@ __device__ __forceinline__ void st_shared_u16(uint32_t addr, unsigned short v)
 // The query map is [groups][R][128] with a box of NQ rows (rows past R are zero-filled), the K/V
 // maps [groups][Nk][128] with 128-row boxes.
 template <int RH>
-__global__ void __launch_bounds__(GqShape<RH>::kThreads, 1) fa_gqa_kernel(const __grid_constant__ SplitParams p)
+__global__ void __launch_bounds__(GqShape<RH>::kThreads, GqCfg<RH>::kCtasPerSm)
+    fa_gqa_kernel(const __grid_constant__ SplitParams p)
 {
-    using C = GqCfg<(RH < 16 ? 16 : RH)>;
+    using C = GqCfg<RH>;
     using G = GqShape<RH>;
     constexpr int kGqWarpProducer = G::kWarpProducer;
     constexpr int kGqWarpMma = G::kWarpMma;
-    constexpr int S = C::kStages;
+    constexpr int SK = C::kKStages;
+    constexpr int SV = C::kVStages;
     extern __shared__ uint8_t gq_smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gq_smem_raw) + 1023) &
                                                ~static_cast<uintptr_t>(1023));
@@ -151,9 +163,13 @@ __global__ void __launch_bounds__(GqShape<RH>::kThreads, 1) fa_gqa_kernel(const 
         mbar_init(bar(kGbPVDone), 1);
         mbar_init(bar(kGbOReady), 1);
         mbar_init(bar(kGbDrain), 1);
-        for (int i = 0; i < S; ++i) {
-            mbar_init(bar(kGbKVFull + i), 1);
-            mbar_init(bar(kGbKVEmpty + i), 1);
+        for (int i = 0; i < SK; ++i) {
+            mbar_init(bar(kGbKFull + i), 1);
+            mbar_init(bar(kGbKEmpty + i), 1);
+        }
+        for (int i = 0; i < SV; ++i) {
+            mbar_init(bar(kGbVFull + i), 1);
+            mbar_init(bar(kGbVEmpty + i), 1);
         }
         for (int i = 0; i < 4; ++i) mbar_init(bar(kGbRed + i), 4);
         *abort_flag = 0;
@@ -178,28 +194,49 @@ __global__ void __launch_bounds__(GqShape<RH>::kThreads, 1) fa_gqa_kernel(const 
             mbar_arrive_expect_tx(bar(kGbQFull), C::kQBytes);
             for (int cb = 0; cb < 2; ++cb)
                 tma_load_3d(sbase + C::kOffQ + cb * C::kQBlkBytes, &p.tm_q, bar(kGbQFull), cb * 64, 0, g, pol);
-            int issued = 0;
+            // K runs one tile ahead of V: K_j is released early in tile j (once S^T(j) is done),
+            // V_j only after the product of tile j
+            int k_issued = 0, v_issued = 0;
             bool ok = true;
-            for (int t = 0; t < nt; ++t) {
-                const int st = t % S;
-                if (t >= S && !mbar_wait(bar(kGbKVEmpty + st), static_cast<uint32_t>(t / S - 1) & 1, limit, abort_flag)) {
+            auto load_k = [&](int t) -> bool {
+                const int st = t % SK;
+                if (t >= SK && !mbar_wait(bar(kGbKEmpty + st), static_cast<uint32_t>(t / SK - 1) & 1, limit, abort_flag))
+                    return false;
+                mbar_arrive_expect_tx(bar(kGbKFull + st), C::kTileBytes);
+                for (int cb = 0; cb < 2; ++cb)
+                    tma_load_3d(sbase + C::kOffK + st * C::kTileBytes + cb * C::kBlkBytes, &p.tm_k, bar(kGbKFull + st),
+                                cb * 64, (j_begin + t) * kBlockN, g, pol);
+                ++k_issued;
+                return true;
+            };
+            auto load_v = [&](int t) -> bool {
+                const int st = t % SV;
+                if (t >= SV && !mbar_wait(bar(kGbVEmpty + st), static_cast<uint32_t>(t / SV - 1) & 1, limit, abort_flag))
+                    return false;
+                mbar_arrive_expect_tx(bar(kGbVFull + st), C::kTileBytes);
+                for (int cb = 0; cb < 2; ++cb)
+                    tma_load_3d(sbase + C::kOffV + st * C::kTileBytes + cb * C::kBlkBytes, &p.tm_v, bar(kGbVFull + st),
+                                cb * 64, (j_begin + t) * kBlockN, g, pol);
+                ++v_issued;
+                return true;
+            };
+            ok = load_k(0);
+            for (int t = 0; ok && t < nt; ++t) {
+                if (t + 1 < nt && !load_k(t + 1)) {
                     ok = false;
                     break;
                 }
-                const int k0 = (j_begin + t) * kBlockN;
-                mbar_arrive_expect_tx(bar(kGbKVFull + st), 2 * C::kTileBytes);
-                for (int cb = 0; cb < 2; ++cb) {
-                    tma_load_3d(sbase + C::kOffK + st * C::kTileBytes + cb * C::kBlkBytes, &p.tm_k, bar(kGbKVFull + st),
-                                cb * 64, k0, g, pol);
-                    tma_load_3d(sbase + C::kOffV + st * C::kTileBytes + cb * C::kBlkBytes, &p.tm_v, bar(kGbKVFull + st),
-                                cb * 64, k0, g, pol);
+                if (!load_v(t)) {
+                    ok = false;
+                    break;
                 }
-                ++issued;
             }
             if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
             mbar_wait(bar(kGbQFull), 0, kDrainLimitNs, nullptr);
-            for (int t = issued - S < 0 ? 0 : issued - S; t < issued; ++t)
-                mbar_wait(bar(kGbKVFull + t % S), static_cast<uint32_t>(t / S) & 1, kDrainLimitNs, nullptr);
+            for (int t = k_issued - SK < 0 ? 0 : k_issued - SK; t < k_issued; ++t)
+                mbar_wait(bar(kGbKFull + t % SK), static_cast<uint32_t>(t / SK) & 1, kDrainLimitNs, nullptr);
+            for (int t = v_issued - SV < 0 ? 0 : v_issued - SV; t < v_issued; ++t)
+                mbar_wait(bar(kGbVFull + t % SV), static_cast<uint32_t>(t / SV) & 1, kDrainLimitNs, nullptr);
         }
     } else if (warp == kGqWarpMma) {
         // ============================================================ MMA issuer
@@ -232,25 +269,27 @@ __global__ void __launch_bounds__(GqShape<RH>::kThreads, 1) fa_gqa_kernel(const 
                     umma_ss(tmem + C::kColO, a0 + oa, b0 + ob, C::kIdescO, (accumulate || kk > 0) ? 1u : 0u);
                 }
             };
-            if (wait(kGbQFull, 0) && wait(kGbKVFull, 0)) {
+            if (wait(kGbQFull, 0) && wait(kGbKFull, 0)) {
                 tc_fence_after_sync();
                 issue_s(0);
                 umma_commit(bar(kGbSFull));
+                umma_commit(bar(kGbKEmpty));  // K_0 is free once S^T(0) has completed
             }
             for (int t = 0; ok && t < nt; ++t) {
-                const int st = t % S;
+                const int sv = t % SV;
                 if (t + 1 < nt) {  // S^T(t+1) as soon as the compute threads have read S^T(t)
-                    const int sn = (t + 1) % S;
-                    if (!wait(kGbKVFull + sn, (t + 1) / S) || !wait(kGbSFree, t)) break;
+                    const int sn = (t + 1) % SK;
+                    if (!wait(kGbKFull + sn, (t + 1) / SK) || !wait(kGbSFree, t)) break;
                     tc_fence_after_sync();
                     issue_s(sn);
                     umma_commit(bar(kGbSFull));
+                    umma_commit(bar(kGbKEmpty + sn));
                 }
-                if (!wait(kGbPFull, t)) break;
+                if (!wait(kGbVFull + sv, t / SV) || !wait(kGbPFull, t)) break;
                 tc_fence_after_sync();
-                issue_pv(st, t & 1, t > 0);
+                issue_pv(sv, t & 1, t > 0);
                 umma_commit(bar(kGbPVDone));
-                umma_commit(bar(kGbKVEmpty + st));
+                umma_commit(bar(kGbVEmpty + sv));
             }
             umma_commit(bar(kGbOReady));
             if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
@@ -354,12 +393,15 @@ __global__ void __launch_bounds__(GqShape<RH>::kThreads, 1) fa_gqa_kernel(const 
             if (set == 0 && k0 + kBlockN > len) {
                 // V rows past the sequence may hold anything: zero them before the product reads
                 // them (their weight is 0, but 0 * NaN would poison O).  Row k of each 128-row column
-                // block is one 128-byte line whatever the swizzle.
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(kGbKVFull + t % S), static_cast<uint32_t>(t / S) & 1, limit,
-                                                       abort_flag));
+                // block is one 128-byte line whatever the swizzle.  V_t is waited for only after the
+                // previous product has completed: with one V stage, the stage's barrier could
+                // otherwise still be on V_{t-1}'s phase, whose parity reads as V_t's being done.
+                bool w = t == 0 || mbar_wait(bar(kGbPVDone), (t - 1) & 1, limit, abort_flag);
+                w = w && mbar_wait(bar(kGbVFull + t % SV), static_cast<uint32_t>(t / SV) & 1, limit, abort_flag);
+                ok = __all_sync(0xffffffffu, w);
                 if (!ok) break;
                 if (k0 + k >= len) {
-                    const uint32_t vrow = sbase + C::kOffV + (t % S) * C::kTileBytes + k * C::kRowBytes;
+                    const uint32_t vrow = sbase + C::kOffV + (t % SV) * C::kTileBytes + k * C::kRowBytes;
 #pragma unroll
                     for (int cb = 0; cb < 2; ++cb)
 #pragma unroll
@@ -435,7 +477,7 @@ __global__ void __launch_bounds__(GqShape<RH>::kThreads, 1) fa_gqa_kernel(const 
 template <int RH>
 cudaError_t launch_gqa_t(const SplitParams& p, cudaStream_t st)
 {
-    using C = GqCfg<(RH < 16 ? 16 : RH)>;
+    using C = GqCfg<RH>;
     auto kern = fa_gqa_kernel<RH>;
     static bool configured[64] = {};
     int dev = 0;

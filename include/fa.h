@@ -177,9 +177,11 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
  * Split count fa_decode_splitkv_gqa uses when asked for n_splits = 0, for Hq query heads over Hkv
  * key/value heads on a device with `num_sms` multiprocessors.  Groups of R = Hq / Hkv = 1, 2 or
  * 4 heads (CUDA cores) take fa_decode_default_splits(B, Hq, Nk_max, num_sms).  Other groups
- * (tensor core, one CTA per multiprocessor) take floor(1.7 * num_sms / (B * Hkv)) splits, raised
- * to 2 while B * Hkv < 2 * num_sms, then clamped to [1, ceil(Nk_max / 128)].  Pure host
- * function.  Returns 0 on invalid arguments (a non-positive size, or Hkv not dividing Hq).
+ * (tensor core) take floor(1.7 * c * num_sms / (B * Hkv)) splits, where c = 2 for R = 5 to 8
+ * (two CTAs per multiprocessor) and 1 otherwise; raised to 2 while B * Hkv < 2 * num_sms, then
+ * to ceil(ceil(Nk_max / 128) / 32) (no split longer than 32 key tiles), then clamped to
+ * [1, ceil(Nk_max / 128)].  Pure host function.  Returns 0 on invalid arguments (a non-positive
+ * size, or Hkv not dividing Hq).
  */
 int fa_decode_gqa_default_splits(int B, int Hq, int Hkv, int Nk_max, int num_sms);
 

@@ -139,11 +139,15 @@ def test_gqa_split_heuristic(lib):
     # groups of 1, 2 and 4 heads (CUDA cores) follow the B * Hq query heads
     for (B, Hq, Hkv) in ((16, 32, 8), (16, 32, 16), (16, 32, 32), (3, 8, 2)):
         assert g(B, Hq, Hkv, 32768, 152) == ds(B, Hq, 32768, 152)
-    # other groups (tensor core): floor(1.7 * SMs / (B * Hkv)), at least 2 while the groups leave
-    # SMs idle, clamped to [1, ceil(Nk_max / 128)]
-    assert g(16, 32, 4, 32768, 152) == 4 and g(16, 32, 2, 32768, 152) == 8 and g(16, 32, 1, 32768, 152) == 16
+    # other groups (tensor core): floor(1.7 * slots / (B * Hkv)) with two CTA slots per SM for 5-8
+    # heads, one otherwise; at least 2 while the groups leave SMs idle; no split longer than 32
+    # key tiles; clamped to [1, ceil(Nk_max / 128)]
+    assert g(16, 32, 4, 32768, 152) == 8 and g(16, 32, 2, 32768, 152) == 8 and g(16, 32, 1, 32768, 152) == 16
+    assert g(4, 32, 4, 32768, 152) == 32 and g(4, 40, 8, 32768, 152) == 16  # 5 heads: two slots per SM
     assert g(64, 32, 4, 4096, 152) == 2 and g(1000, 32, 4, 4096, 152) == 1
+    assert g(64, 32, 4, 32768, 152) == 8 and g(1000, 32, 4, 32768, 152) == 8  # 32 tiles per split at most
     assert g(4, 32, 1, 256, 152) == 2 and g(1, 128, 1, 100, 152) == 1
+    assert g(1, 24, 8, 1 << 20, 152) == 256  # 3 heads: 32 by the slots, 8192 tiles / 32 by length
 
 
 def test_status_strings(lib):
