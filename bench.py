@@ -706,7 +706,7 @@ def run_decode_gqa(fa, dev, stream, args, world, Hkv=None):
     q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=GQA["lo"], hi=GQA["hi"], device=dev)
     lens_d = lens.to(dev)
     n = 0  # the library's automatic split count
-    n_auto = fa.decode_gqa_default_splits(B, Hq, Hkv, Nk_max, fa.num_sms(dev))
+    n_auto = fa.decode_gqa_default_splits(B, Hq, Hkv, Nk_max, d, fa.num_sms(dev))
     ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n_auto), dtype=torch.uint8, device=dev)
     o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
@@ -721,7 +721,7 @@ def run_decode_gqa(fa, dev, stream, args, world, Hkv=None):
     pk, src = peaks()
     gbs = world * (kv_bytes + other) / (ms / 1e3) / 1e9
     return {"workload": f"GQA split-KV decode B={B} Hq={Hq} Hkv={Hkv} d={d}, lengths U[1024,32768] (seed 0), bf16 O",
-            "group": Hq // Hkv, "n_splits": n_auto, "timing": st, "unit": "tensor core" if Hq // Hkv not in (1, 2, 4) else "CUDA cores", "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
+            "group": Hq // Hkv, "n_splits": n_auto, "timing": st, "unit": "CUDA cores" if Hq // Hkv in (1, 2) or (Hq // Hkv == 4 and d != 128) else "tensor core", "ms": ms, "gbs": gbs, "kv_bytes": kv_bytes, "frac_of_hbm": gbs / float(pk["hbm_gbs"]),
             "frac_of_8tbs": gbs / 8000.0, "peak_source": src, "launches_per_call": 2}
 
 
@@ -769,7 +769,7 @@ def _case_call(fa, dev, name):
         Hkv = Hq // (4 if name == "gqa4" else 8)
         q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=GQA["lo"], hi=GQA["hi"], device=dev)
         lens_d = lens.to(dev)
-        n = fa.decode_gqa_default_splits(B, Hq, Hkv, Nk_max, fa.num_sms(dev))
+        n = fa.decode_gqa_default_splits(B, Hq, Hkv, Nk_max, d, fa.num_sms(dev))
         ws = torch.empty(fa.decode_workspace_size(B, Hq, d, n), dtype=torch.uint8, device=dev)
         o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)

@@ -57,7 +57,7 @@ def _load():
     lib.fa_bwd.restype = i
     lib.fa_decode_default_splits.argtypes = [i, i, i, i]
     lib.fa_decode_default_splits.restype = i
-    lib.fa_decode_gqa_default_splits.argtypes = [i, i, i, i, i]
+    lib.fa_decode_gqa_default_splits.argtypes = [i, i, i, i, i, i]
     lib.fa_decode_gqa_default_splits.restype = i
     lib.fa_decode_workspace_size.argtypes = [i, i, i, i]
     lib.fa_decode_workspace_size.restype = sz
@@ -290,8 +290,8 @@ def decode_default_splits(B, H, Nk_max, num_sms):
     return int(_load().fa_decode_default_splits(B, H, Nk_max, num_sms))
 
 
-def decode_gqa_default_splits(B, Hq, Hkv, Nk_max, num_sms):
-    return int(_load().fa_decode_gqa_default_splits(B, Hq, Hkv, Nk_max, num_sms))
+def decode_gqa_default_splits(B, Hq, Hkv, Nk_max, d, num_sms):
+    return int(_load().fa_decode_gqa_default_splits(B, Hq, Hkv, Nk_max, d, num_sms))
 
 
 def decode_workspace_size(B, H, dv, n_splits):
@@ -364,7 +364,7 @@ def decode_splitkv_gqa(q, k_cache, v_cache, seqlens, scale=None, n_splits=0, out
         raise ValueError("shape mismatch between q, caches and seqlens")
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     # (0 for groups the library rejects; the call below then reports why)
-    n = int(n_splits) if n_splits else decode_gqa_default_splits(B, Hq, Hkv, Nk_max, num_sms(dev))
+    n = int(n_splits) if n_splits else decode_gqa_default_splits(B, Hq, Hkv, Nk_max, d, num_sms(dev))
     if workspace is None:
         workspace = torch.empty(max(decode_workspace_size(B, Hq, dv, max(1, min(n, Nk_max))), 256),
                                 dtype=torch.uint8, device=dev)

@@ -430,30 +430,36 @@ cudaError_t merge_rows(const float* o_part, const float* lse_part, int rows, int
     return fa::launch_merge(m, o_dtype, st);
 }
 
-// Groups of 1, 2 or 4 query heads per key/value head run on the CUDA-core split kernel (the
-// packed rows' dot products are cheap there and it keeps more loads in flight); every other
-// group size up to 128 runs on the tensor-core split kernel.  Measured on GB300 with 32 query
-// heads, d = 128 and 1-32K cached tokens: 4 heads per group 4.2 TB/s on CUDA cores vs 3.9 on
-// the tensor core, 8 heads per group 1.2 vs 3.5 TB/s.
-bool gqa_on_cuda_cores(int R) { return R == 1 || R == 2 || R == 4; }
+// Groups of 1 or 2 query heads per key/value head run on the CUDA-core split kernel (the packed
+// rows' dot products are cheap there and it keeps more loads in flight), and so do groups of 4
+// at d != 128; every other group size up to 128 runs on the tensor core.  Measured on GB300 with
+// 32 query heads, d = 128 and 1-32K cached tokens: 4 heads per group 5.1 TB/s on CUDA cores
+// against 6.4-6.7 on the transposed tensor-core kernel; 2 heads 7.0 TB/s on CUDA cores.
+bool gqa_on_cuda_cores(int R, int d) { return R == 1 || R == 2 || (R == 4 && d != 128); }
 
-// Tensor-core groups: one CTA per (b, key/value head, split); groups of 5 to 8 heads at d = 128
-// run two CTAs per SM, the others one.  A CTA's time goes to the per-tile softmax chain more than
-// to the bytes, and the lengths vary (many of the later splits are short or empty), so the count
-// aims at about 1.7 CTAs per CTA slot; splits longer than 32 key tiles are cut down further, so
-// that many groups still spread evenly over the slots.  Measured on GB300, d = 128, 1-32K cached
-// tokens, 32 or 64 query heads over 1-8 key/value heads, 4-64 sequences: within 3 % of the best
-// count swept for 8-, 16- and 32-head groups; 8-head groups of 64 sequences x 4 key/value heads
-// with 2 splits of 32K keys 6.2 TB/s, with 8 splits 6.8.
+// d = 128 with 3-32 query heads per group: the transposed kernel (keys on the TMEM lanes, the
+// group's heads on 16 or 32 columns); otherwise the heads are rows of a 128-row tile
+bool gqa_transposed(int R, int d) { return d == 128 && R >= 3 && R <= 32; }
+
+// Tensor-core groups: one CTA per (b, key/value head, split); the transposed kernel runs two CTAs
+// per SM for 3 to 8 heads, the others one.  A CTA's time goes to the per-tile softmax chain more
+// than to the bytes, and the lengths vary (many of the later splits are short or empty), so the
+// count aims at about 1.7 CTAs per CTA slot; splits longer than T key tiles are cut down further,
+// so that many groups still spread evenly over the slots: T = 32 for more than 4 heads, 64 for up
+// to 4 (their tiles are cheaper, so a CTA's fixed cost weighs more).  Measured on GB300, d = 128,
+// 1-32K cached tokens, 24-64 query heads over 1-8 key/value heads, 4-64 sequences: within 3 %
+// of the best count swept for 3-, 4-, 8-, 16- and 32-head groups; 8-head groups of 64 sequences x
+// 4 key/value heads with 2 splits of 32K keys 6.2 TB/s, with 8 splits 6.8.
 // At least two splits while the groups alone leave SMs idle; each split at least one 128-key tile.
-int gqa_tc_default_splits(int B, int R, int Hkv, int Nk_max, int sms)
+int gqa_tc_default_splits(int B, int R, int Hkv, int Nk_max, int d, int sms)
 {
     const long long groups = static_cast<long long>(B) * Hkv;
-    const long long slots = static_cast<long long>(sms) * (R >= 5 && R <= 8 ? 2 : 1);
+    const long long slots = static_cast<long long>(sms) * (gqa_transposed(R, d) && R <= 8 ? 2 : 1);
     long long n = 17LL * slots / (10LL * groups);
     if (n < 2 && groups < 2LL * sms) n = 2;
     const long long max_n = (static_cast<long long>(Nk_max) + fa::kBlockN - 1) / fa::kBlockN;
-    const long long min_n = (max_n + 31) / 32;
+    const long long tiles_per_split = R <= 4 ? 64 : 32;
+    const long long min_n = (max_n + tiles_per_split - 1) / tiles_per_split;
     if (n < min_n) n = min_n;
     if (n > max_n) n = max_n;
     if (n < 1) n = 1;
@@ -476,14 +482,14 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
         return FA_ERR_INVALID_ARG;
     if (static_cast<long long>(B) * Hq > 0x7fffffffLL || B > 65535 || Hkv > 65535) return FA_ERR_INVALID_ARG;
     const int R = Hq / Hkv;
-    const bool tc = !gqa_on_cuda_cores(R);
+    const bool tc = !gqa_on_cuda_cores(R, d);
     if (!head_ok(d) || dv != d || R > fa::kBlockM) return FA_ERR_UNSUPPORTED;
 
     int n = n_splits;
     if (n == 0) {
         int sms = 0;
         if (sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
-        n = fa_decode_gqa_default_splits(B, Hq, Hkv, Nk_max, sms);
+        n = fa_decode_gqa_default_splits(B, Hq, Hkv, Nk_max, d, sms);
     }
     if (n > Nk_max) n = Nk_max;
     const size_t part_bytes = fa_decode_workspace_size(B, Hq, dv, n);
@@ -499,9 +505,7 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
         if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
         fa::SplitParams sp;
         const long long groups = static_cast<long long>(B) * Hkv;
-        // d = 128 with 5-32 query heads per group: the transposed kernel (keys on the TMEM lanes,
-        // the group's heads on 16 or 32 columns); otherwise the heads are rows of a 128-row tile
-        const bool transposed = d == 128 && R >= 5 && R <= 32;
+        const bool transposed = gqa_transposed(R, d);
         const int q_box = transposed ? (R <= 16 ? 16 : 32) : fa::kBlockM;
         if (!transposed && groups > 65535) return FA_ERR_UNSUPPORTED;  // grid z
         if (!make_map(&sp.tm_q, q, static_cast<int>(groups), R, d, q_box) ||
@@ -565,13 +569,13 @@ fa_status decode_impl(const void* q, const void* k_cache, const void* v_cache, c
 
 extern "C" {
 
-int fa_decode_gqa_default_splits(int B, int Hq, int Hkv, int Nk_max, int num_sms)
+int fa_decode_gqa_default_splits(int B, int Hq, int Hkv, int Nk_max, int d, int num_sms)
 {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nk_max <= 0 || num_sms <= 0 || Hq % Hkv != 0) return 0;
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nk_max <= 0 || d <= 0 || num_sms <= 0 || Hq % Hkv != 0) return 0;
     // On CUDA cores a CTA's arithmetic grows with the R heads it carries, so the count follows the
     // B * Hq query heads (R = 4: 4.3 -> 4.8 TB/s against counting B * Hkv items).
-    return gqa_on_cuda_cores(Hq / Hkv) ? fa_decode_default_splits(B, Hq, Nk_max, num_sms)
-                                       : gqa_tc_default_splits(B, Hq / Hkv, Hkv, Nk_max, num_sms);
+    return gqa_on_cuda_cores(Hq / Hkv, d) ? fa_decode_default_splits(B, Hq, Nk_max, num_sms)
+                                          : gqa_tc_default_splits(B, Hq / Hkv, Hkv, Nk_max, d, num_sms);
 }
 
 fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_cache, const int* seqlens_k, void* o,

@@ -175,15 +175,16 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
 
 /*
  * Split count fa_decode_splitkv_gqa uses when asked for n_splits = 0, for Hq query heads over Hkv
- * key/value heads on a device with `num_sms` multiprocessors.  Groups of R = Hq / Hkv = 1, 2 or
- * 4 heads (CUDA cores) take fa_decode_default_splits(B, Hq, Nk_max, num_sms).  Other groups
- * (tensor core) take floor(1.7 * c * num_sms / (B * Hkv)) splits, where c = 2 for R = 5 to 8
- * (two CTAs per multiprocessor) and 1 otherwise; raised to 2 while B * Hkv < 2 * num_sms, then
- * to ceil(ceil(Nk_max / 128) / 32) (no split longer than 32 key tiles), then clamped to
- * [1, ceil(Nk_max / 128)].  Pure host function.  Returns 0 on invalid arguments (a non-positive
- * size, or Hkv not dividing Hq).
+ * key/value heads of head size d on a device with `num_sms` multiprocessors.  Groups of
+ * R = Hq / Hkv = 1 or 2 heads, and of 4 heads at d != 128, run on CUDA cores and take
+ * fa_decode_default_splits(B, Hq, Nk_max, num_sms).  Other groups (tensor core) take
+ * floor(1.7 * c * num_sms / (B * Hkv)) splits, where c = 2 for 3 to 8 heads at d = 128 (two CTAs
+ * per multiprocessor) and 1 otherwise; raised to 2 while B * Hkv < 2 * num_sms, then to
+ * ceil(ceil(Nk_max / 128) / T) with T = 64 key tiles for R <= 4 and 32 otherwise (no split
+ * longer than T tiles), then clamped to [1, ceil(Nk_max / 128)].  Pure host function.  Returns 0
+ * on invalid arguments (a non-positive size, or Hkv not dividing Hq).
  */
-int fa_decode_gqa_default_splits(int B, int Hq, int Hkv, int Nk_max, int num_sms);
+int fa_decode_gqa_default_splits(int B, int Hq, int Hkv, int Nk_max, int d, int num_sms);
 
 /*
  * Split-KV decode with grouped key/value heads (GQA): Hq query heads share Hkv key/value heads,
@@ -199,13 +200,15 @@ int fa_decode_gqa_default_splits(int B, int Hq, int Hkv, int Nk_max, int num_sms
  *   o          o_dtype [B, Hq, 1, dv]      (device, written)
  *   lse        fp32 [B, Hq, 1]             (device, written; may be NULL)
  *   workspace  ws_bytes >= fa_decode_workspace_size(B, Hq, dv, n) bytes, where n is n_splits or,
- *              for n_splits = 0, fa_decode_gqa_default_splits(B, Hq, Hkv, Nk_max, <SMs of the
+ *              for n_splits = 0, fa_decode_gqa_default_splits(B, Hq, Hkv, Nk_max, d, <SMs of the
  *              device>).
  *   Hkv >= 1 dividing Hq, R = Hq / Hkv <= 128 (larger groups return FA_ERR_UNSUPPORTED).
- *   Hkv = Hq is fa_decode_splitkv.  Groups of 1, 2 or 4 heads run on CUDA cores; other group
- *   sizes on the tensor core, where the R query rows are the rows of a 128-row tile, splits are
- *   whole 128-key tiles (the chunk is rounded up to a multiple of 128 instead of the key block),
- *   and cache rows past a sequence's length are never used, whatever they hold.
+ *   Hkv = Hq is fa_decode_splitkv.  Groups of 1 or 2 heads, and of 4 heads at d != 128, run on
+ *   CUDA cores; other group sizes on the tensor core (3 to 32 heads at d = 128 with the product
+ *   transposed, keys on the tensor-memory lanes; otherwise the R query rows are the rows of a
+ *   128-row tile), where splits are whole 128-key tiles (the chunk is rounded up to a multiple of
+ *   128 instead of the key block) and cache rows past a sequence's length are never used,
+ *   whatever they hold.
  */
 fa_status fa_decode_splitkv_gqa(const void* q, const void* k_cache, const void* v_cache,
                                 const int* seqlens_k, void* o, float* lse, void* workspace,

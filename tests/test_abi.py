@@ -135,19 +135,26 @@ def test_workspace_and_split_heuristic(lib):
 
 def test_gqa_split_heuristic(lib):
     g, ds = lib.fa_decode_gqa_default_splits, lib.fa_decode_default_splits
-    assert g(0, 32, 8, 1024, 152) == 0 and g(1, 6, 4, 1024, 152) == 0 and g(1, 8, 8, 1024, 0) == 0
-    # groups of 1, 2 and 4 heads (CUDA cores) follow the B * Hq query heads
-    for (B, Hq, Hkv) in ((16, 32, 8), (16, 32, 16), (16, 32, 32), (3, 8, 2)):
-        assert g(B, Hq, Hkv, 32768, 152) == ds(B, Hq, 32768, 152)
-    # other groups (tensor core): floor(1.7 * slots / (B * Hkv)) with two CTA slots per SM for 5-8
-    # heads, one otherwise; at least 2 while the groups leave SMs idle; no split longer than 32
-    # key tiles; clamped to [1, ceil(Nk_max / 128)]
-    assert g(16, 32, 4, 32768, 152) == 8 and g(16, 32, 2, 32768, 152) == 8 and g(16, 32, 1, 32768, 152) == 16
-    assert g(4, 32, 4, 32768, 152) == 32 and g(4, 40, 8, 32768, 152) == 16  # 5 heads: two slots per SM
-    assert g(64, 32, 4, 4096, 152) == 2 and g(1000, 32, 4, 4096, 152) == 1
-    assert g(64, 32, 4, 32768, 152) == 8 and g(1000, 32, 4, 32768, 152) == 8  # 32 tiles per split at most
-    assert g(4, 32, 1, 256, 152) == 2 and g(1, 128, 1, 100, 152) == 1
-    assert g(1, 24, 8, 1 << 20, 152) == 256  # 3 heads: 32 by the slots, 8192 tiles / 32 by length
+    assert g(0, 32, 8, 1024, 128, 152) == 0 and g(1, 6, 4, 1024, 128, 152) == 0
+    assert g(1, 8, 8, 1024, 128, 0) == 0 and g(1, 8, 8, 1024, 0, 152) == 0
+    # groups of 1 and 2 heads, and of 4 at d != 128 (CUDA cores), follow the B * Hq query heads
+    for (B, Hq, Hkv, d) in ((16, 32, 32, 128), (16, 32, 16, 128), (16, 32, 8, 64), (3, 8, 2, 32)):
+        assert g(B, Hq, Hkv, 32768, d, 152) == ds(B, Hq, 32768, 152)
+    # other groups (tensor core): floor(1.7 * slots / (B * Hkv)) with two CTA slots per SM for 3-8
+    # heads at d = 128 (the transposed kernel), one otherwise; at least 2 while the groups leave
+    # SMs idle; no split longer than 64 key tiles (up to 4 heads) or 32 (more); clamped to
+    # [1, ceil(Nk_max / 128)]
+    assert g(16, 32, 4, 32768, 128, 152) == 8 and g(16, 32, 2, 32768, 128, 152) == 8
+    assert g(16, 32, 1, 32768, 128, 152) == 16
+    assert g(16, 32, 8, 32768, 128, 152) == 4  # 4 heads at d = 128: 608 / 128 slots per group
+    assert g(16, 24, 8, 32768, 128, 152) == 4 and g(4, 32, 8, 32768, 128, 152) == 16
+    assert g(64, 32, 8, 32768, 128, 152) == 4  # 256 tiles / 64 per split
+    assert g(4, 32, 4, 32768, 128, 152) == 32 and g(4, 40, 8, 32768, 128, 152) == 16  # 8 and 5 heads
+    assert g(4, 32, 4, 32768, 64, 152) == 16  # 8 heads at d = 64: row tiles, one slot per SM
+    assert g(64, 32, 4, 4096, 128, 152) == 2 and g(1000, 32, 4, 4096, 128, 152) == 1
+    assert g(64, 32, 4, 32768, 128, 152) == 8 and g(1000, 32, 4, 32768, 128, 152) == 8  # 32 tiles per split
+    assert g(4, 32, 1, 256, 128, 152) == 2 and g(1, 128, 1, 100, 128, 152) == 1
+    assert g(1, 24, 8, 1 << 20, 64, 152) == 128  # 3 heads at d = 64: 32 by the slots, 8192 tiles / 64
 
 
 def test_status_strings(lib):

@@ -166,7 +166,7 @@ def test_gqa_decode(d, R, n_splits):
         assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16), what=f"gqa d={d} R={R} n={n_splits}")
 
 
-@pytest.mark.parametrize("R", [8, 40], ids=["R8_transposed", "R40_row_tile"])
+@pytest.mark.parametrize("R", [3, 8, 40], ids=["R3_transposed", "R8_transposed", "R40_row_tile"])
 def test_gqa_zero_and_clamped_lengths(R):
     """Grouped decode on the tensor core (d = 128) with a zero-length sequence, lengths just past a
     128-key tile and an out-of-range length: the last is clamped to the cache and reported, a sequence
@@ -184,7 +184,7 @@ def test_gqa_zero_and_clamped_lengths(R):
     assert_close(o[1:], lse[1:], o_ref, lse_ref, what=f"gqa lengths R={R}")
 
 
-@pytest.mark.parametrize("Hkv", [8, 4], ids=["R4_cuda_cores", "R8_tensor_core"])
+@pytest.mark.parametrize("Hkv", [8, 4], ids=["R4_tensor_core", "R8_tensor_core"])
 def test_gqa_full_size_sampled(Hkv):
     """The benchmark's GQA workloads (B=16, Hq=32 over Hkv=8 or 4, d=128, lengths U[1024, 32768]) in
     their launch configuration, with fp32 O and with the benchmark's bf16 O; 24 seeded query heads

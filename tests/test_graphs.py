@@ -111,13 +111,13 @@ def test_decode_graphs():
     assert int(wsf[fa().decode_workspace_size(B, H, d, n):].count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("Hkv", [8, 4, 1])  # groups of 4 (CUDA cores), 8 and 32 (tensor core)
+@pytest.mark.parametrize("Hkv", [16, 8, 4, 1])  # groups of 2 (CUDA cores), 4, 8 and 32 (tensor core)
 def test_gqa_decode_graph(Hkv):
     B, Hq, Nk_max, d = 2, 32, 1500, 128
     lens = torch.tensor([1500, 129], dtype=torch.int32)
     q, k, v, _ = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=Hkv, device=DEV, seqlens=lens)
     ld = lens.to(DEV)
-    n = fa().decode_gqa_default_splits(B, Hq, Hkv, Nk_max, fa().num_sms())
+    n = fa().decode_gqa_default_splits(B, Hq, Hkv, Nk_max, d, fa().num_sms())
     ws = torch.empty(fa().decode_workspace_size(B, Hq, d, n), dtype=torch.uint8, device=DEV)
     o = torch.empty((B, Hq, 1, d), dtype=torch.bfloat16, device=DEV)
     lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=DEV)
