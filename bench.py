@@ -775,6 +775,15 @@ def _case_call(fa, dev, name):
         lse = torch.empty((B, Hq, 1), dtype=torch.float32, device=dev)
         return (lambda: fa.decode_splitkv_gqa(q, k, v, lens_d, n_splits=n, out=o, lse=lse, workspace=ws),
                 f"GQA decode B={B} Hq={Hq} Hkv={Hkv} d={d}")
+    if name == "splitkv-prefill":
+        B, H, N, Nk, d = (SPLIT_PREFILL[x] for x in ("B", "H", "N", "Nk", "d"))
+        q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=0, device=dev)
+        o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        n = fa.fwd_splitkv_default_splits(B, H, N, Nk, fa.num_sms(dev))
+        ws = torch.empty(fa.fwd_splitkv_workspace_size(B, H, N, d, n), dtype=torch.uint8, device=dev)
+        return (lambda: fa.fwd_splitkv(q, k, v, causal=True, n_splits=n, out=o, lse=lse, workspace=ws),
+                f"causal split-KV prefill B={B} H={H} N={N} Nk={Nk} d={d}")
     if name == "decode":
         B, H, Nk_max, d = DEC["B"], DEC["H"], DEC["Nk_max"], DEC["d"]
         q, k, v, lens = decode_inputs(B, H, Nk_max, d, d, seed=0, lo=DEC["lo"], hi=DEC["hi"], device=dev)
@@ -805,7 +814,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="run one workload alone (fwd-c1, fwd-c1-causal, fwd-c2, fwd-c2-causal, fwd-c3a, "
-                         "fwd-c3a-causal, fwd-c3b, fwd-c3b-causal, fwd-c4, decode, gqa4, gqa8) for profiling")
+                         "fwd-c3a-causal, fwd-c3b, fwd-c3b-causal, fwd-c4, decode, gqa4, gqa8, splitkv-prefill) for profiling")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)

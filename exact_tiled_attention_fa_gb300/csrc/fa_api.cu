@@ -23,6 +23,19 @@ cudaError_t launch_fwd(const FwdParams& p, int d, bool causal, fa_dtype o_dtype,
     default: return cudaErrorInvalidValue;
     }
 }
+cudaError_t launch_fwd_split_32(const FwdParams& p, bool causal, cudaStream_t st);
+cudaError_t launch_fwd_split_64(const FwdParams& p, bool causal, cudaStream_t st);
+cudaError_t launch_fwd_split_128(const FwdParams& p, bool causal, cudaStream_t st);
+
+cudaError_t launch_fwd_split(const FwdParams& p, int d, bool causal, cudaStream_t st)
+{
+    switch (d) {
+    case 32: return launch_fwd_split_32(p, causal, st);
+    case 64: return launch_fwd_split_64(p, causal, st);
+    case 128: return launch_fwd_split_128(p, causal, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
 cudaError_t launch_splitkv_32(const SplitParams& p, bool causal, bool varlen, cudaStream_t st);
 cudaError_t launch_splitkv_64(const SplitParams& p, bool causal, bool varlen, cudaStream_t st);
 cudaError_t launch_splitkv_128(const SplitParams& p, bool causal, bool varlen, cudaStream_t st);
@@ -272,7 +285,8 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
     if (BH * n_qp > 0x3fffffffLL) return FA_ERR_INVALID_ARG;
     if (!head_ok(d) || dv != d) return FA_ERR_UNSUPPORTED;
 
-    fa::FwdParams p;
+    fa::FwdParams p{};
+    p.n_splits = 1;
     if (!make_map(&p.tm_q, q, static_cast<int>(BH), N, d) || !make_map(&p.tm_k, k, static_cast<int>(BH), Nk, d) ||
         !make_map(&p.tm_v, v, static_cast<int>(BH), Nk, dv) ||
         !make_out_map(&p.tm_o, o, static_cast<int>(BH), N, dv, o_dtype, 32))
@@ -589,15 +603,14 @@ fa_status fa_decode_splitkv(const void* q, const void* k_cache, const void* v_ca
 int fa_fwd_splitkv_default_splits(int B, int H, int N, int Nk, int num_sms)
 {
     if (B <= 0 || H <= 0 || N <= 0 || Nk <= 0 || num_sms <= 0) return 0;
-    // The split kernel holds an SM per CTA, and a CTA costs about six key tiles beyond its own
-    // (set-up, pipeline fill, partial write, its share of the merge), so a second wave of shorter
-    // splits loses to one wave of longer ones: the count is the largest for which every (head,
-    // query tile, split) CTA runs at once, each split at least one 128-key tile.  Measured on
-    // GB300 over five shapes (d = 64 and 128, causal and not, 4-64 query tiles), this was the best
-    // count swept in each (B=1 H=8 N=512 Nk=32K d=128 causal: 4 splits 557 TFLOP/s, 10 splits 462).
-    const long long tiles = static_cast<long long>(B) * H * ((N + fa::kBlockM - 1) / fa::kBlockM);
+    // A split item is (head, pair of 128-row query tiles, split) on the persistent forward kernel,
+    // one CTA per SM, and an item costs a few key tiles beyond its own (Q load, pipeline fill,
+    // partial write, its share of the merge), so a second round of shorter items loses to one
+    // round of longer ones: the count is the largest for which every item runs at once, each
+    // split at least one 128-key tile.
+    const long long pairs = static_cast<long long>(B) * H * ((N + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM));
     const long long max_n = (static_cast<long long>(Nk) + fa::kBlockN - 1) / fa::kBlockN;
-    long long n = num_sms / tiles;
+    long long n = num_sms / pairs;
     if (n > max_n) n = max_n;
     if (n < 1) n = 1;
     return static_cast<int>(n);
@@ -621,47 +634,51 @@ fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, f
         !aligned(workspace, kAlign))
         return FA_ERR_INVALID_ARG;
     const long long BH = static_cast<long long>(B) * H;
-    const long long Tr = (static_cast<long long>(N) + fa::kBlockM - 1) / fa::kBlockM;
-    if (BH > 65535 || Tr > 65535 || BH * N > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+    const long long n_qp = (static_cast<long long>(N) + 2 * fa::kBlockM - 1) / (2 * fa::kBlockM);
+    if (BH * N > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
     if (!head_ok(d) || dv != d) return FA_ERR_UNSUPPORTED;
+    int sms = 0;
     int n = n_splits;
     if (n == 0) {
-        int sms = 0;
         if (sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
         n = fa_fwd_splitkv_default_splits(B, H, N, Nk, sms);
     }
     if (n > Nk) n = Nk;
     if (ws_bytes < fa_fwd_splitkv_workspace_size(B, H, N, dv, n)) return FA_ERR_WORKSPACE;
-    long long chunk = (static_cast<long long>(Nk) + n - 1) / n;
-    chunk = (chunk + fa::kBlockN - 1) / fa::kBlockN * fa::kBlockN;
-    const int n_eff = static_cast<int>((Nk + chunk - 1) / chunk);
-    if (n_eff > 65535) return FA_ERR_INVALID_ARG;
+    if (sms == 0 && sm_count(&sms) != cudaSuccess) return FA_ERR_CUDA;
+    // whole 128-key tiles per split; trailing splits past the keys are dropped
+    const long long key_tiles = (static_cast<long long>(Nk) + fa::kBlockN - 1) / fa::kBlockN;
+    const long long split_tiles = (key_tiles + n - 1) / n;
+    const long long n_eff = (key_tiles + split_tiles - 1) / split_tiles;
+    // the kernels index items with 32-bit ints and step past the last one by up to the grid size
+    if (BH * n_qp * n_eff > 0x3fffffffLL) return FA_ERR_INVALID_ARG;
 
     int* status = nullptr;
     if (status_word(&status) != cudaSuccess) return FA_ERR_CUDA;
-    fa::SplitParams sp;
-    if (!make_map(&sp.tm_q, q, static_cast<int>(BH), N, d) || !make_map(&sp.tm_k, k, static_cast<int>(BH), Nk, d) ||
-        !make_map(&sp.tm_v, v, static_cast<int>(BH), Nk, dv))
+    fa::FwdParams p{};
+    if (!make_map(&p.tm_q, q, static_cast<int>(BH), N, d) || !make_map(&p.tm_k, k, static_cast<int>(BH), Nk, d) ||
+        !make_map(&p.tm_v, v, static_cast<int>(BH), Nk, dv))
         return FA_ERR_CUDA;
-    const size_t slots = static_cast<size_t>(BH) * N * n_eff;
-    sp.o_part = static_cast<float*>(workspace);
-    sp.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(slots * dv * sizeof(float), kAlign));
-    sp.seqlens = nullptr;
-    sp.status = status;
-    sp.n_groups = static_cast<int>(BH);
-    sp.rows_per_group = N;
-    sp.n_qtiles = static_cast<int>(Tr);
-    sp.groups_per_batch = 1;
-    sp.Nk = Nk;
-    sp.n_splits = n_eff;
-    sp.chunk = static_cast<int>(chunk);
-    sp.causal_off = Nk - N;
-    sp.scale_log2 = scale * 1.4426950408889634f;
-    sp.wait_limit_ns = g_wait_ns.load();
+    const size_t slots = static_cast<size_t>(BH) * N * static_cast<size_t>(n_eff);
+    p.o_part = static_cast<float*>(workspace);
+    p.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + round_up(slots * dv * sizeof(float), kAlign));
+    p.o = nullptr;
+    p.lse = nullptr;
+    p.status = status;
+    p.BH = static_cast<int>(BH);
+    p.N = N;
+    p.Nk = Nk;
+    p.n_splits = static_cast<int>(n_eff);
+    p.split_tiles = static_cast<int>(split_tiles);
+    p.n_qp = static_cast<int>(n_qp * n_eff);  // (query pair, split) items per head
+    p.n_items = static_cast<int>(BH * n_qp * n_eff);
+    p.num_ctas = sms;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.wait_limit_ns = g_wait_ns.load();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (fa::launch_splitkv(sp, d, causal != 0, false, st) != cudaSuccess) return FA_ERR_CUDA;
-    return merge_rows(sp.o_part, sp.lse_part, static_cast<int>(BH * N), n_eff, dv, o, lse, status, o_dtype, st) ==
-                   cudaSuccess
+    if (fa::launch_fwd_split(p, d, causal != 0, st) != cudaSuccess) return FA_ERR_CUDA;
+    return merge_rows(p.o_part, p.lse_part, static_cast<int>(BH * N), static_cast<int>(n_eff), dv, o, lse, status,
+                      o_dtype, st) == cudaSuccess
                ? FA_OK
                : FA_ERR_CUDA;
 }

@@ -54,6 +54,13 @@
 // then reaches 2e-2, above the 1e-2 the results must meet.)  A warp rescales its O
 // rows only when the max of one of its rows grew.
 //
+// Split mode (SPLIT = true, fa_fwd_splitkv; "flash_lab.py" section 4 `split_kv_decode` applied
+// to query tiles): for few query tiles over many keys the keys are also cut into ranges of whole
+// key tiles; an item is (head, query pair, split), its walk covers the split's key tiles (masked
+// as usual by their absolute positions), and its epilogue writes each row's normalised fp32
+// partial O and natural-log LSE to the split's slot (O = 0, LSE = -inf for a row that sees no key
+// of the split); a merge kernel combines the slots.
+//
 // Every barrier wait is bounded (FwdParams::wait_limit_ns).  A role whose wait runs
 // out records FA_ERR_TIMEOUT and raises the CTA's abort flag so the other roles stop
 // too; each role then drains what it has in flight (TMA copies, tensor-core
@@ -216,6 +223,7 @@ __device__ __forceinline__ void stage_row(uint32_t stg, int r, const uint32_t (&
 // issuer i) takes rows [r0[i], r0[i] + 128).
 struct Item {
     int bh, i0;
+    int split, j0;  // split mode: the item's key range starts at key tile j0 (0 otherwise)
     int r0[2];    // first query row of slot 0 / 1
     int rows[2];  // valid query rows of slot 0 / 1 (0 when the tile lies past N)
     int n[2];     // key/value tiles each query tile visits
@@ -296,6 +304,7 @@ __device__ __forceinline__ void next_item(const FwdParams& p, ItemCursor& c, boo
     c.k += 1;
 }
 
+template <bool SPLIT = false>
 __device__ __forceinline__ Item decode_item(const FwdParams& p, const ItemCursor& c, bool causal, bool alternate,
                                             bool ordered = false)
 {
@@ -303,8 +312,17 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, const ItemCursor
     Item it;
     it.bh = c.bh;
     const int t = c.t;
-    // heavy, light, heavy, light, ...; in the ordered walk (no mask, one-tile last pairs) t is the pair
-    const int qp = ordered ? t : (t & 1) ? (t >> 1) : p.n_qp - 1 - (t >> 1);
+    int qp;
+    it.split = 0;
+    it.j0 = 0;
+    if constexpr (SPLIT) {  // t = query pair * n_splits + split
+        qp = t / p.n_splits;
+        it.split = t - qp * p.n_splits;
+        it.j0 = it.split * p.split_tiles;
+    } else {
+        // heavy, light, heavy, light, ...; in the ordered walk (no mask, one-tile last pairs) t is the pair
+        qp = ordered ? t : (t & 1) ? (t >> 1) : p.n_qp - 1 - (t >> 1);
+    }
     it.i0 = qp * 2 * kBlockM;
     const int n_all = (p.Nk + kBlockN - 1) / kBlockN;
     const int off = p.Nk - p.N;
@@ -324,6 +342,7 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, const ItemCursor
             const int last_pos = off + r0 + it.rows[i] - 1;  // position of the tile's last query row
             n = last_pos < 0 ? 0 : min(n_all, last_pos / kBlockN + 1);
         }
+        if constexpr (SPLIT) n = max(0, min(n, it.j0 + p.split_tiles) - it.j0);  // tiles j0 .. j0 + n - 1
         it.n[i] = n;
     }
     it.n_kv = max(it.n[0], it.n[1]);
@@ -336,7 +355,7 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, const ItemCursor
 // written the rows' 1 / l (LFull), it reads O_i 32 columns at a time and stores the rows of
 // O / l; then it releases the columns (OFree: the next item's first P V may overwrite them and
 // the softmax may write the next 1 / l).
-template <int D, bool CAUSAL, typename OutT>
+template <int D, bool CAUSAL, typename OutT, bool SPLIT>
 __device__ __forceinline__ void fwd_correction(const FwdParams& p, const uint8_t* smem, uint32_t bar0, uint32_t tmem,
                                                volatile int* abort_flag)
 {
@@ -351,7 +370,7 @@ __device__ __forceinline__ void fwd_correction(const FwdParams& p, const uint8_t
     int done[2] = {0, 0};  // items whose O_i this warpgroup has read, per query tile
     bool ok = true;
     for (ItemCursor cur = first_item(p, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp)) {
-        const Item it = decode_item(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
+        const Item it = decode_item<SPLIT>(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
             const int rows = it.rows[i];
@@ -365,7 +384,9 @@ __device__ __forceinline__ void fwd_correction(const FwdParams& p, const uint8_t
             }
             const float inv = n > 0 ? inv_l[i * kBlockM + r] : 0.f;
             const bool valid = r < rows;
-            OutT* orow = reinterpret_cast<OutT*>(p.o) + (static_cast<size_t>(it.bh) * p.N + static_cast<size_t>(it.r0[i] + r)) * D;
+            const size_t row = static_cast<size_t>(it.bh) * p.N + static_cast<size_t>(it.r0[i] + r);
+            OutT* orow = SPLIT ? reinterpret_cast<OutT*>(p.o_part) + (row * p.n_splits + it.split) * D
+                               : reinterpret_cast<OutT*>(p.o) + row * D;
             const uint32_t t_o = tmem + lane_base + C::col_o(i);
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -392,10 +413,11 @@ __device__ __forceinline__ void fwd_correction(const FwdParams& p, const uint8_t
     if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
 }
 
-template <int D, bool CAUSAL, typename OutT>
+template <int D, bool CAUSAL, typename OutT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __grid_constant__ FwdParams p)
 {
     using C = FwdCfg<D, static_cast<int>(sizeof(OutT))>;
+    static_assert(!SPLIT || sizeof(OutT) == 4, "split partials are fp32");
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -446,7 +468,7 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
         if constexpr (kWithCorr) {
             regs_decrease<kCorrRegs>();
             // ============================================================ correction / epilogue
-            fwd_correction<D, CAUSAL, OutT>(p, smem, bar0, tmem, abort_flag);
+            fwd_correction<D, CAUSAL, OutT, SPLIT>(p, smem, bar0, tmem, abort_flag);
         }
     } else if (warp >= kWarpProducer) {
       regs_decrease<kWithCorr ? kCorrControlRegs : kControlRegs<D>>();
@@ -456,14 +478,14 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
             prefetch_tensormap(&p.tm_q);
             prefetch_tensormap(&p.tm_k);
             prefetch_tensormap(&p.tm_v);
-            if (C::kStoreO) prefetch_tensormap(&p.tm_o);
+            if (C::kStoreO && !SPLIT) prefetch_tensormap(&p.tm_o);
             const uint64_t pol_q = policy_evict_first();
             const uint64_t pol_kv = policy_evict_last();
             int q_loads[2] = {0, 0};  // loads issued into each Q buffer
             long long g = 0;          // K/V tiles issued so far (ring position)
             bool ok = true;
             for (ItemCursor cur = first_item(p, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp)) {
-                const Item it = decode_item(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
+                const Item it = decode_item<SPLIT>(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
                 for (int i = 0; i < 2 && ok; ++i) {
                     if (it.n[i] == 0) continue;
                     const int b = q_loads[i] % C::kQBuf;  // buffer of this load
@@ -491,11 +513,11 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
 #pragma unroll
                     for (int cb = 0; cb < C::kNumCB; ++cb)
                         tma_load_3d(sbase + C::kOffK + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_k,
-                                    bar(kBarKVFull + s), cb * C::kCB, j * kBlockN, it.bh, pol_kv);
+                                    bar(kBarKVFull + s), cb * C::kCB, (it.j0 + j) * kBlockN, it.bh, pol_kv);
 #pragma unroll
                     for (int cb = 0; cb < C::kNumCB; ++cb)
                         tma_load_3d(sbase + C::kOffV + s * C::kTileBytes + cb * C::kBlkBytes, &p.tm_v,
-                                    bar(kBarKVFull + s), cb * C::kCB, j * kBlockN, it.bh, pol_kv);
+                                    bar(kBarKVFull + s), cb * C::kCB, (it.j0 + j) * kBlockN, it.bh, pol_kv);
                 }
             }
             if (!ok && !*abort_flag) record_failure(p.status, abort_flag, FA_ERR_TIMEOUT);
@@ -561,7 +583,7 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
             };
 
             for (ItemCursor cur = first_item(p, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp)) {
-                const Item it = decode_item(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
+                const Item it = decode_item<SPLIT>(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
                 const int n = i ? it.n[1] : it.n[0];
                 const int q_bar = 2 * (q_uses % C::kQBuf) + i;
                 if (n > 0 && !mbar_wait(bar(kBarQFull + q_bar), (q_uses / C::kQBuf) & 1, limit, abort_flag)) {
@@ -651,7 +673,7 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
         bool ok = true;
 
         for (ItemCursor cur = first_item(p, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp); ok && cur.item < p.n_items; next_item(p, cur, CAUSAL && p.pairs, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp)) {
-            const Item it = decode_item(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
+            const Item it = decode_item<SPLIT>(p, cur, CAUSAL, C::kAlternate, kOrderedWalk<D, CAUSAL> && p.n_full != p.n_qp);
             const int n = wg ? it.n[1] : it.n[0];
             const int rows = wg ? it.rows[1] : it.rows[0];
             const int row0 = wg ? it.r0[1] : it.r0[0];  // first query row of this tile
@@ -676,7 +698,7 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
                 float s[kBlockN];
 #pragma unroll
                 for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(u[c]);
-                const int k0 = j * kBlockN;
+                const int k0 = (it.j0 + j) * kBlockN;
                 const bool need_mask = (k0 + kBlockN > p.Nk) || (CAUSAL && k0 + kBlockN - 1 > off + row0);
                 if (need_mask) {  // diagonal or ragged tile: mask, then take the max in registers
                     const int last = CAUSAL ? min(qpos, p.Nk - 1) : p.Nk - 1;  // last visible key
@@ -774,9 +796,14 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
                     mbar_arrive(bar(kBarLFull + wg));
                     ++items;
                 }
-                if (p.lse != nullptr && r < rows)
-                    p.lse[static_cast<size_t>(it.bh) * p.N + static_cast<size_t>(row0 + r)] =
-                        l > 0.f ? (m_run + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+                if (r < rows) {
+                    const size_t row = static_cast<size_t>(it.bh) * p.N + static_cast<size_t>(row0 + r);
+                    const float lse = l > 0.f ? (m_run + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+                    if constexpr (SPLIT)
+                        p.lse_part[row * p.n_splits + it.split] = lse;
+                    else if (p.lse != nullptr)
+                        p.lse[row] = lse;
+                }
                 continue;
             }
             if (n > 0) {
@@ -788,7 +815,7 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const size_t row = static_cast<size_t>(it.bh) * p.N + static_cast<size_t>(row0 + r);
             const bool valid = r < rows;
-            if constexpr (C::kStoreO) {
+            if constexpr (C::kStoreO && !SPLIT) {
                 using OS = OStage<OutT, D>;
                 const uint32_t stg = sbase + C::kOffStage + static_cast<uint32_t>(wg) * C::kStageTileBytes;
                 // Each warp stages its 32 rows and stores them itself (a 32-row box), so the epilogue
@@ -818,7 +845,9 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
                 }
                 ++staged;
             } else {
-                OutT* orow = reinterpret_cast<OutT*>(p.o) + row * D;
+                // split mode: this split's slot of the row's fp32 partials
+                OutT* orow = SPLIT ? reinterpret_cast<OutT*>(p.o_part) + (row * p.n_splits + it.split) * D
+                                   : reinterpret_cast<OutT*>(p.o) + row * D;
 #pragma unroll
                 for (int c = 0; c < D / 32; ++c) {
                     float v[32];
@@ -835,8 +864,13 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
                     if (valid) store_row32<OutT>(orow + 32 * c, v);
                 }
             }
-            if (p.lse != nullptr && valid)
-                p.lse[row] = l > 0.f ? (m_run + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+            if (valid) {
+                const float lse = l > 0.f ? (m_run + lg2_approx(l)) * 0.69314718055994531f : -INFINITY;
+                if constexpr (SPLIT)
+                    p.lse_part[row * p.n_splits + it.split] = lse;
+                else if (p.lse != nullptr)
+                    p.lse[row] = lse;
+            }
         }
         // Bulk stores must finish before the CTA's shared memory goes away.
         if (C::kStoreO && lane == 0 && staged > 0) bulk_wait_all();
@@ -852,11 +886,11 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
     }
 }
 
-template <int D, bool CAUSAL, typename OutT>
+template <int D, bool CAUSAL, typename OutT, bool SPLIT = false>
 cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
 {
     using C = FwdCfg<D, static_cast<int>(sizeof(OutT))>;
-    auto kern = fa_fwd_kernel<D, CAUSAL, OutT>;
+    auto kern = fa_fwd_kernel<D, CAUSAL, OutT, SPLIT>;
     static bool configured[64] = {};  // the shared-memory attribute is set once per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -881,13 +915,13 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
         return cudaErrorLaunchOutOfResources;  // the register split would not fit
     FwdParams q = p;
     // Pairs balance causal work over several rounds; with no more items than CTAs every item gets
-    // a CTA of its own.
-    q.pairs = (CAUSAL && p.n_items > p.num_ctas) ? 1 : 0;
+    // a CTA of its own.  Split items go out singly, in (head, query pair, split) order.
+    q.pairs = (!SPLIT && CAUSAL && p.n_items > p.num_ctas) ? 1 : 0;
     const int units = q.pairs ? (p.n_items + 1) / 2 : p.n_items;  // pairs of items, or items
     const int grid = units < p.num_ctas ? units : p.num_ctas;
     const long long step = q.pairs ? 2LL * grid - 1 : grid;  // see next_item
     const int rem_rows = p.N % (2 * kBlockM);
-    q.n_full = (rem_rows > 0 && rem_rows <= kBlockM) ? p.n_qp - 1 : p.n_qp;
+    q.n_full = (!SPLIT && rem_rows > 0 && rem_rows <= kBlockM) ? p.n_qp - 1 : p.n_qp;
     // pairs per head of the walk: n_full in the ordered walk (no mask, one-tile last pairs), else n_qp
     const int per_head = (kOrderedWalk<D, CAUSAL> && q.n_full != p.n_qp) ? (q.n_full > 0 ? q.n_full : 1) : p.n_qp;
     q.step_heads = static_cast<int>(step / per_head);
@@ -902,6 +936,12 @@ cudaError_t launch_fwd_d(const FwdParams& p, bool causal, fa_dtype o_dtype, cuda
     if (o_dtype == FA_F32)
         return causal ? launch_fwd_t<D, true, float>(p, st) : launch_fwd_t<D, false, float>(p, st);
     return causal ? launch_fwd_t<D, true, __nv_bfloat16>(p, st) : launch_fwd_t<D, false, __nv_bfloat16>(p, st);
+}
+
+template <int D>
+cudaError_t launch_fwd_split_d(const FwdParams& p, bool causal, cudaStream_t st)
+{
+    return causal ? launch_fwd_t<D, true, float, true>(p, st) : launch_fwd_t<D, false, float, true>(p, st);
 }
 
 }  // namespace fa

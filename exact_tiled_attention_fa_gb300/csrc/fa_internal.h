@@ -38,10 +38,19 @@ struct FwdParams {
     // 128 rows).  Items 0 .. BH * n_full - 1 are those pairs, head-major; the BH one-tile last
     // pairs (if any) come after them, so that they fill the last round instead of lengthening it.
     int n_full;
+    // Split mode (fa_fwd_splitkv): the keys are cut into n_splits ranges of split_tiles key
+    // tiles, an item is (head, query pair, split), n_qp counts the (query pair, split) items of a
+    // head (pair-major), and each item writes its rows' normalised partial O (fp32) and natural-log
+    // LSE to o_part [B*H*N][n_splits][dv] and lse_part [B*H*N][n_splits] instead of o / lse.
+    int n_splits, split_tiles;
+    float* o_part;
+    float* lse_part;
 };
 
 // Launch the forward kernel for head size d (= dv), causal flag and output type.
 cudaError_t launch_fwd(const FwdParams& p, int d, bool causal, fa_dtype o_dtype, cudaStream_t st);
+// The same kernel in split mode (fp32 partials; FwdParams::n_splits, split_tiles, o_part, lse_part).
+cudaError_t launch_fwd_split(const FwdParams& p, int d, bool causal, cudaStream_t st);
 
 // Backward.  Work item: one head and one 128-key tile; the CTA walks every query tile
 // that sees a key of it.  Per-row vectors and the dQ accumulator are padded to whole

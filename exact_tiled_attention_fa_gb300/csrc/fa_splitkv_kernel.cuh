@@ -7,13 +7,12 @@
 // kernel in fa_decode.cu).  Within a split the walk over key tiles is the FlashAttention-2
 // loop of section 3 `flash_fwd` (running max m and sum l, O rescaled by exp(m_old - m_new)).
 //
-// Two uses of the same kernel:
-//   * grouped-query decode: the rows of the query tile are the R query heads that share one
-//     key/value head ("flash_lab.py" section 4 packs a group's query heads as the rows of q;
-//     `decode_attention_time` method "fd" pads them to a tensor-core tile), each sequence
-//     with its own cached length;
-//   * prefill with few query tiles: the rows are 128 queries of one head, with the causal
-//     mask (query i at position Nk - N + i), and the splits give the GPU enough CTAs.
+// Used for grouped-query decode: the rows of the query tile are the R query heads that share one
+// key/value head ("flash_lab.py" section 4 packs a group's query heads as the rows of q;
+// `decode_attention_time` method "fd" pads them to a tensor-core tile), each sequence with its
+// own cached length (VARLEN).  The kernel also carries a causal form for a tile of 128 queries
+// of one head (query i at position Nk - N + i), which the prefill with few query tiles used
+// before it moved to the forward kernel's split mode; only the decode form is instantiated.
 //
 // GB300 mapping: one CTA per (split, query tile, group); six warps.
 //   warps 0-3  softmax: thread t owns row t of the tile (TMEM lane t).
@@ -402,8 +401,8 @@ cudaError_t launch_splitkv_t(const SplitParams& p, cudaStream_t st)
 template <int D>
 cudaError_t launch_splitkv_d(const SplitParams& p, bool causal, bool varlen, cudaStream_t st)
 {
-    if (varlen) return causal ? cudaErrorInvalidValue : launch_splitkv_t<D, false, true>(p, st);
-    return causal ? launch_splitkv_t<D, true, false>(p, st) : launch_splitkv_t<D, false, false>(p, st);
+    if (!varlen || causal) return cudaErrorInvalidValue;  // grouped-query decode only
+    return launch_splitkv_t<D, false, true>(p, st);
 }
 
 }  // namespace fa

@@ -240,9 +240,9 @@ fa_status fa_decode_splitkv_fused(const void* q, const void* k_cache, const void
 
 /*
  * Split count fa_fwd_splitkv uses for n_splits = 0 on a device with `num_sms` multiprocessors:
- * the largest count for which the B*H*ceil(N/128) query tiles times the splits fit one CTA per
- * multiprocessor (one wave), at least 1 and at most ceil(Nk/128) (each split at least one
- * 128-key tile).  Pure host function; 0 on invalid arguments.
+ * the largest count for which the B*H*ceil(N/256) pairs of query tiles times the splits fit one
+ * persistent CTA per multiprocessor (one round), at least 1 and at most ceil(Nk/128) (each split
+ * at least one 128-key tile).  Pure host function; 0 on invalid arguments.
  */
 int fa_fwd_splitkv_default_splits(int B, int H, int N, int Nk, int num_sms);
 
@@ -255,16 +255,17 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int dv, int n_splits);
 
 /*
  * Exact attention forward with the keys split ("flash_lab.py" section 4 `split_kv_decode`
- * applied to a query tile): for workloads with few 128-row query
- * tiles (B*H*ceil(N/128) below the number of multiprocessors) the keys are cut into n_splits
- * chunks of whole 128-key tiles; each (head, query tile, chunk) computes its normalised output
- * and log-sum-exp, and a second kernel merges them.  Same arguments, masks, result and output
+ * applied to a query tile): for workloads with few 128-row query tiles (B*H*ceil(N/256) pairs
+ * of them below the number of multiprocessors) the keys are cut into chunks of whole 128-key
+ * tiles (ceil(ceil(Nk/128) / n_splits) tiles each; chunks past the keys are dropped); the
+ * forward kernel computes each (head, query tile pair, chunk)'s normalised output and
+ * log-sum-exp, and a second kernel merges them.  Same arguments, masks, result and output
  * conventions as fa_fwd, plus:
  *   workspace  ws_bytes >= fa_fwd_splitkv_workspace_size(B, H, N, dv, n) bytes, 256-byte aligned,
  *              where n is n_splits or, for 0, fa_fwd_splitkv_default_splits(B, H, N, Nk, <SMs>);
  *   n_splits   >= 0; values above Nk are reduced to it.
- * B*H and ceil(N/128) must each be at most 65535.  Returns FA_ERR_WORKSPACE if ws_bytes is too
- * small (nothing launched).
+ * B*H*N must be below 2^31 and B*H*ceil(N/256)*chunks below 2^30.  Returns FA_ERR_WORKSPACE if
+ * ws_bytes is too small (nothing launched).
  */
 fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
                          void* workspace, size_t ws_bytes, int B, int H, int N, int Nk, int d, int dv,

@@ -103,11 +103,11 @@ def test_fwd_splitkv_rejects_bad_arguments(lib):
     ds = lib.fa_fwd_splitkv_default_splits
     assert ds(1, 1, 1, 100000, 152) >= 2 and ds(64, 16, 1024, 1024, 152) == 1
     assert 1 <= ds(8, 8, 77, 513, 152) <= 5
-    # one wave: the most splits for which query tiles x splits fit one CTA per SM
-    assert ds(1, 8, 512, 32768, 152) == 4 and ds(1, 4, 128, 131072, 152) == 38 and ds(2, 8, 384, 16384, 152) == 3
+    # one round: the most splits for which pairs of query tiles x splits fit one CTA per SM
+    assert ds(1, 8, 512, 32768, 152) == 9 and ds(1, 4, 128, 131072, 152) == 38 and ds(2, 8, 384, 16384, 152) == 4
     for (B, H, N, Nk) in ((1, 8, 512, 32768), (1, 3, 200, 50000), (2, 5, 129, 9000), (1, 1, 64, 1000)):
-        tiles, n = B * H * -(-N // 128), ds(B, H, N, Nk, 152)
-        assert n == min(max(1, 152 // tiles), -(-Nk // 128))
+        pairs, n = B * H * -(-N // 256), ds(B, H, N, Nk, 152)
+        assert n == min(max(1, 152 // pairs), -(-Nk // 128))
 
 
 def test_merge_rejects_bad_arguments(lib):
