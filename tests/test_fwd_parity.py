@@ -182,6 +182,7 @@ SPLIT = [
     (2, 1, 700, 333, 128, 1.0),   # N > Nk: causal rows with no visible key
     (1, 1, 1, 2000, 64, 1.0),
     (1, 3, 256, 4097, 128, 2.0),
+    (4, 16, 300, 2000, 64, 1.0),  # 128 heads x 2 query pairs: several split items per CTA
 ]
 
 
@@ -198,6 +199,19 @@ def test_fwd_splitkv_full_oracle(B, H, N, Nk, d, mult, n_splits, causal):
         assert fa().get_device_error() == 0
         assert_close(o, lse, o_ref, lse_ref, bf16_out=(dt == torch.bfloat16),
                      what=f"splitkv {B,H,N,Nk,d} n={n_splits} causal={causal} {dt}")
+
+
+@pytest.mark.parametrize("B,H,N,Nk,d", [(1, 2, 300, 1000, 64), (2, 1, 700, 333, 128)])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_splitkv_one_key_tile_per_split(B, H, N, Nk, d, causal):
+    """n_splits = 999 (reduced to Nk, then to one 128-key tile per split): the most split items,
+    each with a single key tile (the last one ragged)."""
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=3, device=DEV)
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=causal, scale=1.0 / math.sqrt(d))
+    o, lse = fa().fwd_splitkv(q, k, v, causal=causal, n_splits=999, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert fa().get_device_error() == 0
+    assert_close(o, lse, o_ref, lse_ref, what=f"splitkv one tile per split {B,H,N,Nk,d} causal={causal}")
 
 
 def test_fwd_splitkv_long_context_sampled():
