@@ -401,7 +401,12 @@ __device__ __forceinline__ void fwd_correction(const FwdParams& p, const uint8_t
 #pragma unroll
                     for (int e = 0; e < 32; ++e) v[e] = 0.f;
                 }
-                if (valid) store_row32<OutT>(orow + 32 * c, v);
+                if (valid) {
+                    if constexpr (SPLIT)
+                        store_row32_aligned32(reinterpret_cast<float*>(orow) + 32 * c, v);
+                    else
+                        store_row32<OutT>(orow + 32 * c, v);
+                }
             }
             if (n > 0) {
                 tc_fence_before_sync();
@@ -861,7 +866,12 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
 #pragma unroll
                         for (int e = 0; e < 32; ++e) v[e] = 0.f;
                     }
-                    if (valid) store_row32<OutT>(orow + 32 * c, v);
+                    if (valid) {
+                        if constexpr (SPLIT)  // partial slots are 512-byte multiples into the aligned workspace
+                            store_row32_aligned32(reinterpret_cast<float*>(orow) + 32 * c, v);
+                        else
+                            store_row32<OutT>(orow + 32 * c, v);
+                    }
                 }
             }
             if (valid) {

@@ -42,6 +42,13 @@ __device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, c
     }
 }
 
+// 32 fp32 values to a 32-byte aligned destination, in 32-byte stores.
+__device__ __forceinline__ void store_row32_aligned32(float* dst, const float (&v)[32])
+{
+#pragma unroll
+    for (int i = 0; i < 32; i += 8) st_global_v8_f32(dst + i, v + i);
+}
+
 template <typename OutT>
 __device__ __forceinline__ void store_row16(OutT* dst, const float (&v)[16]);
 
