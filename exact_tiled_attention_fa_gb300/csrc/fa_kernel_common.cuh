@@ -42,7 +42,8 @@ __device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* dst, c
     }
 }
 
-// 32 fp32 values to a 32-byte aligned destination, in 32-byte stores.
+// 32 fp32 values of a row to a 32-byte aligned destination, in 32-byte stores (a warp writing one
+// row per thread then fills whole sectors instead of halves).
 __device__ __forceinline__ void store_row32_aligned32(float* dst, const float (&v)[32])
 {
 #pragma unroll

@@ -74,24 +74,27 @@ def test_rows_without_visible_keys():
 
 @pytest.mark.parametrize("d", [128, 64, 32])
 def test_deterministic_and_no_writes_past_output(d):
-    # d <= 64 writes O through a staging tile and bulk tensor stores, d = 128 row by row; both
-    # must leave the memory after the last row untouched (the last query tile is ragged).
+    # d <= 64 writes O through a staging tile and bulk tensor stores, d = 128 row by row; at an
+    # output 32-byte aligned or only 16-byte aligned, both must leave the memory around O untouched
+    # (the last query tile is ragged) and give the same bits.
     B, H, N, Nk = 2, 2, 333, 257
     q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=6, device=DEV)
     guard = 4096
+    n = B * H * N * d
     for causal in (False, True):
         for dt in (torch.float32, torch.bfloat16):
-            buf = torch.full((B * H * N * d + guard,), float("nan"), dtype=dt, device=DEV)
-            lbuf = torch.full((B * H * N + guard,), float("nan"), dtype=torch.float32, device=DEV)
-            o = buf[: B * H * N * d].view(B, H, N, d)
-            lse = lbuf[: B * H * N].view(B, H, N)
-            fa().fwd(q, k, v, causal=causal, out=o, lse=lse)
-            torch.cuda.synchronize()
-            assert not torch.isnan(o).any() and not torch.isnan(lse).any()
-            assert torch.isnan(buf[B * H * N * d:]).all() and torch.isnan(lbuf[B * H * N:]).all()
             o2, lse2 = fa().fwd(q, k, v, causal=causal, out_dtype=dt)
-            torch.cuda.synchronize()
-            assert torch.equal(o, o2) and torch.equal(lse, lse2)
+            for shift in (0, 16 // torch.empty((), dtype=dt).element_size()):  # 0 or 16 bytes past 32-byte alignment
+                buf = torch.full((n + 2 * guard,), float("nan"), dtype=dt, device=DEV)
+                lbuf = torch.full((B * H * N + guard,), float("nan"), dtype=torch.float32, device=DEV)
+                o = buf[guard + shift: guard + shift + n].view(B, H, N, d)
+                lse = lbuf[: B * H * N].view(B, H, N)
+                fa().fwd(q, k, v, causal=causal, out=o, lse=lse)
+                torch.cuda.synchronize()
+                assert not torch.isnan(o).any() and not torch.isnan(lse).any()
+                assert torch.isnan(buf[: guard + shift]).all() and torch.isnan(buf[guard + shift + n:]).all()
+                assert torch.isnan(lbuf[B * H * N:]).all()
+                assert torch.equal(o, o2) and torch.equal(lse, lse2)
 
 
 def test_q_zero_averages_visible_values():
