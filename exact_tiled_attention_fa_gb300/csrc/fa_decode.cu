@@ -225,6 +225,7 @@ __device__ __forceinline__ void store_row_value(const DecodeParams& p, size_t i,
 template <int D, int R, bool FUSED>
 __global__ void __launch_bounds__(kDecWarps * 32) fa_decode_split_kernel(const DecodeParams p)
 {
+    grid_launch_dependents();  // the merge that follows may begin launching (it waits for this grid)
     using C = DecCfg<D, R>;
     constexpr int S = C::kSteps;
     const int s = blockIdx.x;
@@ -422,6 +423,7 @@ __global__ void __launch_bounds__(128) fa_merge_kernel(const MergeParams p)
     }
     OutT* out = reinterpret_cast<OutT*>(p.o) + static_cast<size_t>(row) * p.dv;
     float* lse = p.lse;
+    grid_dependency_wait();  // the parts are written by the split kernel launched before this one
     merge_row<VEC, IT, false>(
         p.lse_parts + static_cast<size_t>(row) * p.lse_row_stride, p.lse_part_stride,
         p.o_parts + static_cast<size_t>(row) * p.o_row_stride, p.o_part_stride, n_valid, p.dv, lane,
@@ -434,19 +436,26 @@ __global__ void __launch_bounds__(128) fa_merge_kernel(const MergeParams p)
 template <typename OutT>
 cudaError_t launch_merge_t(const MergeParams& p, cudaStream_t st)
 {
-    const unsigned grid = static_cast<unsigned>((p.rows + 3) / 4);
+    // Launched with programmatic stream serialization: the merge's CTAs may be scheduled while
+    // the split kernel's last CTAs still run, and wait in-kernel for its completion, so the
+    // launch latency between the two kernels is hidden.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((p.rows + 3) / 4));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     // float4 loads when every part row starts on 16 bytes (dv <= 512)
     const bool vec4 = p.dv % 4 == 0 && p.o_part_stride % 4 == 0 && p.o_row_stride % 4 == 0 &&
                       (reinterpret_cast<uintptr_t>(p.o_parts) & 15u) == 0;
-    if (!vec4)
-        fa_merge_kernel<OutT, 1, 16><<<grid, 128, 0, st>>>(p);
-    else if (p.dv <= 128)
-        fa_merge_kernel<OutT, 4, 1><<<grid, 128, 0, st>>>(p);
-    else if (p.dv <= 256)
-        fa_merge_kernel<OutT, 4, 2><<<grid, 128, 0, st>>>(p);
-    else
-        fa_merge_kernel<OutT, 4, 4><<<grid, 128, 0, st>>>(p);
-    return cudaGetLastError();
+    if (!vec4) return cudaLaunchKernelEx(&cfg, fa_merge_kernel<OutT, 1, 16>, p);
+    if (p.dv <= 128) return cudaLaunchKernelEx(&cfg, fa_merge_kernel<OutT, 4, 1>, p);
+    if (p.dv <= 256) return cudaLaunchKernelEx(&cfg, fa_merge_kernel<OutT, 4, 2>, p);
+    return cudaLaunchKernelEx(&cfg, fa_merge_kernel<OutT, 4, 4>, p);
 }
 
 template <int D>

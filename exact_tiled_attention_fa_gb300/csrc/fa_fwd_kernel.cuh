@@ -423,6 +423,7 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
 {
     using C = FwdCfg<D, static_cast<int>(sizeof(OutT))>;
     static_assert(!SPLIT || sizeof(OutT) == 4, "split partials are fp32");
+    if constexpr (SPLIT) grid_launch_dependents();  // the merge may begin launching (it waits for this grid)
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &

@@ -122,6 +122,7 @@ template <int RH>
 __global__ void __launch_bounds__(GqShape<RH>::kThreads, GqCfg<RH>::kCtasPerSm)
     fa_gqa_kernel(const __grid_constant__ SplitParams p)
 {
+    grid_launch_dependents();  // the merge that follows may begin launching (it waits for this grid)
     using C = GqCfg<RH>;
     using G = GqShape<RH>;
     constexpr int kGqWarpProducer = G::kWarpProducer;

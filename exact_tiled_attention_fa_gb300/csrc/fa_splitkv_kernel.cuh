@@ -80,6 +80,7 @@ struct SkCfg {
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kSkThreads, 1) fa_splitkv_kernel(const __grid_constant__ SplitParams p)
 {
+    grid_launch_dependents();  // the merge that follows may begin launching (it waits for this grid)
     using C = SkCfg<D>;
     constexpr int S = C::kStages;
     extern __shared__ uint8_t sk_smem_raw[];

@@ -133,6 +133,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Programmatic dependent launch (sm_90 and later).  A kernel that feeds a merge lets it start
+// launching (the merge is launched with programmatic stream serialization); the merge still
+// waits, in grid_dependency_wait, until this grid has completed and its writes are visible.
+// Both are no-ops for kernels launched the ordinary way.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Plain (untiled) bulk copy global -> shared of `bytes` (a multiple of 16, both
 // addresses 16-byte aligned), completion on an mbarrier.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
