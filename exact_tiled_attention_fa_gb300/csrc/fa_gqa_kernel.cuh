@@ -44,11 +44,11 @@ namespace fa {
 constexpr int kGqD = 128;  // head size of this kernel
 
 // Warp layout for RH heads per group: one set of four compute warps (thread t = key t / value
-// column t) per 8 or 16 heads, so a thread handles at most 16 heads; then the producer and the
-// issuer.  Each set reads the same TMEM lanes, its own columns.
+// column t) per 8 heads, so a thread handles 8 heads; then the producer and the issuer.  Each set
+// reads the same TMEM lanes, its own columns.
 template <int RH>
 struct GqShape {
-    static constexpr int kSets = RH >= 16 ? 2 : 1;
+    static constexpr int kSets = RH / 8;
     static constexpr int kRHS = RH / kSets;  // heads per set
     static constexpr int kCompute = 4 * kSets;
     static constexpr int kThreads = 32 * (kCompute + 2);
@@ -69,7 +69,7 @@ enum : int {
     kGbVFull = 14,   // + V stage (up to 2)
     kGbVEmpty = 16,  // + V stage: the tile's product has completed
     kGbRed = 18,     // + 2 * set + tile parity: a set's four warps' partial maxima (or sums) are in (count 4)
-    kGbCount = 22
+    kGbCount = 26
 };
 
 template <int RH>
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(GqShape<RH>::kThreads, GqCfg<RH>::kCtasPerSm)
             mbar_init(bar(kGbVFull + i), 1);
             mbar_init(bar(kGbVEmpty + i), 1);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(bar(kGbRed + i), 4);
+        for (int i = 0; i < 2 * G::kSets; ++i) mbar_init(bar(kGbRed + i), 4);
         *abort_flag = 0;
         fence_barrier_init();
     }
