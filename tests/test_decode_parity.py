@@ -184,11 +184,12 @@ def test_gqa_zero_and_clamped_lengths(R):
     assert_close(o[1:], lse[1:], o_ref, lse_ref, what=f"gqa lengths R={R}")
 
 
-@pytest.mark.parametrize("Hkv", [8, 4], ids=["R4_tensor_core", "R8_tensor_core"])
+@pytest.mark.parametrize("Hkv", [8, 4, 1], ids=["R4_tensor_core", "R8_tensor_core", "R32_four_warp_sets"])
 def test_gqa_full_size_sampled(Hkv):
     """The benchmark's GQA workloads (B=16, Hq=32 over Hkv=8 or 4, d=128, lengths U[1024, 32768]) in
-    their launch configuration, with fp32 O and with the benchmark's bf16 O; 24 seeded query heads
-    against the oracle."""
+    their launch configuration, and the same cache with 32 heads per group (four warp sets of the
+    transposed kernel), with fp32 O and with the benchmark's bf16 O; 24 seeded query heads against
+    the oracle."""
     B, Hq, Nk_max, d = 16, 32, 32768, 128
     q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=1024, hi=Nk_max, device=DEV)
     R = Hq // Hkv
