@@ -151,7 +151,7 @@ def oracle_gqa_compact(q, k, v, lens, scale):
 
 
 @pytest.mark.parametrize("d", [32, 64, 128])
-@pytest.mark.parametrize("R", [1, 2, 3, 4, 6, 8, 12, 16, 32, 40])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 6, 8, 12, 16, 24, 32, 40])  # 24: a padded fourth warp set
 @pytest.mark.parametrize("n_splits", [1, 5, 0])
 def test_gqa_decode(d, R, n_splits):
     B, Hkv, Nk_max = 3, 2, 700

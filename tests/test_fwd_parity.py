@@ -186,6 +186,7 @@ SPLIT = [
     (1, 1, 1, 2000, 64, 1.0),
     (1, 3, 256, 4097, 128, 2.0),
     (4, 16, 300, 2000, 64, 1.0),  # 128 heads x 2 query pairs: several split items per CTA
+    (2, 3, 500, 260, 64, 1.0),    # N > Nk at d = 64: causal rows with no visible key, ragged key tail
 ]
 
 
