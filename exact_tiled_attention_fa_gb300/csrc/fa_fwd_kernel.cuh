@@ -695,6 +695,7 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
                 // row in two 64-column loads (C3-shaped prefill 1000 -> 1036 TFLOP/s against four
                 // 32-column ones); d <= 64 keeps four (two measured 0.7 % slower there).
                 float mrow;
+                float mql[4];  // the load's per-chunk maxima (causal d <= 64)
                 if constexpr (D == 128) {
                     float mh[2];
                     tmem_ld64_max(t_s + 0, *reinterpret_cast<uint32_t(*)[64]>(&u[0]), mh[0]);
@@ -709,6 +710,10 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
                     tmem_ld32_max(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&u[96]), mq[3]);
                     tmem_ld_wait();
                     mrow = max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+                    if constexpr (CAUSAL) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) mql[q] = mq[q];
+                    }
                 }
                 if constexpr (!C::kAliasP) {  // S_i is in registers: its columns may be overwritten
                     tc_fence_before_sync();
@@ -719,7 +724,36 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
                 for (int c = 0; c < kBlockN; ++c) s[c] = __uint_as_float(u[c]);
                 const int k0 = (it.j0 + j) * kBlockN;
                 const bool need_mask = (k0 + kBlockN > p.Nk) || (CAUSAL && k0 + kBlockN - 1 > off + row0);
-                if (need_mask) {  // diagonal or ragged tile: mask, then take the max in registers
+                if (CAUSAL && D <= 64 && need_mask) {
+                    // Causal, d <= 64: the mask is taken per 32-column chunk, decided for the whole
+                    // warp.  A chunk every row of the warp sees keeps its load maximum; a chunk no row
+                    // sees is set to -inf (one select per column on the warp-wide test, no maximum);
+                    // only the chunk the warp's rows cut is tested column by column.  On a diagonal
+                    // tile every warp then masks one chunk instead of four (B=64 H=16 N=1024 d=64
+                    // causal prefill 707 -> 716 TFLOP/s).  Hidden scores become -inf rather than being offset, so a
+                    // non-finite score in a key a row cannot see never reaches that row; a constant
+                    // store in place of the select made the compiler spill the score row.
+                    const int lim = min(qpos, p.Nk - 1) - k0;  // columns 0 .. lim visible to this row
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        if (__all_sync(0xffffffffu, lim < 32 * q)) {
+                            float* t = s + 32 * q;
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) t[c] = lim < 32 * q ? -INFINITY : t[c];
+                            mql[q] = -INFINITY;
+                        } else if (!__all_sync(0xffffffffu, lim >= 32 * q + 31)) {
+                            float* t = s + 32 * q;
+#pragma unroll
+                            for (int c = 0; c < 32; ++c)
+                                if (32 * q + c > lim) t[c] = -INFINITY;
+                            float a = max3(t[0], t[1], t[2]);
+#pragma unroll
+                            for (int c = 3; c < 31; c += 2) a = max3(a, t[c], t[c + 1]);
+                            mql[q] = fmaxf(a, t[31]);
+                        }
+                    }
+                    mrow = max3(mql[0], mql[1], fmaxf(mql[2], mql[3]));
+                } else if (need_mask) {  // diagonal or ragged tile: mask, then take the max in registers
                     const int last = CAUSAL ? min(qpos, p.Nk - 1) : p.Nk - 1;  // last visible key
 #pragma unroll
                     for (int c = 0; c < kBlockN; ++c)

@@ -110,6 +110,27 @@ def test_q_zero_averages_visible_values():
             assert np.abs(to_np(lse)[:, :, i] - math.log(n)).max() <= 1e-5
 
 
+@pytest.mark.parametrize("d", [32, 64, 128])
+@pytest.mark.parametrize("N,Nk,j", [(512, 512, 300), (512, 512, 200), (512, 512, 511), (512, 512, 5),
+                                    (300, 512, 400)])
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")], ids=["nan", "inf"])
+def test_causal_hidden_key_does_not_reach_earlier_rows(d, N, Nk, j, bad):
+    """Under the causal mask a key reaches only the rows that see it: with every element of key j
+    non-finite, the rows placed before position j must equal the oracle on the clean keys.  Key 300
+    lies in the second 32-column chunk of diagonal tile 2 (a chunk hidden from the tile's first warp
+    and cut by its second), key 200 in the third chunk of tile 1, key 511 in the last chunk of the
+    last tile; with N < Nk the rows sit at positions Nk - N + i."""
+    B, H = 1, 2
+    q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=8, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    r1 = j - (Nk - N)  # rows 0 .. r1 - 1 do not see key j
+    o_ref, lse_ref = oracle.attention(q.cpu(), k.cpu(), v.cpu(), causal=True, scale=scale, rows=(0, r1))
+    kb = k.clone()
+    kb[:, :, j, :] = bad
+    o, lse = run(q, kb, v, True, scale, torch.float32)
+    assert_close(o[:, :, :r1], lse[:, :, :r1], o_ref, lse_ref, what=f"d={d} N={N} Nk={Nk} key {j} = {bad}")
+
+
 def _sampled_check(B, H, N, Nk, d, mult, causal, n_slices, rows=None, seed=0, out_dtype=torch.float32):
     q, k, v = attention_inputs(B, H, N, Nk, d, d, seed=seed, mult=mult, device=DEV)
     scale = 1.0 / math.sqrt(d)
