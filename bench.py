@@ -10,10 +10,12 @@ needed between iterations.  The split-KV decode (B=16, H=32, d=128, lengths unif
 [1024, 32768], 4.4 GB of K/V read per call) is timed in the same run and reported under
 "decode" in GB/s of algorithmic K/V bytes.
 
-Timing: CUDA events recorded on the launching stream around every kernel launch, W
-untimed warm-up steps, a barrier and a device synchronisation on both sides of exactly K
-timed steps, max over ranks.  SM clocks and throttle reasons are sampled with nvidia-smi
-during the timed region.  Under torchrun every rank runs the same per-GPU work on its own
+Timing: W untimed warm-up steps, then exactly K steps launched back to back between two
+CUDA events on the launching stream, with a barrier and a device synchronisation on both
+sides, max over ranks (`value`, `ms_per_step`).  A second pass of K steps records an event
+between the two calls of every step for the per-kernel times (`kernels`, `roofline`); the
+events serialise the kernels, so that pass's steps are slightly longer.  SM clocks and
+throttle reasons are sampled with nvidia-smi during both passes.  Under torchrun every rank runs the same per-GPU work on its own
 GPU (replicas: the path has no data exchange), so scaling is weak.
 
 --impl reference times the CPU FP64 oracle on the host cores instead (each step a bounded
@@ -48,8 +50,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the SHA-256 of the kernel code it was taken on (comments excluded); reported only while the
 # code is unchanged.
 KERNEL_TRAFFIC = {
-    # profiles/fa_fwd_kernel_d64_gpt2medium_prefill.md: non-causal launch, 402.81 MB read + 109.88 MB written
-    "f81e2a61c8b2a341f4205a20b7cbe7ec656ae1d89b71c99d070d41420747b1e3": 512.70e6,
+    # profiles/fa_fwd_kernel_d64_gpt2medium_prefill.md: non-causal launch, 402.76 MB read + 109.59 MB written
+    "cdef320a0acc6b04802af5e041d008046b8751c95bc310cf2ca748af932fbaa2": 512.35e6,
 }
 
 
@@ -267,12 +269,22 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     t_start.record(stream)
     for i in range(args.steps):
-        step(evs[i])
+        step()
     t_end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    clocks = sampler.stop()
     total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    # Kernel breakdown: the same K steps again with an event recorded between the two calls.  An
+    # event between two kernels serialises them (the second no longer starts its setup during the
+    # first one's tail), so these steps take a little longer than the back-to-back ones above.
+    b_start, b_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    b_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    b_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    breakdown_ms = b_start.elapsed_time(b_end)
     nc_all = [e[0].elapsed_time(e[1]) for e in evs]
     c_all = [e[2].elapsed_time(e[3]) for e in evs]
     nc_ms, c_ms = statistics.mean(nc_all), statistics.mean(c_all)
@@ -303,6 +315,8 @@ def run_ours(args, world, rank, local):
                    "flops_per_step": f_nc + f_c, "l2": "inputs 403 MB > 129 MB L2 (no flush needed)",
                    "parallelism": f"replicas x{world}"},
         "kernels": {
+            "pass": f"{args.steps} more steps with an event between the two calls, "
+                    f"{breakdown_ms / args.steps:.4f} ms per step (events serialise the launches)",
             "fa_fwd non-causal": {"ms": nc_ms, "tflops": achieved, "frac_of_peak": achieved / peak,
                                   "timing": {"ms_median": statistics.median(nc_all), "ms_min": min(nc_all),
                                              "ms_max": max(nc_all), "calls": len(nc_all)}},

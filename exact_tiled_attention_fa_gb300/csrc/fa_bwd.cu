@@ -45,6 +45,8 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8])
 template <typename OT>
 __global__ void __launch_bounds__(kPrepThreads) fa_bwd_prep_kernel(const BwdPrepParams p)
 {
+    grid_launch_dependents();  // the tensor-core kernel may begin its setup (it waits for this grid)
+    grid_dependency_wait();    // O, dO and LSE are written by earlier kernels on the stream
     const int G = p.d / 8;
     const long long rows = static_cast<long long>(p.BH) * p.Tr * kBlockM;
     const long long t = static_cast<long long>(blockIdx.x) * kPrepThreads + threadIdx.x;
@@ -87,6 +89,8 @@ __global__ void __launch_bounds__(kPrepThreads) fa_bwd_prep_kernel(const BwdPrep
 template <typename GradT>
 __global__ void __launch_bounds__(128) fa_bwd_dq_kernel(const BwdDqParams p)
 {
+    grid_launch_dependents();
+    grid_dependency_wait();  // the accumulator is complete once the tensor-core kernel has finished
     const long long row = static_cast<long long>(blockIdx.x) * 128 + threadIdx.x;
     if (row >= static_cast<long long>(p.BH) * p.N) return;
     const int bh = static_cast<int>(row / p.N);
@@ -111,11 +115,8 @@ cudaError_t launch_bwd_prep(const BwdPrepParams& p, fa_dtype o_dtype, cudaStream
     const long long blocks = (threads + kPrepThreads - 1) / kPrepThreads;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    if (o_dtype == FA_F32)
-        fa_bwd_prep_kernel<float><<<static_cast<unsigned>(blocks), kPrepThreads, 0, st>>>(p);
-    else
-        fa_bwd_prep_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), kPrepThreads, 0, st>>>(p);
-    return cudaGetLastError();
+    if (o_dtype == FA_F32) return launch_pdl(fa_bwd_prep_kernel<float>, static_cast<unsigned>(blocks), kPrepThreads, 0, st, p);
+    return launch_pdl(fa_bwd_prep_kernel<__nv_bfloat16>, static_cast<unsigned>(blocks), kPrepThreads, 0, st, p);
 }
 
 cudaError_t launch_bwd_dq(const BwdDqParams& p, fa_dtype grad_dtype, cudaStream_t st)
@@ -124,11 +125,8 @@ cudaError_t launch_bwd_dq(const BwdDqParams& p, fa_dtype grad_dtype, cudaStream_
     const long long blocks = (rows + 127) / 128;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    if (grad_dtype == FA_F32)
-        fa_bwd_dq_kernel<float><<<static_cast<unsigned>(blocks), 128, 0, st>>>(p);
-    else
-        fa_bwd_dq_kernel<__nv_bfloat16><<<static_cast<unsigned>(blocks), 128, 0, st>>>(p);
-    return cudaGetLastError();
+    if (grad_dtype == FA_F32) return launch_pdl(fa_bwd_dq_kernel<float>, static_cast<unsigned>(blocks), 128, 0, st, p);
+    return launch_pdl(fa_bwd_dq_kernel<__nv_bfloat16>, static_cast<unsigned>(blocks), 128, 0, st, p);
 }
 
 }  // namespace fa

@@ -423,7 +423,10 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
 {
     using C = FwdCfg<D, static_cast<int>(sizeof(OutT))>;
     static_assert(!SPLIT || sizeof(OutT) == 4, "split partials are fp32");
-    if constexpr (SPLIT) grid_launch_dependents();  // the merge may begin launching (it waits for this grid)
+    // Programmatic dependent launch: the next kernel on the stream (the merge of split mode, or the
+    // next forward) may begin launching now and set itself up while this grid's last CTAs run; it
+    // waits for this grid's completion before touching memory, as this grid does below.
+    grid_launch_dependents();
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -468,6 +471,9 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    // Launched with programmatic stream serialization: the setup above may overlap the previous
+    // kernel on the stream; every global read and write comes after that kernel has completed.
+    grid_dependency_wait();
 
     constexpr bool kWithCorr = kCorr<D, CAUSAL>;
     if (kWithCorr && warp >= kWarpCorr) {
@@ -986,8 +992,7 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t st)
     const int per_head = (kOrderedWalk<D, CAUSAL> && q.n_full != p.n_qp) ? (q.n_full > 0 ? q.n_full : 1) : p.n_qp;
     q.step_heads = static_cast<int>(step / per_head);
     q.step_rem = static_cast<int>(step % per_head);
-    kern<<<grid, kThreads<D, CAUSAL>, C::kSmemBytes, st>>>(q);
-    return cudaGetLastError();
+    return launch_pdl(kern, static_cast<unsigned>(grid), kThreads<D, CAUSAL>, C::kSmemBytes, st, q);
 }
 
 template <int D>

@@ -133,10 +133,11 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Programmatic dependent launch (sm_90 and later).  A kernel that feeds a merge lets it start
-// launching (the merge is launched with programmatic stream serialization); the merge still
-// waits, in grid_dependency_wait, until this grid has completed and its writes are visible.
-// Both are no-ops for kernels launched the ordinary way.
+// Programmatic dependent launch (sm_90 and later).  grid_launch_dependents lets the next kernel
+// on the stream, if it was launched with programmatic stream serialization, start launching and
+// run its setup while this grid finishes; that kernel still waits, in grid_dependency_wait, until
+// this grid has completed and its writes are visible.  Both are no-ops for kernels launched the
+// ordinary way.
 __device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
