@@ -45,8 +45,8 @@ __device__ __forceinline__ void load8(const float* p, float (&v)[8])
 template <typename OT>
 __global__ void __launch_bounds__(kPrepThreads) fa_bwd_prep_kernel(const BwdPrepParams p)
 {
-    grid_launch_dependents();  // the tensor-core kernel may begin its setup (it waits for this grid)
     grid_dependency_wait();    // O, dO and LSE are written by earlier kernels on the stream
+    grid_launch_dependents();  // the tensor-core kernel may begin its setup (it waits for this grid)
     const int G = p.d / 8;
     const long long rows = static_cast<long long>(p.BH) * p.Tr * kBlockM;
     const long long t = static_cast<long long>(blockIdx.x) * kPrepThreads + threadIdx.x;
@@ -89,8 +89,8 @@ __global__ void __launch_bounds__(kPrepThreads) fa_bwd_prep_kernel(const BwdPrep
 template <typename GradT>
 __global__ void __launch_bounds__(128) fa_bwd_dq_kernel(const BwdDqParams p)
 {
-    grid_launch_dependents();
     grid_dependency_wait();  // the accumulator is complete once the tensor-core kernel has finished
+    grid_launch_dependents();
     const long long row = static_cast<long long>(blockIdx.x) * 128 + threadIdx.x;
     if (row >= static_cast<long long>(p.BH) * p.N) return;
     const int bh = static_cast<int>(row / p.N);

@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "fa_internal.h"
+#include "fa_kernel_common.cuh"
 #include "ptx.cuh"
 
 namespace fa {
@@ -225,6 +226,7 @@ __device__ __forceinline__ void store_row_value(const DecodeParams& p, size_t i,
 template <int D, int R, bool FUSED>
 __global__ void __launch_bounds__(kDecWarps * 32) fa_decode_split_kernel(const DecodeParams p)
 {
+    grid_dependency_wait();    // launched as a programmatic dependent of the previous kernel
     grid_launch_dependents();  // the merge that follows may begin launching (it waits for this grid)
     using C = DecCfg<D, R>;
     constexpr int S = C::kSteps;
@@ -424,6 +426,7 @@ __global__ void __launch_bounds__(128) fa_merge_kernel(const MergeParams p)
     OutT* out = reinterpret_cast<OutT*>(p.o) + static_cast<size_t>(row) * p.dv;
     float* lse = p.lse;
     grid_dependency_wait();  // the parts are written by the split kernel launched before this one
+    grid_launch_dependents();
     merge_row<VEC, IT, false>(
         p.lse_parts + static_cast<size_t>(row) * p.lse_row_stride, p.lse_part_stride,
         p.o_parts + static_cast<size_t>(row) * p.o_row_stride, p.o_part_stride, n_valid, p.dv, lane,
@@ -463,18 +466,16 @@ cudaError_t launch_decode_d(const DecodeParams& p, fa_dtype o_dtype, cudaStream_
 {
     dim3 grid(p.n_splits, p.Hkv, p.B);
     const int R = p.H / p.Hkv;
+    cudaError_t e;
     switch (R) {
     case 1:
-        if (p.counters != nullptr)
-            fa_decode_split_kernel<D, 1, true><<<grid, kDecWarps * 32, 0, st>>>(p);
-        else
-            fa_decode_split_kernel<D, 1, false><<<grid, kDecWarps * 32, 0, st>>>(p);
+        e = p.counters != nullptr ? launch_pdl(fa_decode_split_kernel<D, 1, true>, grid, kDecWarps * 32, 0, st, p)
+                                  : launch_pdl(fa_decode_split_kernel<D, 1, false>, grid, kDecWarps * 32, 0, st, p);
         break;
-    case 2: fa_decode_split_kernel<D, 2, false><<<grid, kDecWarps * 32, 0, st>>>(p); break;
-    case 4: fa_decode_split_kernel<D, 4, false><<<grid, kDecWarps * 32, 0, st>>>(p); break;
+    case 2: e = launch_pdl(fa_decode_split_kernel<D, 2, false>, grid, kDecWarps * 32, 0, st, p); break;
+    case 4: e = launch_pdl(fa_decode_split_kernel<D, 4, false>, grid, kDecWarps * 32, 0, st, p); break;
     default: return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || p.counters != nullptr) return e;  // fused: no second launch
     MergeParams m{};
     m.o_parts = p.o_part;

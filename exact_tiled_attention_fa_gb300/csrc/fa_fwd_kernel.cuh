@@ -423,10 +423,6 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
 {
     using C = FwdCfg<D, static_cast<int>(sizeof(OutT))>;
     static_assert(!SPLIT || sizeof(OutT) == 4, "split partials are fp32");
-    // Programmatic dependent launch: the next kernel on the stream (the merge of split mode, or the
-    // next forward) may begin launching now and set itself up while this grid's last CTAs run; it
-    // waits for this grid's completion before touching memory, as this grid does below.
-    grid_launch_dependents();
     constexpr int S = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -473,7 +469,10 @@ __global__ void __launch_bounds__(kThreads<D, CAUSAL>, 1) fa_fwd_kernel(const __
     const uint32_t tmem = *tmem_slot;
     // Launched with programmatic stream serialization: the setup above may overlap the previous
     // kernel on the stream; every global read and write comes after that kernel has completed.
+    // Then the next kernel (the merge of split mode, or the next forward) may begin launching and
+    // set itself up while this grid runs; it waits for this grid's completion in the same way.
     grid_dependency_wait();
+    grid_launch_dependents();
 
     constexpr bool kWithCorr = kCorr<D, CAUSAL>;
     if (kWithCorr && warp >= kWarpCorr) {

@@ -122,6 +122,7 @@ template <int RH>
 __global__ void __launch_bounds__(GqShape<RH>::kThreads, GqCfg<RH>::kCtasPerSm)
     fa_gqa_kernel(const __grid_constant__ SplitParams p)
 {
+    grid_dependency_wait();    // launched as a programmatic dependent of the previous kernel
     grid_launch_dependents();  // the merge that follows may begin launching (it waits for this grid)
     using C = GqCfg<RH>;
     using G = GqShape<RH>;
@@ -491,8 +492,7 @@ cudaError_t launch_gqa_t(const SplitParams& p, cudaStream_t st)
         configured[dev] = true;
     }
     dim3 grid(p.n_splits, p.groups_per_batch, p.n_groups / p.groups_per_batch);
-    kern<<<grid, GqShape<RH>::kThreads, C::kSmemBytes, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, GqShape<RH>::kThreads, C::kSmemBytes, st, p);
 }
 
 // Query heads per group R in [5, 32], head size 128.

@@ -77,15 +77,17 @@ __device__ __forceinline__ void store_row16<__nv_bfloat16>(__nv_bfloat16* dst, c
 
 // Launch with programmatic stream serialization: the kernel may start (and run its setup) while
 // the previous kernel on the stream finishes, if that kernel has called grid_launch_dependents.
-// Every kernel launched this way calls grid_dependency_wait() before its first global read or write,
-// which returns once the previous kernel has completed and its writes are visible.
+// Every kernel launched this way calls grid_dependency_wait() before its first global read or write
+// that the previous kernel could affect, and calls grid_launch_dependents() only after that wait:
+// the wait returns once the previous kernel has completed and its writes are visible, so when any
+// of these kernels starts, every kernel before its immediate predecessor has completed.
 template <typename... Expected, typename... Actual>
-inline cudaError_t launch_pdl(void (*kern)(Expected...), unsigned grid, unsigned block, size_t smem,
+inline cudaError_t launch_pdl(void (*kern)(Expected...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t st, const Actual&... args)
 {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

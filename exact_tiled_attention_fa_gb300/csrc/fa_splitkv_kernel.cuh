@@ -80,6 +80,7 @@ struct SkCfg {
 template <int D, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kSkThreads, 1) fa_splitkv_kernel(const __grid_constant__ SplitParams p)
 {
+    grid_dependency_wait();    // launched as a programmatic dependent of the previous kernel
     grid_launch_dependents();  // the merge that follows may begin launching (it waits for this grid)
     using C = SkCfg<D>;
     constexpr int S = C::kStages;
@@ -395,8 +396,7 @@ cudaError_t launch_splitkv_t(const SplitParams& p, cudaStream_t st)
         configured[dev] = true;
     }
     dim3 grid(p.n_splits, p.n_qtiles, p.n_groups);
-    kern<<<grid, kSkThreads, C::kSmemBytes, st>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, grid, kSkThreads, C::kSmemBytes, st, p);
 }
 
 template <int D>
