@@ -40,6 +40,11 @@
  *     nothing.  Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
  *     NULL = the legacy default stream) and never synchronise, except
  *     fa_get_device_error.
+ *   - Stream order is kept: every kernel is launched with programmatic stream
+ *     serialization, so it may start its setup (barriers, tensor memory) while the kernel
+ *     before it on `stream` finishes, but it reads and writes global memory only after that
+ *     kernel has completed and its writes are visible.  A caller's kernel launched after a
+ *     call without that attribute starts once the call's kernels have completed, as usual.
  *   - CUDA graphs: after the first call on a device (which caches kernel attributes and
  *     device addresses), a call launches kernels on `stream` and does nothing else on the
  *     device, so every entry point but fa_get_device_error may be captured into a CUDA
