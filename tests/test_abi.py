@@ -59,6 +59,31 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, d=256, dv=256) == fa.FA_ERR_UNSUPPORTED
 
 
+def test_sizes_past_the_index_limits_are_rejected(lib):
+    # The kernels index work items (and, in split mode, rows) with 32-bit integers; sizes whose
+    # item or row count passes the stated limits return FA_ERR_INVALID_ARG before any launch.  Each
+    # case has a control just under the limit that gets past the size check and is then rejected by
+    # a later one (head size or workspace), so nothing is launched on the fake pointers.
+    assert _fwd(lib, B=32768, H=32768, N=256, Nk=256) == fa.FA_ERR_INVALID_ARG  # 2^30 items
+    assert _fwd(lib, B=32767, H=32767, N=256, Nk=256, d=48, dv=48) == fa.FA_ERR_UNSUPPORTED
+    assert _fwd(lib, B=16384, H=32768, N=512, Nk=256) == fa.FA_ERR_INVALID_ARG
+    bwd = lib.fa_bwd
+    def call_bwd(B, H, ws_bytes):
+        return bwd(P, P, P, P, P, P, P, P, P, P, ws_bytes, B, H, 128, 128, 64, 64, 0, 0.125, 0, 0, NULL)
+    assert call_bwd(32768, 32768, 1 << 40) == fa.FA_ERR_INVALID_ARG  # 2^30 key-tile items
+    assert call_bwd(32767, 32767, 0) == fa.FA_ERR_WORKSPACE
+    skv = lib.fa_fwd_splitkv
+    def call_skv(B, H, N, Nk, n, d=64):
+        return skv(P, P, P, P, P, P, 1 << 60, B, H, N, Nk, d, d, 0, 0.125, n, 0, NULL)
+    assert call_skv(65536, 32768, 1, 128, 1) == fa.FA_ERR_INVALID_ARG  # B*H*N = 2^31 rows
+    assert call_skv(65535, 32768, 1, 128, 1, d=48) == fa.FA_ERR_UNSUPPORTED
+    gqa = lib.fa_decode_splitkv_gqa
+    def call_gqa(B, d=128):
+        return gqa(P, P, P, P, P, P, P, 1 << 40, B, 8, 2, 1000, d, d, 0.1, 4, 0, NULL)
+    assert call_gqa(65536) == fa.FA_ERR_INVALID_ARG
+    assert call_gqa(65535, d=96) == fa.FA_ERR_UNSUPPORTED
+
+
 def _dec(lib, ws_bytes=1 << 20, n_splits=4, q=P, ws=P, B=2, H=2, Nk=1000, d=128, dv=128, scale=0.1, odt=0):
     return lib.fa_decode_splitkv(q, P, P, P, P, P, ws, ws_bytes, B, H, Nk, d, dv, scale, n_splits, odt, NULL)
 
