@@ -778,9 +778,9 @@ def _case_call(fa, dev, name):
         o = torch.empty((B, H, N, d), dtype=torch.bfloat16, device=dev)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         return (lambda: fa.fwd(q, k, v, causal=causal, out=o, lse=lse)), desc
-    if name in ("gqa4", "gqa8"):
+    if name in ("gqa4", "gqa8", "gqa16", "gqa32"):
         B, Hq, Nk_max, d = GQA["B"], GQA["Hq"], GQA["Nk_max"], GQA["d"]
-        Hkv = Hq // (4 if name == "gqa4" else 8)
+        Hkv = Hq // int(name[3:])
         q, k, v, lens = gqa_decode_inputs(B, Hq, Hkv, Nk_max, d, d, seed=0, lo=GQA["lo"], hi=GQA["hi"], device=dev)
         lens_d = lens.to(dev)
         n = fa.decode_gqa_default_splits(B, Hq, Hkv, Nk_max, d, fa.num_sms(dev))
@@ -828,7 +828,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", default=None,
                     help="run one workload alone (fwd-c1, fwd-c1-causal, fwd-c2, fwd-c2-causal, fwd-c3a, "
-                         "fwd-c3a-causal, fwd-c3b, fwd-c3b-causal, fwd-c4, decode, gqa4, gqa8, splitkv-prefill) for profiling")
+                         "fwd-c3a-causal, fwd-c3b, fwd-c3b-causal, fwd-c4, decode, gqa4, gqa8, gqa16, gqa32, splitkv-prefill) for profiling")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
