@@ -6,9 +6,10 @@
 // for rows past N and rows that see no key (their P is then exactly 0); and the fp32
 // dQ accumulator is zeroed.  Rows are padded to whole 128-row query tiles.
 //
-// dQ conversion: the accumulator, laid out [head][query tile][d/4][128 rows][4] so that
-// the tensor-core kernel's atomics from one warp cover 512 contiguous bytes, is written
-// out as dQ [head][N][d] in the gradient dtype.
+// dQ conversion: the accumulator, laid out per (head, query tile) as [d/4][128 rows][4] (d = 128:
+// the tensor-core kernel's atomics from one warp cover 512 contiguous bytes) or [4][d/4][32][4]
+// (d <= 64: each warp's bulk reductions cover 2 KB blocks), is written out as dQ [head][N][d] in
+// the gradient dtype.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -95,14 +96,18 @@ __global__ void __launch_bounds__(128) fa_bwd_dq_kernel(const BwdDqParams p)
     if (row >= static_cast<long long>(p.BH) * p.N) return;
     const int bh = static_cast<int>(row / p.N);
     const int q = static_cast<int>(row - static_cast<long long>(bh) * p.N);
+    const int qt = q % kBlockM;  // row within the query tile
+    const bool bulk = dq_bulk(p.d);
+    // plane stride: 128 rows of a tile ([d/4][128][4]) or the 32 rows of a row quarter ([4][d/4][32][4])
+    const int plane = bulk ? 32 * 4 : kBlockM * 4;
     const float* src = p.dq_acc + (static_cast<size_t>(bh) * p.Tr + q / kBlockM) * (p.d / 4) * (kBlockM * 4) +
-                       (q % kBlockM) * 4;
+                       (bulk ? (qt / 32) * (p.d / 4) * (32 * 4) + (qt % 32) * 4 : qt * 4);
     GradT* dst = reinterpret_cast<GradT*>(p.dq) + static_cast<size_t>(row) * p.d;
     for (int c = 0; c < p.d; c += 16) {
         float v[16];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const float4 f = *reinterpret_cast<const float4*>(src + static_cast<size_t>(c / 4 + e) * (kBlockM * 4));
+            const float4 f = *reinterpret_cast<const float4*>(src + static_cast<size_t>(c / 4 + e) * plane);
             v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
         }
         store_row16<GradT>(dst + c, v);

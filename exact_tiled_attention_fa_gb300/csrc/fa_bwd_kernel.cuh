@@ -23,8 +23,10 @@
 // threads write their dS^T rows to shared memory: read there as K-major rows they are
 // the A operand of dK (d <= 64; d = 128 keeps dS^T in tensor memory too), and read as
 // MN-major (M-contiguous) they are dS, the A operand of dQ_i = dS K_j.  dQ_i (fp32, TMEM) is added
-// into a zeroed fp32 accumulator in global memory with vector atomics; a final
-// kernel converts it.  The scale is folded into dS (both dQ and dK carry it).
+// into a zeroed fp32 accumulator in global memory, for d <= 64 with bulk reductions from shared
+// memory (2 KB blocks; fp32 atomics from the threads measured 13 % slower, the L2's atomic rate being
+// the limit), for d = 128 with vector atomics; a final kernel converts it.  The scale is folded into
+// dS (both dQ and dK carry it).
 //
 // Sixteen warps (four warpgroups):
 //   warps 0-3 / 4-7  compute: thread t of the warpgroup owns key row t (TMEM lane t)
@@ -130,7 +132,10 @@ struct BwdCfg {
     static constexpr int kOffDS = kOffDO + kQStages * kTileBytes;         // two query halves of kDSBlk
     static constexpr int kOffL = kOffDS + 2 * kDSBlk;                     // + stage * 512
     static constexpr int kOffDsc = kOffL + kQStages * 512;                // + stage * 512
-    static constexpr int kOffBar = kOffDsc + kQStages * 512;
+    // dQ staging for the bulk reductions (dq_bulk): per dQ warp two 2 KB blocks of 32 rows x 16 columns
+    static constexpr bool kDQBulk = dq_bulk(D);
+    static constexpr int kOffDQS = kOffDsc + kQStages * 512;
+    static constexpr int kOffBar = kOffDQS + (kDQBulk ? 4 * 2 * 2048 : 0);
     static constexpr int kNumBars = 26;
     static_assert(kBbCount <= kNumBars, "barrier slots");
     static constexpr int kUsedBytes = kOffBar + kNumBars * 8 + 16;
@@ -458,7 +463,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fa_bwd_kernel(const __grid_con
         const uint32_t t_dq = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + C::kColDQ;
         bool ok = true;
         int g = 0;
-        for (Cursor cur = first_item(); ok && cur.x < n_items; next_item(cur)) {
+        if constexpr (C::kDQBulk) {
+            // Each warp stages its 32 rows 16 columns at a time (column groups of 4: lane l writes 16
+            // bytes at (group * 32 + l) * 16, so a warp's stores hit distinct banks) and lane 0 adds the
+            // 2 KB block into the accumulator with one bulk reduction; two blocks alternate, and before
+            // refilling one, lane 0 waits until the reduction issued from it has read it.
+            const int wq = warp & 3;
+            const int lane = threadIdx.x & 31;
+            const uint32_t stg = sbase + C::kOffDQS + static_cast<uint32_t>(wq) * 4096u;
+            int chunks = 0;
+            for (Cursor cur = first_item(); ok && cur.x < n_items; next_item(cur)) {
+                const Item it = item_at(cur);
+                for (int t = 0; t < it.n; ++t, ++g) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDQFull), g & 1, limit, abort_flag));
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    // this warp's [d/4][32][4] block of the (head, query tile) accumulator
+                    float* acc = p.dq_acc + (static_cast<size_t>(it.bh) * p.Tr + (it.i_first + t)) * (D * kBlockM) +
+                                 static_cast<size_t>(wq) * (D * 32);
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(t_dq + 32u * c, v);
+                        tmem_ld_wait();
+                        if (c == D / 32 - 1) {  // the whole dQ row is in registers: release the columns
+                            tc_fence_before_sync();
+                            mbar_arrive(bar(kBbDQFree));
+                        }
+#pragma unroll
+                        for (int k2 = 0; k2 < 2; ++k2, ++chunks) {
+                            const uint32_t blk = stg + static_cast<uint32_t>(chunks & 1) * 2048u;
+                            if (lane == 0) bulk_wait_read<1>();  // the reduction from this block two chunks ago read it
+                            __syncwarp();
+#pragma unroll
+                            for (int q4 = 0; q4 < 4; ++q4)
+                                st_shared_v4(blk + static_cast<uint32_t>(q4 * 32 + lane) * 16u, v[16 * k2 + 4 * q4],
+                                             v[16 * k2 + 4 * q4 + 1], v[16 * k2 + 4 * q4 + 2], v[16 * k2 + 4 * q4 + 3]);
+                            fence_proxy_async_shared();
+                            __syncwarp();
+                            if (lane == 0) {
+                                bulk_reduce_add_f32(acc + (2 * c + k2) * (4 * 32 * 4), blk, 2048u);
+                                bulk_commit_group();
+                            }
+                        }
+                    }
+                }
+            }
+            if (lane == 0 && chunks > 0) bulk_wait_all();  // reductions complete before the CTA exits
+        }
+        for (Cursor cur = first_item(); !C::kDQBulk && ok && cur.x < n_items; next_item(cur)) {
             const Item it = item_at(cur);
             for (int t = 0; t < it.n; ++t, ++g) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(kBbDQFull), g & 1, limit, abort_flag));

@@ -64,7 +64,7 @@ struct BwdParams {
     CUtensorMap tm_dv;  // dV, the same
     const float* lse2;  // [B*H][Tr*128]: LSE * log2(e); +inf past N and where no key is visible
     const float* dsc;   // [B*H][Tr*128]: scale * sum_c dO[c] O[c]; 0 past N
-    float* dq_acc;      // [B*H][Tr][d/4][128][4] fp32, zeroed before the kernel
+    float* dq_acc;      // [B*H][Tr] tiles of 128 x d fp32 (layout: see dq_bulk), zeroed before the kernel
     void* dk;           // [B*H][Nk][d], gradient dtype
     void* dv;           // [B*H][Nk][d]
     int* status;
@@ -77,6 +77,15 @@ struct BwdParams {
     // (the causal rotation), so that the kernel advances its items without a division
     int step_heads, step_jr, step_rot;
 };
+
+#ifndef FA_DQ_BULK
+#define FA_DQ_BULK 1
+#endif
+// d <= 64: the tensor-core kernel adds its dQ tiles into the accumulator with bulk reductions from
+// shared memory, and the accumulator of a (head, query tile) is laid out [row quarter w][d/4][32][4]
+// (row q: w = q / 32, lane q mod 32), so that each warp's 16-column block is 2 KB contiguous.
+// d = 128 (no shared memory left for the staging) keeps vector atomics and the [d/4][128][4] layout.
+constexpr bool dq_bulk(int d) { return FA_DQ_BULK != 0 && d <= 64; }
 
 struct BwdPrepParams {
     const void* o;      // [B*H][N][d], bf16 or fp32 (forward output)

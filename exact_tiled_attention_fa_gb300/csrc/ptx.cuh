@@ -169,6 +169,20 @@ __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bu
 // Waits until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Waits until at most N of this thread's committed bulk groups are still reading shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory"); }
+
+// Bulk reduction shared -> global: dst[i] += src[i] for `bytes` / 4 fp32 values (both addresses
+// 16-byte aligned, bytes a multiple of 16), performed by the memory system, tracked by the issuing
+// thread's bulk-async groups.
+__device__ __forceinline__ void bulk_reduce_add_f32(float* dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+}
+
 // Generic-proxy writes to shared memory become visible to the async proxy.
 __device__ __forceinline__ void fence_proxy_async_shared()
 {
