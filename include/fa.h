@@ -128,6 +128,9 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  * dQ accumulator), the tensor-core pass (a persistent grid, one CTA per SM, walking the
  * (b, h, 128-key tile) items; each item's dK and dV written when its walk ends, dQ added into
  * the accumulator) and the dQ conversion.
+ * The key tiles' shares of dQ are added into the fp32 accumulator by the memory system in
+ * whatever order the CTAs reach it, so grad_q can differ in its last bits from run to run;
+ * grad_k and grad_v are summed on chip in a fixed order and are reproducible.
  * Returns FA_ERR_WORKSPACE if ws_bytes is too small (nothing launched).
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
