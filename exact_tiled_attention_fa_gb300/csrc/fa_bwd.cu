@@ -86,8 +86,8 @@ __global__ void __launch_bounds__(kPrepThreads) fa_bwd_prep_kernel(const BwdPrep
 }
 
 // One thread per query row: reads its row from the d / 4 planes (a warp reads 512
-// contiguous bytes per plane) and writes it contiguously.
-template <typename GradT>
+// contiguous bytes per plane), all of them before the first store, and writes it contiguously.
+template <typename GradT, int D>
 __global__ void __launch_bounds__(128) fa_bwd_dq_kernel(const BwdDqParams p)
 {
     grid_dependency_wait();  // the accumulator is complete once the tensor-core kernel has finished
@@ -97,21 +97,20 @@ __global__ void __launch_bounds__(128) fa_bwd_dq_kernel(const BwdDqParams p)
     const int bh = static_cast<int>(row / p.N);
     const int q = static_cast<int>(row - static_cast<long long>(bh) * p.N);
     const int qt = q % kBlockM;  // row within the query tile
-    const bool bulk = dq_bulk(p.d);
+    constexpr bool kBulk = dq_bulk(D);
     // plane stride: 128 rows of a tile ([d/4][128][4]) or the 32 rows of a row quarter ([4][d/4][32][4])
-    const int plane = bulk ? 32 * 4 : kBlockM * 4;
-    const float* src = p.dq_acc + (static_cast<size_t>(bh) * p.Tr + q / kBlockM) * (p.d / 4) * (kBlockM * 4) +
-                       (bulk ? (qt / 32) * (p.d / 4) * (32 * 4) + (qt % 32) * 4 : qt * 4);
-    GradT* dst = reinterpret_cast<GradT*>(p.dq) + static_cast<size_t>(row) * p.d;
-    for (int c = 0; c < p.d; c += 16) {
-        float v[16];
+    constexpr int kPlane = kBulk ? 32 * 4 : kBlockM * 4;
+    const float* __restrict__ src = p.dq_acc + (static_cast<size_t>(bh) * p.Tr + q / kBlockM) * (D * kBlockM) +
+                                    (kBulk ? (qt / 32) * (D * 32) + (qt % 32) * 4 : qt * 4);
+    GradT* __restrict__ dst = reinterpret_cast<GradT*>(p.dq) + static_cast<size_t>(row) * D;
+    float v[D];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float4 f = *reinterpret_cast<const float4*>(src + static_cast<size_t>(c / 4 + e) * plane);
-            v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
-        }
-        store_row16<GradT>(dst + c, v);
+    for (int e = 0; e < D / 4; ++e) {
+        const float4 f = __ldcs(reinterpret_cast<const float4*>(src + static_cast<size_t>(e) * kPlane));
+        v[4 * e] = f.x; v[4 * e + 1] = f.y; v[4 * e + 2] = f.z; v[4 * e + 3] = f.w;
     }
+#pragma unroll
+    for (int c = 0; c < D; c += 16) store_row16<GradT>(dst + c, *reinterpret_cast<const float(*)[16]>(&v[c]));
 }
 
 cudaError_t launch_bwd_prep(const BwdPrepParams& p, fa_dtype o_dtype, cudaStream_t st)
@@ -130,8 +129,17 @@ cudaError_t launch_bwd_dq(const BwdDqParams& p, fa_dtype grad_dtype, cudaStream_
     const long long blocks = (rows + 127) / 128;
     if (blocks <= 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    if (grad_dtype == FA_F32) return launch_pdl(fa_bwd_dq_kernel<float>, static_cast<unsigned>(blocks), 128, 0, st, p);
-    return launch_pdl(fa_bwd_dq_kernel<__nv_bfloat16>, static_cast<unsigned>(blocks), 128, 0, st, p);
+    const unsigned g = static_cast<unsigned>(blocks);
+    const bool f32 = grad_dtype == FA_F32;
+    switch (p.d) {
+    case 32: return f32 ? launch_pdl(fa_bwd_dq_kernel<float, 32>, g, 128, 0, st, p)
+                        : launch_pdl(fa_bwd_dq_kernel<__nv_bfloat16, 32>, g, 128, 0, st, p);
+    case 64: return f32 ? launch_pdl(fa_bwd_dq_kernel<float, 64>, g, 128, 0, st, p)
+                        : launch_pdl(fa_bwd_dq_kernel<__nv_bfloat16, 64>, g, 128, 0, st, p);
+    case 128: return f32 ? launch_pdl(fa_bwd_dq_kernel<float, 128>, g, 128, 0, st, p)
+                         : launch_pdl(fa_bwd_dq_kernel<__nv_bfloat16, 128>, g, 128, 0, st, p);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace fa
